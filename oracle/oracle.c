@@ -1,0 +1,348 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU reference for paged-KV decode and
+ * speculative-verify attention, and for the split-K log-sum-exp merge.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library calls, links or
+ * loads this file; only the test suite, the package's smoke check and the
+ * benchmark's CPU-baseline leg do.  It shares no code, header, table or
+ * constant with the CUDA library.
+ *
+ * What it computes (the plain definition of the method):
+ *   PagedAttention (Kwon et al., "Efficient Memory Management for Large
+ *   Language Model Serving with PagedAttention", cited on "vLLM Fork with
+ *   focus on GB10 Homelabs", section "About"): the keys and values of a
+ *   sequence live in fixed-size physical blocks; logical token t of
+ *   sequence b sits in block  block_tables[b][t / block_size]  at slot
+ *   t % block_size.  Decode attention is exact softmax attention of the new
+ *   query over those keys; "vLLM-SM70", section "Why", checks every kernel
+ *   against such an exact-softmax oracle (fp32 there, fp64 here).
+ *
+ *   For sequence b, query token i < Q and query head h (kv head h / G):
+ *     n   = L_b - Q + 1 + i         (speculative verify: query i sees the
+ *                                    prior context and new tokens 0..i --
+ *                                    the "virtual batch" reading of
+ *                                    "vLLM-SM70", "Why"; decode: n = L_b)
+ *     s_t = scale * sum_d q[d] * k_t[d]          for t < n
+ *     m   = max_t s_t,  w_t = exp(s_t - m)
+ *     o   = sum_t w_t v_t / sum_t w_t,  lse = m + log(sum_t w_t)
+ *   L_b = 0 (a padded row) gives o = 0 and lse = -inf.
+ *
+ *   Split-K ("split-KV merge", "vLLM Fork with focus on GB10 Homelabs",
+ *   "Acknowledgments"): partial results (o_p, lse_p) over disjoint key
+ *   ranges combine as  M = max lse_p,  w_p = exp(lse_p - M),
+ *   o = sum w_p o_p / sum w_p,  lse = M + log sum w_p.
+ *
+ * Storage formats, decoded here from their bit-field definitions:
+ *   bf16  : the fp32 whose upper 16 bits are the code.
+ *   int8  : value = (float)code * (float)scale, scale an IEEE fp16 per
+ *           (token, kv head)  ("vLLM-SM70": int8 KV cache).
+ *   NVFP4 : value = RN_fp32( (e2m1(code) * e4m3(scale)) * g ), one E4M3
+ *           scale per 16 consecutive head-dim elements and one fp32 g per
+ *           cache tensor ("vLLM All-NVFP4 DFlash2 for Blackwell", "What
+ *           makes this stack different": NVFP4 KV cache; UE4M3 block
+ *           scales: "vLLM Fork with focus on GB10 Homelabs",
+ *           "Acknowledgments").  Element 2i of a byte pair is the low
+ *           nibble.  e2m1 * e4m3 is exact in fp32, so the value is one
+ *           fp32 rounding of the product with g -- block scale first.
+ *   The fp32 dequantised value is widened to double for the attention.
+ *
+ * Build: gcc -O2 -std=c11 -fPIC -shared -ffp-contract=off -pthread
+ *        (no fast-math: the fp32 dequant must round exactly once).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { OR_BF16 = 0, OR_INT8 = 1, OR_NVFP4 = 2 };
+
+typedef struct {
+  int32_t dtype;
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  const void *k_cache, *v_cache;
+  const void *k_scale, *v_scale;
+  float k_global, v_global;
+} oracle_cache;
+
+/* ---------------------------------------------------------------- formats */
+
+double oracle_bf16_value(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* IEEE binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+double oracle_fp16_value(uint16_t h) {
+  int s = (h >> 15) & 1, e = (h >> 10) & 0x1f, m = h & 0x3ff;
+  double v;
+  if (e == 0)
+    v = ldexp((double)m, -24);                 /* (m / 2^10) * 2^-14 */
+  else if (e == 31)
+    v = m ? NAN : INFINITY;
+  else
+    v = ldexp((double)(1024 + m), e - 25);     /* (1 + m/2^10) * 2^(e-15) */
+  return s ? -v : v;
+}
+
+/* OCP FP8 E4M3 ("fn" variant): 1 sign, 4 exponent (bias 7), 3 mantissa
+ * bits, no infinities, S.1111.111 is NaN; max 448, min subnormal 2^-9. */
+double oracle_e4m3_value(uint8_t c) {
+  int s = (c >> 7) & 1, e = (c >> 3) & 0xf, m = c & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m, -9);                  /* (m/8) * 2^-6 */
+  else
+    v = ldexp((double)(8 + m), e - 10);        /* (1 + m/8) * 2^(e-7) */
+  return s ? -v : v;
+}
+
+/* OCP FP4 E2M1: 1 sign, 2 exponent (bias 1), 1 mantissa bit. */
+double oracle_e2m1_value(uint8_t c) {
+  int s = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+  double v = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return s ? -v : v;
+}
+
+/* fp32 value of element d of token slot (blk, head, slot); which = 0 K, 1 V */
+static float dequant(const oracle_cache *c, int which, int64_t blk, int head, int slot, int d) {
+  const int64_t row = (blk * c->num_kv_heads + head) * c->block_size + slot;
+  const int D = c->head_dim;
+  const void *data = which ? c->v_cache : c->k_cache;
+  const void *scale = which ? c->v_scale : c->k_scale;
+  switch (c->dtype) {
+    case OR_BF16:
+      return (float)oracle_bf16_value(((const uint16_t *)data)[row * D + d]);
+    case OR_INT8: {
+      float code = (float)((const int8_t *)data)[row * D + d];
+      float s = (float)oracle_fp16_value(((const uint16_t *)scale)[row]);
+      return code * s;
+    }
+    case OR_NVFP4: {
+      uint8_t byte = ((const uint8_t *)data)[row * (D / 2) + d / 2];
+      uint8_t code = (d & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xf);
+      uint8_t sc = ((const uint8_t *)scale)[row * (D / 16) + d / 16];
+      float prod = (float)(oracle_e2m1_value(code) * oracle_e4m3_value(sc));
+      float g = which ? c->v_global : c->k_global;
+      return prod * g;
+    }
+  }
+  return NAN;
+}
+
+/* Dequantised row (D floats) of logical token t of sequence b; returns 0 and
+ * writes zeros if the table entry is out of range. */
+static int token_row(const oracle_cache *c, int which, const int32_t *tables, int32_t stride,
+                     int b, int t, int head, float *out) {
+  int32_t blk = tables[(int64_t)b * stride + t / c->block_size];
+  if (blk < 0 || blk >= c->num_blocks) {
+    for (int d = 0; d < c->head_dim; ++d) out[d] = 0.0f;
+    return 0;
+  }
+  for (int d = 0; d < c->head_dim; ++d)
+    out[d] = dequant(c, which, blk, head, t % c->block_size, d);
+  return 1;
+}
+
+/* Dequantised K and V through the block table, [B, Hkv, max_len, D] fp32;
+ * positions t >= seq_len are zero. */
+void oracle_gather(const oracle_cache *c, const int32_t *tables, int32_t stride,
+                   const int32_t *seq_lens, int32_t B, int32_t max_len, float *k_out, float *v_out) {
+  const int D = c->head_dim, H = c->num_kv_heads;
+  for (int b = 0; b < B; ++b)
+    for (int h = 0; h < H; ++h)
+      for (int t = 0; t < max_len; ++t) {
+        int64_t off = (((int64_t)b * H + h) * max_len + t) * D;
+        if (t < seq_lens[b]) {
+          token_row(c, 0, tables, stride, b, t, h, k_out + off);
+          token_row(c, 1, tables, stride, b, t, h, v_out + off);
+        } else {
+          for (int d = 0; d < D; ++d) k_out[off + d] = v_out[off + d] = 0.0f;
+        }
+      }
+}
+
+/* ------------------------------------------------------------ attention */
+
+typedef struct {
+  const oracle_cache *c;
+  const uint16_t *q;          /* bf16 bits [B, Q, Hq, D] */
+  int32_t B, Q, Hq;
+  const int32_t *tables;
+  int32_t stride;
+  const int32_t *seq_lens;
+  const int32_t *key_begin;   /* optional [B]: first key index considered */
+  const int32_t *key_end;     /* optional [B]: one past the last key considered */
+  double scale;
+  double *out;                /* [B, Q, Hq, D] */
+  double *lse;                /* [B, Q, Hq] */
+  const int32_t *items;       /* optional list of (b, kv_head) pairs */
+  int32_t nitems;
+  int32_t next;               /* shared work counter */
+  pthread_mutex_t mu;
+} attend_job;
+
+static void attend_item(attend_job *J, int b, int kvh, double *scores, float *row, double *acc) {
+  const oracle_cache *c = J->c;
+  const int D = c->head_dim, Q = J->Q, Hq = J->Hq;
+  const int G = Hq / c->num_kv_heads;
+  const int R = Q * G;
+  const int L = J->seq_lens[b];
+  int lo = J->key_begin ? J->key_begin[b] : 0;
+  int hi_all = J->key_end ? J->key_end[b] : L;
+  if (lo < 0) lo = 0;
+  if (hi_all > L) hi_all = L;
+
+  /* query vectors, exact bf16 -> double */
+  double *qv = (double *)malloc(sizeof(double) * (size_t)R * D);
+  int *n = (int *)malloc(sizeof(int) * R);
+  for (int i = 0; i < Q; ++i)
+    for (int g = 0; g < G; ++g) {
+      int h = kvh * G + g, r = i * G + g;
+      const uint16_t *qs = J->q + (((int64_t)b * Q + i) * Hq + h) * D;
+      for (int d = 0; d < D; ++d) qv[(int64_t)r * D + d] = oracle_bf16_value(qs[d]);
+      int lim = L - Q + 1 + i; /* keys visible to query token i */
+      if (L == 0) lim = 0;
+      if (lim > hi_all) lim = hi_all;
+      n[r] = lim;
+    }
+  int tmax = 0;
+  for (int r = 0; r < R; ++r) if (n[r] > tmax) tmax = n[r];
+
+  /* pass 1: scores */
+  for (int t = lo; t < tmax; ++t) {
+    token_row(c, 0, J->tables, J->stride, b, t, kvh, row);
+    for (int r = 0; r < R; ++r) {
+      if (t >= n[r]) continue;
+      double dot = 0.0;
+      for (int d = 0; d < D; ++d) dot += qv[(int64_t)r * D + d] * (double)row[d];
+      scores[(int64_t)r * tmax + t] = J->scale * dot;
+    }
+  }
+  /* pass 2: max */
+  double *mx = (double *)malloc(sizeof(double) * R);
+  double *sum = (double *)malloc(sizeof(double) * R);
+  for (int r = 0; r < R; ++r) {
+    mx[r] = -INFINITY;
+    sum[r] = 0.0;
+    for (int t = lo; t < n[r]; ++t)
+      if (scores[(int64_t)r * tmax + t] > mx[r]) mx[r] = scores[(int64_t)r * tmax + t];
+  }
+  /* pass 3: weights and values */
+  memset(acc, 0, sizeof(double) * (size_t)R * D);
+  for (int t = lo; t < tmax; ++t) {
+    token_row(c, 1, J->tables, J->stride, b, t, kvh, row);
+    for (int r = 0; r < R; ++r) {
+      if (t >= n[r]) continue;
+      double w = exp(scores[(int64_t)r * tmax + t] - mx[r]);
+      sum[r] += w;
+      for (int d = 0; d < D; ++d) acc[(int64_t)r * D + d] += w * (double)row[d];
+    }
+  }
+  for (int i = 0; i < Q; ++i)
+    for (int g = 0; g < G; ++g) {
+      int h = kvh * G + g, r = i * G + g;
+      int64_t o = (((int64_t)b * Q + i) * Hq + h);
+      if (n[r] <= lo || sum[r] == 0.0) {
+        for (int d = 0; d < D; ++d) J->out[o * D + d] = 0.0;
+        J->lse[o] = -INFINITY;
+      } else {
+        for (int d = 0; d < D; ++d) J->out[o * D + d] = acc[(int64_t)r * D + d] / sum[r];
+        J->lse[o] = mx[r] + log(sum[r]);
+      }
+    }
+  free(qv);
+  free(n);
+  free(mx);
+  free(sum);
+}
+
+static void *attend_worker(void *arg) {
+  attend_job *J = (attend_job *)arg;
+  const oracle_cache *c = J->c;
+  const int D = c->head_dim, G = J->Hq / c->num_kv_heads, R = J->Q * G;
+  int lmax = 1;
+  for (int b = 0; b < J->B; ++b) if (J->seq_lens[b] > lmax) lmax = J->seq_lens[b];
+  double *scores = (double *)malloc(sizeof(double) * (size_t)R * lmax);
+  float *row = (float *)malloc(sizeof(float) * D);
+  double *acc = (double *)malloc(sizeof(double) * (size_t)R * D);
+  const int total = J->items ? J->nitems : J->B * c->num_kv_heads;
+  for (;;) {
+    pthread_mutex_lock(&J->mu);
+    int it = J->next++;
+    pthread_mutex_unlock(&J->mu);
+    if (it >= total) break;
+    int b, kvh;
+    if (J->items) {
+      b = J->items[2 * it];
+      kvh = J->items[2 * it + 1];
+    } else {
+      b = it / c->num_kv_heads;
+      kvh = it % c->num_kv_heads;
+    }
+    attend_item(J, b, kvh, scores, row, acc);
+  }
+  free(scores);
+  free(row);
+  free(acc);
+  return NULL;
+}
+
+/* Exact attention for every (b, query token, query head), or only for the
+ * (b, kv head) pairs listed in `items` (nitems pairs) when items != NULL.
+ * key_begin / key_end (optional, [B]) restrict the keys to a sub-range,
+ * which yields the partial (o, lse) of one split.  Returns 0. */
+int oracle_attend(const oracle_cache *c, const uint16_t *q, int32_t B, int32_t Q, int32_t Hq,
+                  const int32_t *tables, int32_t stride, const int32_t *seq_lens,
+                  const int32_t *key_begin, const int32_t *key_end, double scale,
+                  double *out, double *lse, const int32_t *items, int32_t nitems,
+                  int32_t nthreads) {
+  attend_job J;
+  memset(&J, 0, sizeof J);
+  J.c = c; J.q = q; J.B = B; J.Q = Q; J.Hq = Hq; J.tables = tables; J.stride = stride;
+  J.seq_lens = seq_lens; J.key_begin = key_begin; J.key_end = key_end; J.scale = scale;
+  J.out = out; J.lse = lse; J.items = items; J.nitems = nitems; J.next = 0;
+  pthread_mutex_init(&J.mu, NULL);
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  pthread_t th[256];
+  for (int i = 1; i < nthreads; ++i) pthread_create(&th[i], NULL, attend_worker, &J);
+  attend_worker(&J);
+  for (int i = 1; i < nthreads; ++i) pthread_join(th[i], NULL);
+  pthread_mutex_destroy(&J.mu);
+  return 0;
+}
+
+/* Log-sum-exp merge of S partials: part_o [S, R, D], part_lse [S, R]
+ * (-inf marks an empty partial) -> out [R, D], lse [R]. */
+void oracle_merge(const double *part_o, const double *part_lse, int32_t S, int32_t R, int32_t D,
+                  double *out, double *lse) {
+  for (int r = 0; r < R; ++r) {
+    double M = -INFINITY;
+    for (int p = 0; p < S; ++p)
+      if (part_lse[(int64_t)p * R + r] > M) M = part_lse[(int64_t)p * R + r];
+    if (M == -INFINITY) {
+      for (int d = 0; d < D; ++d) out[(int64_t)r * D + d] = 0.0;
+      lse[r] = -INFINITY;
+      continue;
+    }
+    double wsum = 0.0;
+    for (int d = 0; d < D; ++d) out[(int64_t)r * D + d] = 0.0;
+    for (int p = 0; p < S; ++p) {
+      double l = part_lse[(int64_t)p * R + r];
+      if (l == -INFINITY) continue;
+      double w = exp(l - M);
+      wsum += w;
+      for (int d = 0; d < D; ++d)
+        out[(int64_t)r * D + d] += w * part_o[((int64_t)p * R + r) * D + d];
+    }
+    for (int d = 0; d < D; ++d) out[(int64_t)r * D + d] /= wsum;
+    lse[r] = M + log(wsum);
+  }
+}

@@ -1,0 +1,80 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case compiles a copy of ``oracle/oracle.c`` with one planted mistake
+(a dropped term, a wrong sign, a wrong index or bias, a swapped operand)
+into a temporary directory, points the oracle module at it, and requires
+at least one pin of ``test_oracle_pins`` to fail.  Only the CPU runs here.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import tests.test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTANTS = {
+    "nibble_order_swapped": ("(d & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xf)",
+                             "(d & 1) ? (uint8_t)(byte & 0xf) : (uint8_t)(byte >> 4)"),
+    "e4m3_bias_off_by_one": ("v = ldexp((double)(8 + m), e - 10);", "v = ldexp((double)(8 + m), e - 9);"),
+    "e2m1_mantissa_dropped": ("ldexp(1.0 + 0.5 * m, e - 1)", "ldexp(1.0, e - 1)"),
+    "gqa_head_mapping_strided": ("int h = kvh * G + g, r = i * G + g;",
+                                 "int h = g * c->num_kv_heads + kvh, r = i * G + g;"),
+    "causal_offset_off_by_one": ("int lim = L - Q + 1 + i;", "int lim = L - Q + i;"),
+    "softmax_sign_flipped": ("double w = exp(scores[(int64_t)r * tmax + t] - mx[r]);",
+                             "double w = exp(mx[r] - scores[(int64_t)r * tmax + t]);"),
+    "softmax_scale_dropped": ("scores[(int64_t)r * tmax + t] = J->scale * dot;",
+                              "scores[(int64_t)r * tmax + t] = dot;"),
+    "int8_scale_dropped": ("return code * s;", "return code;"),
+    "nvfp4_global_scale_dropped": ("return prod * g;", "return prod;"),
+    "slot_index_shifted": ("token_row(const oracle_cache *c, int which, const int32_t *tables, int32_t stride,\n"
+                           "                     int b, int t, int head, float *out) {\n"
+                           "  int32_t blk = tables[(int64_t)b * stride + t / c->block_size];",
+                           "token_row(const oracle_cache *c, int which, const int32_t *tables, int32_t stride,\n"
+                           "                     int b, int t, int head, float *out) {\n"
+                           "  t = t ^ 1;\n"
+                           "  int32_t blk = tables[(int64_t)b * stride + t / c->block_size];"),
+    "lse_log_dropped": ("J->lse[o] = mx[r] + log(sum[r]);", "J->lse[o] = mx[r] + sum[r];"),
+    "merge_weight_dropped": ("+= w * part_o[((int64_t)p * R + r) * D + d];",
+                             "+= part_o[((int64_t)p * R + r) * D + d];"),
+    "fp16_subnormal_exponent": ("v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
+}
+
+
+def _checks():
+    yield pins.test_fp16_decoder_exhaustive, ()
+    yield pins.test_e4m3_decoder_exhaustive, ()
+    yield pins.test_e2m1_decoder_table, ()
+    for dt in ("bf16", "int8", "nvfp4"):
+        yield pins.test_gather_bit_exact_vs_numpy_decode, (dt,)
+        for Q in (1, 3):
+            yield pins.test_attention_matches_dense_brute_force, (dt, Q)
+    yield pins.test_merge_ignores_empty_partials_and_handles_all_empty, ()
+    yield pins.test_golden_closed_form_examples, ()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
+    mutated = src.replace(old, new)
+    c = tmp_path / "mutant.c"
+    so = tmp_path / "libmutant.so"
+    c.write_text(mutated)
+    subprocess.run(["gcc", "-O1", "-std=gnu11", "-fPIC", "-shared", "-ffp-contract=off",
+                    "-pthread", str(c), "-o", str(so), "-lm"], check=True)
+    oracle.use_library(str(so))
+    caught = []
+    try:
+        for fn, args in _checks():
+            try:
+                fn(*args)
+            except AssertionError:
+                caught.append(fn.__name__)
+                break
+    finally:
+        oracle.use_library(None)
+    assert caught, f"no pin failed for planted mistake {name}"
