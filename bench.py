@@ -1,0 +1,431 @@
+#!/usr/bin/env python3
+"""Benchmark of paged-KV decode attention on GB300.
+
+One step = one pa_decode call (device planner -> attention kernel -> LSE
+merge) over one batch of the synthetic int8 workload: 32 sequences with
+seq_lens uniform in [1024, 32768], 24 query / 4 kv heads, head dim 256,
+int8 KV with per-(token, kv head) fp16 scales, blocks drawn at random from
+a shared pool, bf16 q and out.  Inputs are resident in HBM when timing
+starts; the KV pool (~1.1 GB) is larger than the 129 MB L2, so every step
+streams it from HBM.
+
+Prints ONE JSON line (rank 0).  Metric: achieved algorithmic HBM GB/s
+(KV codes + scales of every valid token, table entries, q and out, divided
+by the step time), with KV tokens/s and % of the measured copy bandwidth
+beside it.  `--impl reference` times the fp64 CPU oracle on a bounded
+sample of the same workload instead (the baseline arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "int8_b32_l1k_32k_d256"
+METRIC = "paged decode attention: achieved HBM GB/s (% of peak) and KV tokens/s, 1×GB300"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def kv_bytes_per_token_head(dtype: str, D: int) -> int:
+    """Bytes of K+V (codes and scales) one token of one kv head occupies."""
+    if dtype == "bf16":
+        return 2 * D * 2
+    if dtype == "int8":
+        return 2 * (D + 2)
+    return 2 * (D // 2 + D // 16)
+
+
+def algorithmic_bytes(spec: dict, seq_lens) -> dict:
+    lens = [int(x) for x in seq_lens]
+    tokens = sum(lens)
+    B, Q, Hq, Hkv, D = spec["B_eff"], spec["Q"], spec["Hq"], spec["Hkv"], spec["D"]
+    kv = tokens * Hkv * kv_bytes_per_token_head(spec["dtype"], D)
+    table = sum((L + 15) // 16 for L in lens) * 4
+    q = B * Q * Hq * D * 2
+    out = B * Q * Hq * D * 2
+    return dict(total=kv + table + q + out, kv=kv, tokens=tokens)
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_decode_07_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """dram bytes per launch of the attention kernel from the committed ncu
+    summary for this workload, or None if absent or taken on other source."""
+    path = os.path.join(ROOT, "profiles", f"decode_{workload}.md")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    vals = {}
+    for ln in lines:
+        if ":" in ln and ln.startswith("- "):
+            k, v = ln[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ln in open(self.path).read().splitlines():
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl != "reference" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available() and args.impl != "reference":
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- oracle
+
+def oracle_sample(wl, bs, nthreads):
+    """Times the fp64 oracle on sequences `bs` of the workload (compact host
+    copy of their blocks).  Returns (seconds, seq_lens of the sample)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    lens = wl.seq_lens.cpu()[bs]
+    nblk = [(int(L) + 15) // 16 for L in lens.tolist()]
+    tabs = wl.block_tables.cpu()
+    ids = torch.cat([tabs[b, :n] for b, n in zip(bs, nblk)]).long().to(wl.k_cache.device)
+
+    def take(t):
+        if t is None:
+            return None
+        a = t[ids].contiguous().cpu()
+        if a.dtype in (torch.bfloat16, torch.float16):
+            return a.view(torch.int16).numpy().view(np.uint16)
+        return a.numpy()
+
+    tab = np.zeros((len(bs), max(nblk)), np.int32)
+    pos = 0
+    for r, n in enumerate(nblk):
+        tab[r, :n] = np.arange(pos, pos + n)
+        pos += n
+    cache = oracle.HostCache(wl.dtype, take(wl.k_cache), take(wl.v_cache), take(wl.k_scale),
+                             take(wl.v_scale), wl.k_global, wl.v_global)
+    qb = wl.q[bs].contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    oracle.attend(cache, qb, tab, lens.numpy().astype(np.int32), wl.softmax_scale,
+                  nthreads=nthreads)
+    return time.perf_counter() - t0, lens.tolist()
+
+
+def pick_sample(seq_lens, budget_tokens):
+    """Deterministic sample: sequences in index order until the token budget."""
+    bs, tot = [], 0
+    for b, L in enumerate(seq_lens):
+        if L <= 0:
+            continue
+        bs.append(b)
+        tot += int(L)
+        if tot >= budget_tokens:
+            break
+    return bs
+
+
+# ------------------------------------------------------------------ arms
+
+def run_reference(args, world, rank):
+    """The baseline arm: the fp64 CPU oracle, each step a bounded sample."""
+    import torch
+
+    from paged_kv_decode_07_gb300 import workloads as W
+    if rank != 0:
+        return
+    spec = W.spec(args.workload)
+    full_lens = W.make_seq_lens(spec["lens"], spec["B"], torch.Generator().manual_seed(1000 + spec["id"]))
+    bs = pick_sample(full_lens.tolist(), args.ref_tokens)
+    sample_lens = [int(full_lens[b]) for b in bs]
+    wl = W.make_workload(args.workload, device="cpu", seq_lens=sample_lens)
+    nthreads = os.cpu_count() or 1
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt, _ = oracle_sample(wl, list(range(len(bs))), nthreads)
+        if i >= args.warmup:
+            times.append(dt)
+    sp = dict(spec, B_eff=len(bs))
+    ab = algorithmic_bytes(sp, sample_lens)
+    sec = sum(times) / len(times)
+    value = ab["total"] / sec / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "impl": "reference",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "sample_sequences": len(bs),
+                   "sample_tokens": ab["tokens"]},
+        "kv_tokens_per_s": ab["tokens"] / sec,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+                         "sample": f"{len(bs)} of {spec['B']} sequences ({ab['tokens']} keys) "
+                                   f"of {args.workload}, fp64 two-pass softmax"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    from paged_kv_decode_07_gb300 import pa
+    from paged_kv_decode_07_gb300 import workloads as W
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    spec = W.spec(args.workload)
+    # weak scaling: every rank runs its own full batch (different seed)
+    wl = W.make_workload(args.workload, device=dev, seed=1000 + spec["id"] + 7919 * rank)
+    kv = pa.KvCache.from_workload(wl)
+    lens = wl.seq_lens.cpu().tolist()
+    sp = dict(spec, B_eff=wl.B)
+    ab = algorithmic_bytes(sp, lens)
+    fn = "pa_verify" if wl.Q > 1 else "pa_decode"
+    out = torch.empty((wl.B, wl.Q, wl.Hq, wl.D), dtype=torch.bfloat16, device=dev)
+    maxlen = wl.max_seq_len()
+    ws_bytes = pa.workspace_bytes(kv, wl.B, wl.Q, wl.Hq, maxlen, kernel=args.kernel)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    call = pa.verify if wl.Q > 1 else pa.decode
+
+    def step(events=None, q=None, tables=None, seq_lens=None):
+        call(kv, wl.q if q is None else q, wl.block_tables if tables is None else tables,
+             wl.seq_lens if seq_lens is None else seq_lens, wl.softmax_scale, out=out,
+             max_seq_len=maxlen, workspace=ws, kernel=args.kernel, events=events)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    flags = pa.read_error(ws)
+    if flags:
+        raise RuntimeError(f"device error flags {flags:#x}")
+
+    # ---- device-timed region: inputs resident
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(events=kev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = t0.elapsed_time(t1)
+    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    ms_step = max_over_ranks(total_ms / args.steps, world)
+    kern_avg = max_over_ranks(sum(kern_ms) / len(kern_ms), world)
+    launches = 3 * args.steps    # planner, attention kernel, merge per step
+
+    # ---- end-to-end: pinned host inputs copied in, output copied out, every step
+    e2e = None
+    if not args.no_e2e:
+        hq = wl.q.cpu().pin_memory()
+        ht = wl.block_tables.cpu().pin_memory()
+        hl = wl.seq_lens.cpu().pin_memory()
+        dq, dt_, dl = torch.empty_like(wl.q), torch.empty_like(wl.block_tables), torch.empty_like(wl.seq_lens)
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = hq.numel() * hq.element_size() + ht.numel() * 4 + hl.numel() * 4
+        d2h = hout.numel() * hout.element_size()
+        for _ in range(2):
+            dq.copy_(hq, non_blocking=True)
+            dt_.copy_(ht, non_blocking=True)
+            dl.copy_(hl, non_blocking=True)
+            step(q=dq, tables=dt_, seq_lens=dl)
+            hout.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        barrier(world)
+        s0 = time.perf_counter()
+        for _ in range(args.steps):
+            dq.copy_(hq, non_blocking=True)
+            dt_.copy_(ht, non_blocking=True)
+            dl.copy_(hl, non_blocking=True)
+            step(q=dq, tables=dt_, seq_lens=dl)
+            hout.copy_(out, non_blocking=True)
+            torch.cuda.current_stream().synchronize()   # the host reads the result each step
+        e2e_s = max_over_ranks((time.perf_counter() - s0) / args.steps, world)
+        e2e = {"value": world * ab["total"] / e2e_s / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_s * 1e3,
+               "resident": "KV pool (cache state, written by prefill/append)"}
+
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    value = world * ab["total"] / (ms_step * 1e-3) / 1e9
+    achieved = ab["total"] / (kern_avg * 1e-3) / 1e9
+    traffic = profiled_traffic(args.workload) if args.kernel in (0,) else None
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import numpy as np  # noqa: F401
+        nthreads = os.cpu_count() or 1
+        bs = pick_sample(lens, args.cpu_tokens)
+        dt, slens = oracle_sample(wl, bs, nthreads)
+        cab = algorithmic_bytes(dict(spec, B_eff=len(bs)), slens)
+        cpu = {"value": cab["total"] / dt / 1e9, "unit": "GB/s", "cores": nthreads,
+               "kind": "oracle",
+               "sample": f"{len(bs)} of {wl.B} sequences ({cab['tokens']} keys) of "
+                         f"{args.workload}, fp64 two-pass softmax, {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": {"bf16": "bf16", "int8": "int8", "nvfp4": "nvfp4"}[wl.dtype] + "-kv/fp32-acc",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "batch": wl.B, "q_len": wl.Q,
+                       "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": wl.D,
+                       "kv_tokens": ab["tokens"], "algorithmic_bytes": ab["total"],
+                       "l2": "inputs larger than L2 (KV pool %.2f GB > 129 MB)" % (ab["kv"] / 1e9),
+                       "parallelism": f"replicas x{world}, no collective"},
+            "kv_tokens_per_s": world * ab["tokens"] / (ms_step * 1e-3),
+            "pct_of_peak": 100.0 * value / world / peak,
+            "peak_gbs": peak, "peak_kind": peak_kind,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel_ms": kern_avg, "kernel": f"{fn} attention kernel",
+                         "peak_kind": peak_kind},
+            "gpu_launches": launches,
+            "clocks": clk,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-tokens", type=int, default=60000,
+                    help="keys in the oracle's bounded sample")
+    ap.add_argument("--cpu-tokens", type=int, default=1 << 40,
+                    help="keys in the cpu_baseline sample (default: the whole workload)")
+    args = ap.parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,189 @@
+/*
+ * pa.h -- C ABI of the GB300 (sm_103a) paged-KV decode attention library.
+ *
+ * The operation (PagedAttention decode; Kwon et al., "Efficient Memory
+ * Management for Large Language Model Serving with PagedAttention", cited
+ * on "vLLM Fork with focus on GB10 Homelabs", section "About"): each
+ * sequence b owns a list of fixed-size physical KV blocks; logical token t
+ * lives in block  block_tables[b][t / 16]  at slot  t % 16.  For every
+ * query token i < q_len and query head h (kv head h / G, G = Hq / Hkv):
+ *
+ *     n   = seq_lens[b] - q_len + 1 + i        (keys visible to query i)
+ *     s_t = softmax_scale * <q[b,i,h,:], K_t>  for t < n
+ *     out[b,i,h,:] = sum_t exp(s_t - m) V_t / sum_t exp(s_t - m),  m = max s
+ *     lse[b,i,h]   = m + ln sum_t exp(s_t - m)          (natural log)
+ *
+ * q_len = 1 is decode.  q_len > 1 is speculative verify: the q_len new
+ * tokens are the last q_len keys already written to the cache and each
+ * sees the prior context plus the new tokens up to itself (the "virtual
+ * batch for speculative positions" of "vLLM-SM70", section "Why"; 8 query
+ * tokens = DFlash2 K=7 on "vLLM All-NVFP4 DFlash2 for Blackwell", section
+ * "What makes this stack different").  Keys are split into partitions that
+ * run in parallel and are combined with a log-sum-exp merge ("split-KV
+ * merge", "vLLM Fork with focus on GB10 Homelabs", "Acknowledgments").
+ *
+ * KV storage formats (dequantised in registers inside the kernels):
+ *   PA_KV_BF16  : k/v bf16 [NB, Hkv, 16, D]; no scales.
+ *   PA_KV_INT8  : k/v int8 [NB, Hkv, 16, D]; k/v_scale fp16 [NB, Hkv, 16]
+ *                 (one scale per token and kv head); value = code * scale
+ *                 ("vLLM-SM70", "Why": int8 KV cache).
+ *   PA_KV_NVFP4 : k/v uint8 [NB, Hkv, 16, D/2], E2M1 codes, element 2i in
+ *                 the low nibble; k/v_scale uint8 [NB, Hkv, 16, D/16], one
+ *                 FP8-E4M3 scale per 16 consecutive head-dim elements;
+ *                 k/v_global_scale fp32 per tensor; value =
+ *                 (e2m1(code) * e4m3(scale)) * global  ("vLLM All-NVFP4
+ *                 DFlash2 for Blackwell", "What makes this stack
+ *                 different": NVFP4 KV cache; UE4M3 block scales: "vLLM
+ *                 Fork with focus on GB10 Homelabs", "Acknowledgments").
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers unless marked (host).  Every data
+ *     pointer must be 16-byte aligned.  The caller owns every buffer; the
+ *     library never allocates, never synchronises (except pa_read_error)
+ *     and keeps no state between calls: it is reentrant and thread-safe,
+ *     and a call can be captured in a CUDA graph (no host reads of device
+ *     data; the split plan is computed on the device).
+ *   - All work is enqueued asynchronously on `stream` (NULL = legacy
+ *     default stream).
+ *   - Argument errors are detected on the host and return a negative
+ *     pa_status with NOTHING launched.  A failed launch returns
+ *     PA_ERR_CUDA.
+ *   - Errors that only the device can see (a block-table entry outside
+ *     [0, num_blocks), seq_len < 0 or beyond the table's capacity, a
+ *     verify row with seq_len < q_len) never trap: the offending block is
+ *     skipped or the length clamped, and a bit is set in the workspace
+ *     header, which pa_read_error returns.  The flags describe the most
+ *     recent pa_decode / pa_verify call that used the workspace.
+ *   - seq_lens[b] = 0 marks a padded row: its outputs are 0 and lse -inf.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *pa_stream_t;   /* same type as cudaStream_t */
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = -1,          /* null pointer, bad size, misalignment */
+  PA_ERR_UNSUPPORTED = -2,          /* head_dim, block_size, G or q_len not built */
+  PA_ERR_WORKSPACE_TOO_SMALL = -3,  /* ws_bytes < pa_workspace_bytes(...) */
+  PA_ERR_CUDA = -4                  /* a CUDA runtime call or launch failed */
+} pa_status;
+
+typedef enum { PA_KV_BF16 = 0, PA_KV_INT8 = 1, PA_KV_NVFP4 = 2 } pa_kv_dtype;
+
+/* Device error flags (pa_read_error). */
+#define PA_ERRF_BAD_BLOCK_ID      0x1u  /* table entry outside [0, num_blocks): block skipped */
+#define PA_ERRF_LEN_OVER_CAPACITY 0x2u  /* seq_len > 16 * block_table_stride: clamped */
+#define PA_ERRF_NEG_LEN           0x4u  /* seq_len < 0: treated as 0 */
+#define PA_ERRF_LEN_LT_QLEN       0x8u  /* verify: 0 < seq_len < q_len: rows with no key get 0 */
+#define PA_ERRF_WAIT_TIMEOUT      0x10u /* an in-kernel wait hit its iteration cap: outputs invalid */
+#define PA_ERRF_PLAN_OVERFLOW     0x20u /* the split plan did not fit the workspace: nothing computed */
+
+/* The paged KV pool.  block_size must be 16; head_dim 128 or 256. */
+typedef struct pa_kv_cache {
+  int32_t dtype;          /* pa_kv_dtype */
+  int32_t num_blocks;     /* NB, physical blocks in the pool */
+  int32_t block_size;     /* tokens per block (16) */
+  int32_t num_kv_heads;   /* Hkv */
+  int32_t head_dim;       /* D */
+  const void *k_cache;    /* layouts: see the format list above */
+  const void *v_cache;
+  const void *k_scale;    /* NULL for bf16 */
+  const void *v_scale;
+  float k_global_scale;   /* (host) NVFP4 per-tensor scale; ignored otherwise */
+  float v_global_scale;
+} pa_kv_cache;
+
+/* One batched call. */
+typedef struct pa_problem {
+  int32_t batch;               /* B >= 0 */
+  int32_t num_q_heads;         /* Hq, a multiple of num_kv_heads; Hq / Hkv <= 8 */
+  int32_t q_len;               /* 1 for pa_decode; 1..16 for pa_verify */
+  const void *q;               /* bf16 [B, q_len, Hq, D] */
+  const int32_t *block_tables; /* int32 [B, block_table_stride] physical block ids */
+  int32_t block_table_stride;  /* >= 1 entries per row; capacity = 16 * stride tokens */
+  const int32_t *seq_lens;     /* int32 [B] keys in the cache per sequence, including
+                                  the q_len new ones; 0 = padded row */
+  int32_t max_seq_len;         /* (host) upper bound of seq_lens, sizes the workspace */
+  float softmax_scale;         /* multiplies q.k, e.g. 1/sqrt(D) */
+  void *out;                   /* bf16 (or fp32 if out_fp32) [B, q_len, Hq, D] */
+  int32_t out_fp32;            /* 0: bf16 round-to-nearest-even output; 1: fp32 */
+  float *lse_out;              /* optional fp32 [B, q_len, Hq] natural-log LSE, or NULL */
+} pa_problem;
+
+/* Optional knobs; pass NULL for defaults. */
+typedef struct pa_options {
+  int32_t kernel;          /* 0 auto; 1 CUDA-core (SIMT) kernel; 2 tensor-core kernel */
+  int32_t split_blocks;    /* 0 auto; >0 = fixed number of 16-token blocks per partition
+                              (a value >= the longest sequence's block count disables
+                              split-K) */
+  int32_t target_items;    /* 0 auto; >0 = aim for about this many work items */
+  void *event_begin;       /* optional cudaEvent_t recorded just before the attention
+                              kernel (after the planner) -- for timing that kernel */
+  void *event_end;         /* optional cudaEvent_t recorded just after it */
+} pa_options;
+
+/* Bytes of device workspace a pa_decode / pa_verify call with these
+ * arguments needs (an upper bound computed from batch, q_len, heads and
+ * max_seq_len only).  The workspace needs no initialisation; it may be
+ * reused by consecutive calls on the same stream, never by two calls that
+ * can run at the same time.  Returns 0 on invalid arguments. */
+size_t pa_workspace_bytes(const pa_kv_cache *kv, const pa_problem *prob, const pa_options *opt);
+
+/* Decode (q_len == 1): out = attention of q over the paged cache.
+ * ws: device workspace of ws_bytes >= pa_workspace_bytes(...). */
+int pa_decode(const pa_kv_cache *kv, const pa_problem *prob, const pa_options *opt,
+              void *ws, size_t ws_bytes, pa_stream_t stream);
+
+/* Speculative verify (1 <= q_len <= 16), causal among the q_len new tokens
+ * (query i sees keys t < seq_len - q_len + 1 + i).  Requires seq_len >=
+ * q_len or 0; other rows set PA_ERRF_LEN_LT_QLEN. */
+int pa_verify(const pa_kv_cache *kv, const pa_problem *prob, const pa_options *opt,
+              void *ws, size_t ws_bytes, pa_stream_t stream);
+
+/* Log-sum-exp merge of S partial attention results over disjoint key sets
+ * (split-KV merge, "vLLM Fork with focus on GB10 Homelabs",
+ * "Acknowledgments"):
+ *   part_out fp32 [S, R, D] (each partial normalised by its own weights),
+ *   part_lse fp32 [S, R] natural-log LSE, -inf marks an empty partial.
+ *   out[r,:] = sum_p exp(lse_p - M) part_out[p,r,:] / sum_p exp(lse_p - M),
+ *   M = max_p lse_p;  lse_out[r] = M + ln sum_p exp(lse_p - M) (optional).
+ * A row whose partials are all empty gets 0 and -inf.  out is bf16 or
+ * fp32 (out_fp32) [R, D].  D <= 1024, a multiple of 4. */
+int pa_merge(const float *part_out, const float *part_lse, int32_t S, int32_t R, int32_t D,
+             void *out, int32_t out_fp32, float *lse_out, pa_stream_t stream);
+
+/* Debug: gathers through the block table and dequantises exactly as the
+ * attention kernels do, writing fp32 k_out / v_out [B, Hkv, max_seq_len, D]
+ * (positions t >= seq_len, and blocks with an out-of-range id, are 0).
+ * The values are bit-exact: bf16 widened; int8 (float)code * (float)scale;
+ * NVFP4 fp32_round((e2m1 * e4m3) * global).  ws may be NULL; if given (>=
+ * 256 bytes) its header receives the device error flags. */
+int pa_dequant_gather(const pa_kv_cache *kv, const int32_t *block_tables,
+                      int32_t block_table_stride, const int32_t *seq_lens, int32_t batch,
+                      int32_t max_seq_len, float *k_out, float *v_out, void *ws,
+                      pa_stream_t stream);
+
+/* Copies the device error flags (PA_ERRF_*) of the last call that used ws
+ * to *host_flags (host).  Synchronises `stream`. */
+int pa_read_error(const void *ws, uint32_t *host_flags, pa_stream_t stream);
+
+/* Human-readable name of a pa_status value (static string). */
+const char *pa_status_string(int status);
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -8,15 +8,16 @@ the CUDA library.  Calling any entry point without the built library raises.
 """
 from __future__ import annotations
 
-__all__ = ["pa", "workloads"]
+import importlib
+
+_SUBMODULES = ("pa", "workloads", "build")
+_API = ("decode", "verify", "merge", "dequant_gather", "workspace_bytes", "read_error",
+        "status_string", "KvCache", "PaError", "library_path")
 
 
 def __getattr__(name):
-    if name in ("pa", "workloads"):
-        import importlib
+    if name in _SUBMODULES:
         return importlib.import_module(f"{__name__}.{name}")
-    # convenience: paged_kv_decode_07_gb300.decode(...) etc.
-    from . import pa as _pa
-    if hasattr(_pa, name):
-        return getattr(_pa, name)
+    if name in _API:
+        return getattr(importlib.import_module(f"{__name__}.pa"), name)
     raise AttributeError(name)

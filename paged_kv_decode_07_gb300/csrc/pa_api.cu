@@ -1,0 +1,304 @@
+// pa_api.cu -- host side of the C ABI declared in include/pa.h: argument
+// validation (errors return before anything is launched), workspace layout,
+// and the planner -> attention kernel -> merge launch sequence.
+#include <cmath>
+#include <cstring>
+
+#include "pa_internal.cuh"
+
+namespace pa {
+cudaError_t launch_decode_simt_bf16(const AttnParams &p, int grid, cudaStream_t s);
+cudaError_t launch_decode_simt_int8(const AttnParams &p, int grid, cudaStream_t s);
+cudaError_t launch_decode_simt_nvfp4(const AttnParams &p, int grid, cudaStream_t s);
+
+cudaError_t launch_decode_simt(const AttnParams &p, int grid, cudaStream_t s) {
+  switch (p.kv.dtype) {
+    case PA_KV_BF16: return launch_decode_simt_bf16(p, grid, s);
+    case PA_KV_INT8: return launch_decode_simt_int8(p, grid, s);
+    case PA_KV_NVFP4: return launch_decode_simt_nvfp4(p, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+int simt_supported(int dtype, int D, int R) {
+  (void)dtype;
+  return (D == 128 || D == 256) && (R == 1 || R == 2 || R == 4 || R == 6 || R == 8);
+}
+}  // namespace pa
+
+using namespace pa;
+
+namespace {
+
+constexpr int kVersion = 100;
+constexpr int kMinSplitBlocks = 8;       // partitions never shorter than 128 tokens (auto mode)
+constexpr size_t kAlign = 256;
+
+size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+struct Layout {
+  size_t hdr = 0, units = 0, prefix_a = 0, prefix_b = 0, items = 0, part_lse = 0, part_o = 0;
+  size_t total = 0;
+  int U = 0, R = 0, max_items = 0, max_slots = 0;
+};
+
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+// Workspace regions for one plan mode.  `target` is the item target the
+// call uses (auto: the maximum, so the bound holds for any choice).
+Layout make_layout(const pa_kv_cache *kv, const pa_problem *p, const pa_options *o, bool virt) {
+  Layout L;
+  const int B = p->batch, Q = p->q_len, Hkv = kv->num_kv_heads;
+  const int G = p->num_q_heads / Hkv;
+  L.U = virt ? B * Q : B;
+  L.R = virt ? G : Q * G;
+  const int maxblk = ceil_div(std::max(p->max_seq_len, 0), kBlock);
+  long long items, slots;
+  if (o && o->split_blocks > 0) {
+    const long long parts = std::max(1, ceil_div(maxblk, o->split_blocks));
+    items = (long long)Hkv * L.U * parts;
+    slots = (long long)L.U * parts;
+  } else {
+    const int target = (o && o->target_items > 0) ? std::min(o->target_items, kMaxTargetItems)
+                                                  : kMaxTargetItems;
+    items = (long long)target + (long long)Hkv * L.U;
+    slots = (long long)ceil_div(target, Hkv) + L.U + 1;
+    // never more partitions than blocks
+    items = std::min(items, (long long)Hkv * L.U * std::max(1, maxblk));
+    slots = std::min(slots, (long long)L.U * std::max(1, maxblk));
+  }
+  L.max_items = (int)std::min<long long>(items, 1LL << 30);
+  L.max_slots = (int)std::min<long long>(slots, 1LL << 30);
+  size_t off = 0;
+  L.hdr = off;
+  off += up(kHdrWords * 4);
+  L.units = off;
+  off += up((size_t)L.U * sizeof(UnitInfo));
+  L.prefix_a = off;
+  off += up((size_t)L.U * 4);
+  L.prefix_b = off;
+  off += up((size_t)L.U * 4);
+  L.items = off;
+  off += up((size_t)L.max_items * sizeof(WorkItem));
+  L.part_lse = off;
+  off += up((size_t)L.max_slots * Hkv * L.R * 4);
+  L.part_o = off;
+  off += up((size_t)L.max_slots * Hkv * L.R * kv->head_dim * 4);
+  L.total = off;
+  return L;
+}
+
+int check_kv(const pa_kv_cache *kv) {
+  if (!kv) return PA_ERR_INVALID_ARG;
+  if (kv->dtype < PA_KV_BF16 || kv->dtype > PA_KV_NVFP4) return PA_ERR_INVALID_ARG;
+  if (kv->block_size != kBlock) return PA_ERR_UNSUPPORTED;
+  if (kv->head_dim != 128 && kv->head_dim != 256) return PA_ERR_UNSUPPORTED;
+  if (kv->num_kv_heads < 1 || kv->num_blocks < 1) return PA_ERR_INVALID_ARG;
+  if (!kv->k_cache || !kv->v_cache) return PA_ERR_INVALID_ARG;
+  if (!aligned16(kv->k_cache) || !aligned16(kv->v_cache)) return PA_ERR_INVALID_ARG;
+  if (kv->dtype != PA_KV_BF16) {
+    if (!kv->k_scale || !kv->v_scale) return PA_ERR_INVALID_ARG;
+    if (!aligned16(kv->k_scale) || !aligned16(kv->v_scale)) return PA_ERR_INVALID_ARG;
+  }
+  if (kv->dtype == PA_KV_NVFP4 &&
+      (!std::isfinite(kv->k_global_scale) || !std::isfinite(kv->v_global_scale)))
+    return PA_ERR_INVALID_ARG;
+  return PA_OK;
+}
+
+int check_problem(const pa_kv_cache *kv, const pa_problem *p, int max_qlen) {
+  if (!p) return PA_ERR_INVALID_ARG;
+  if (p->batch < 0 || p->q_len < 1 || p->max_seq_len < 0) return PA_ERR_INVALID_ARG;
+  if (p->q_len > max_qlen) return PA_ERR_UNSUPPORTED;
+  if (p->num_q_heads < 1 || p->num_q_heads % kv->num_kv_heads) return PA_ERR_INVALID_ARG;
+  const int G = p->num_q_heads / kv->num_kv_heads;
+  if (G > kMaxG) return PA_ERR_UNSUPPORTED;
+  if (!std::isfinite(p->softmax_scale)) return PA_ERR_INVALID_ARG;
+  if (p->batch == 0) return PA_OK;
+  if (!p->q || !p->block_tables || !p->seq_lens || !p->out) return PA_ERR_INVALID_ARG;
+  if (p->block_table_stride < 1) return PA_ERR_INVALID_ARG;
+  if (!aligned16(p->q) || !aligned16(p->out)) return PA_ERR_INVALID_ARG;
+  if (!aligned4(p->block_tables) || !aligned4(p->seq_lens)) return PA_ERR_INVALID_ARG;
+  if (p->lse_out && !aligned4(p->lse_out)) return PA_ERR_INVALID_ARG;
+  if ((long long)p->batch * p->q_len * p->num_q_heads > (1LL << 30)) return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+KvView view_of(const pa_kv_cache *kv) {
+  KvView v;
+  v.dtype = kv->dtype;
+  v.num_blocks = kv->num_blocks;
+  v.hkv = kv->num_kv_heads;
+  v.D = kv->head_dim;
+  v.k = kv->k_cache;
+  v.v = kv->v_cache;
+  v.ks = kv->k_scale;
+  v.vs = kv->v_scale;
+  v.kg = kv->dtype == PA_KV_NVFP4 ? kv->k_global_scale : 1.0f;
+  v.vg = kv->dtype == PA_KV_NVFP4 ? kv->v_global_scale : 1.0f;
+  return v;
+}
+
+int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *o, void *ws,
+                  size_t ws_bytes, cudaStream_t stream, bool verify) {
+  int st = check_kv(kv);
+  if (st) return st;
+  st = check_problem(kv, p, verify ? kMaxQLen : 1);
+  if (st) return st;
+  const int kernel = o ? o->kernel : 0;
+  if (kernel < 0 || kernel > 2) return PA_ERR_INVALID_ARG;
+  if (o && (o->split_blocks < 0 || o->target_items < 0)) return PA_ERR_INVALID_ARG;
+  if (p->batch == 0) return PA_OK;
+  const int G = p->num_q_heads / kv->num_kv_heads;
+  // the CUDA-core kernel runs verify as a virtual batch (one unit per query
+  // token); it is the only kernel built so far
+  if (kernel == 2) return PA_ERR_UNSUPPORTED;
+  const bool virt = true;
+  if (!simt_supported(kv->dtype, kv->head_dim, G)) return PA_ERR_UNSUPPORTED;
+  if (!ws) return PA_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return PA_ERR_INVALID_ARG;
+  const Layout L = make_layout(kv, p, o, virt);
+  if (ws_bytes < L.total) return PA_ERR_WORKSPACE_TOO_SMALL;
+
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  PlanParams pp;
+  std::memset(&pp, 0, sizeof pp);
+  pp.seq_lens = p->seq_lens;
+  pp.B = p->batch;
+  pp.Q = p->q_len;
+  pp.virt = virt;
+  pp.hkv = kv->num_kv_heads;
+  pp.capacity = (int)std::min<long long>((long long)p->block_table_stride * kBlock, 1LL << 30);
+  pp.target_items = (o && o->target_items > 0) ? std::min(o->target_items, kMaxTargetItems) : 1184;
+  pp.split_blocks = o ? o->split_blocks : 0;
+  pp.min_split_blocks = kMinSplitBlocks;
+  pp.max_items = L.max_items;
+  pp.max_slots = L.max_slots;
+  pp.hdr = reinterpret_cast<uint32_t *>(w + L.hdr);
+  pp.items = reinterpret_cast<WorkItem *>(w + L.items);
+  pp.units = reinterpret_cast<UnitInfo *>(w + L.units);
+  pp.prefix_a = reinterpret_cast<int *>(w + L.prefix_a);
+  pp.prefix_b = reinterpret_cast<int *>(w + L.prefix_b);
+
+  AttnParams ap;
+  std::memset(&ap, 0, sizeof ap);
+  ap.kv = view_of(kv);
+  ap.q = static_cast<const __nv_bfloat16 *>(p->q);
+  ap.B = p->batch;
+  ap.Q = p->q_len;
+  ap.Hq = p->num_q_heads;
+  ap.G = G;
+  ap.tables = p->block_tables;
+  ap.stride = p->block_table_stride;
+  ap.seq_lens = p->seq_lens;
+  ap.scale_log2 = p->softmax_scale * 1.4426950408889634f;
+  ap.out = p->out;
+  ap.out_fp32 = p->out_fp32 ? 1 : 0;
+  ap.lse_out = p->lse_out;
+  ap.hdr = pp.hdr;
+  ap.items = pp.items;
+  ap.units = pp.units;
+  ap.part_o = reinterpret_cast<float *>(w + L.part_o);
+  ap.part_lse = reinterpret_cast<float *>(w + L.part_lse);
+  ap.max_items = L.max_items;
+  ap.max_slots = L.max_slots;
+  ap.virt = virt;
+  ap.R = L.R;
+
+  if (launch_plan(pp, stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (o && o->event_begin &&
+      cudaEventRecord(static_cast<cudaEvent_t>(o->event_begin), stream) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (launch_decode_simt(ap, L.max_items, stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (o && o->event_end &&
+      cudaEventRecord(static_cast<cudaEvent_t>(o->event_end), stream) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (launch_merge_plan(ap, stream) != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pa_workspace_bytes(const pa_kv_cache *kv, const pa_problem *prob, const pa_options *opt) {
+  if (check_kv(kv) != PA_OK || !prob) return 0;
+  if (prob->batch < 0 || prob->q_len < 1 || prob->q_len > kMaxQLen || prob->max_seq_len < 0)
+    return 0;
+  if (prob->num_q_heads < 1 || prob->num_q_heads % kv->num_kv_heads) return 0;
+  if (opt && (opt->split_blocks < 0 || opt->target_items < 0)) return 0;
+  const Layout a = make_layout(kv, prob, opt, true);
+  const Layout b = make_layout(kv, prob, opt, false);
+  return std::max(a.total, b.total);
+}
+
+int pa_decode(const pa_kv_cache *kv, const pa_problem *prob, const pa_options *opt, void *ws,
+              size_t ws_bytes, pa_stream_t stream) {
+  return run_attention(kv, prob, opt, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+int pa_verify(const pa_kv_cache *kv, const pa_problem *prob, const pa_options *opt, void *ws,
+              size_t ws_bytes, pa_stream_t stream) {
+  return run_attention(kv, prob, opt, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+int pa_merge(const float *part_out, const float *part_lse, int32_t S, int32_t R, int32_t D,
+             void *out, int32_t out_fp32, float *lse_out, pa_stream_t stream) {
+  if (S < 0 || R < 0 || D < 4 || D % 4) return PA_ERR_INVALID_ARG;
+  if (R == 0) return PA_OK;
+  if (!out || (S > 0 && (!part_out || !part_lse))) return PA_ERR_INVALID_ARG;
+  if (!aligned16(out) || (part_out && !aligned16(part_out)) || (part_lse && !aligned4(part_lse)))
+    return PA_ERR_INVALID_ARG;
+  if (lse_out && !aligned4(lse_out)) return PA_ERR_INVALID_ARG;
+  if (launch_merge_dense(part_out, part_lse, S, R, D, out, out_fp32 ? 1 : 0, lse_out,
+                         reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+int pa_dequant_gather(const pa_kv_cache *kv, const int32_t *block_tables, int32_t stride,
+                      const int32_t *seq_lens, int32_t batch, int32_t max_seq_len, float *k_out,
+                      float *v_out, void *ws, pa_stream_t stream) {
+  int st = check_kv(kv);
+  if (st) return st;
+  if (batch < 0 || max_seq_len < 0) return PA_ERR_INVALID_ARG;
+  if (batch == 0 || max_seq_len == 0) return PA_OK;
+  if (!block_tables || !seq_lens || !k_out || !v_out || stride < 1) return PA_ERR_INVALID_ARG;
+  if (!aligned16(k_out) || !aligned16(v_out) || !aligned4(block_tables) || !aligned4(seq_lens))
+    return PA_ERR_INVALID_ARG;
+  if (ws && !aligned16(ws)) return PA_ERR_INVALID_ARG;
+  uint32_t *hdr = static_cast<uint32_t *>(ws);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (hdr && cudaMemsetAsync(hdr, 0, 4, s) != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_gather(view_of(kv), block_tables, stride, seq_lens, batch, max_seq_len, k_out, v_out,
+                    hdr, s) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+int pa_read_error(const void *ws, uint32_t *host_flags, pa_stream_t stream) {
+  if (!ws || !host_flags) return PA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(host_flags, ws, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+const char *pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_WORKSPACE_TOO_SMALL: return "PA_ERR_WORKSPACE_TOO_SMALL";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+  }
+  return "PA_UNKNOWN_STATUS";
+}
+
+int pa_version(void) { return kVersion; }
+
+}  // extern "C"

@@ -1,0 +1,222 @@
+// pa_plan.cu -- device-side split-K planner.
+//
+// Splits every sequence's keys into partitions of whole 16-token blocks so
+// that partitions of all sequences run in parallel across the SMs
+// (flash-decoding; "split-KV merge", "vLLM Fork with focus on GB10
+// Homelabs", "Acknowledgments").  Like stream-K scheduling ("SM120 Stream-K
+// Decode Optimization" on the same page), the K dimension of a small-M
+// problem is what gets spread across SMs; here it is the key axis.
+//
+// One CTA of 1024 threads reads seq_lens on the device (no host read, so a
+// call can be captured in a CUDA graph) and writes:
+//   units[u]  = {parts, slot_base, nblk, len}
+//   items[j]  = {unit, kvh, blk_begin, blk_end, part, parts, slot}
+// Partition size W (blocks) = max(min_split, ceil(total_blocks * Hkv /
+// target_items)) unless fixed by the caller; parts_u = ceil(nblk_u / W);
+// blocks are split evenly, ceil(nblk_u / parts_u) per part (never empty).
+// Items of multi-part units come first (they are about W blocks each), then
+// the single-part ones (shorter), a longest-first order for the hardware's
+// in-order CTA dispatch.
+#include "pa_internal.cuh"
+
+namespace pa {
+
+namespace {
+
+constexpr int kThreads = 1024;
+
+__device__ __forceinline__ int unit_len(const PlanParams &p, int u, uint32_t &err) {
+  int b = p.virt ? u / p.Q : u;
+  int i = p.virt ? u % p.Q : p.Q - 1;
+  int L = p.seq_lens[b];
+  if (L < 0) {
+    err |= PA_ERRF_NEG_LEN;
+    L = 0;
+  }
+  if (L > p.capacity) {
+    err |= PA_ERRF_LEN_OVER_CAPACITY;
+    L = p.capacity;
+  }
+  if (L > 0 && L < p.Q) err |= PA_ERRF_LEN_LT_QLEN;
+  if (L == 0) return 0;
+  int n = L - p.Q + 1 + i;  // keys visible to the unit's last row
+  return n > 0 ? n : 0;
+}
+
+// exclusive block-wide scan of a pair of ints; returns totals in tot
+__device__ __forceinline__ int2 block_scan2(int2 v, int2 &tot) {
+  __shared__ int2 warp_sums[kThreads / 32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int2 x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int a = __shfl_up_sync(0xffffffffu, x.x, o);
+    int b = __shfl_up_sync(0xffffffffu, x.y, o);
+    if (lane >= o) {
+      x.x += a;
+      x.y += b;
+    }
+  }
+  if (lane == 31) warp_sums[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int2 s = warp_sums[lane];
+    int2 y = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int a = __shfl_up_sync(0xffffffffu, y.x, o);
+      int b = __shfl_up_sync(0xffffffffu, y.y, o);
+      if (lane >= o) {
+        y.x += a;
+        y.y += b;
+      }
+    }
+    warp_sums[lane] = make_int2(y.x - s.x, y.y - s.y);  // exclusive warp offsets
+    if (lane == 31) tot = y;                             // only thread 31 of warp 0 sets it
+  }
+  __syncthreads();
+  int2 off = warp_sums[w];
+  int2 r = make_int2(off.x + x.x - v.x, off.y + x.y - v.y);
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ int upper_bound_minus1(const int *pre, int n, int j) {
+  int lo = 0, hi = n;  // first index with pre[idx] > j
+  while (lo < hi) {
+    int mid = (lo + hi) >> 1;
+    if (pre[mid] > j)
+      hi = mid;
+    else
+      lo = mid + 1;
+  }
+  return lo - 1;
+}
+
+__global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
+  __shared__ unsigned long long s_total;
+  __shared__ uint32_t s_err;
+  __shared__ int2 s_tot;
+  __shared__ int s_W;
+  const int tid = threadIdx.x;
+  const int U = p.virt ? p.B * p.Q : p.B;
+  if (tid == 0) {
+    s_total = 0;
+    s_err = 0;
+  }
+  __syncthreads();
+
+  // sweep 1: total key blocks
+  uint32_t err = 0;
+  unsigned long long tot = 0;
+  for (int u = tid; u < U; u += kThreads) {
+    int n = unit_len(p, u, err);
+    tot += (unsigned long long)((n + kBlock - 1) / kBlock);
+  }
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_down_sync(0xffffffffu, tot, o);
+  if ((tid & 31) == 0) atomicAdd(&s_total, tot);
+  if (err) atomicOr(&s_err, err);
+  __syncthreads();
+  if (tid == 0) {
+    long long W;
+    if (p.split_blocks > 0) {
+      W = p.split_blocks;
+    } else {
+      long long work = (long long)s_total * p.hkv;
+      W = (work + p.target_items - 1) / p.target_items;
+      if (W < p.min_split_blocks) W = p.min_split_blocks;
+    }
+    if (W < 1) W = 1;
+    if (W > (1 << 30)) W = 1 << 30;
+    s_W = (int)W;
+  }
+  __syncthreads();
+  const int W = s_W;
+
+  // sweep 2: multi-part units (items + slots), then single-part units
+  int2 carry = make_int2(0, 0);
+  for (int base = 0; base < U; base += kThreads) {
+    int u = base + tid;
+    uint32_t e2 = 0;
+    int n = u < U ? unit_len(p, u, e2) : 0;
+    int nblk = (n + kBlock - 1) / kBlock;
+    int parts = nblk ? (nblk + W - 1) / W : 0;
+    int multi = parts > 1;
+    int2 v = make_int2(multi ? parts * p.hkv : 0, multi ? parts : 0);
+    int2 ex = block_scan2(v, s_tot);
+    if (u < U) {
+      p.prefix_a[u] = carry.x + ex.x;
+      UnitInfo ui;
+      ui.parts = parts;
+      ui.slot_base = multi ? carry.y + ex.y : -1;
+      ui.nblk = nblk;
+      ui.len = n;
+      p.units[u] = ui;
+    }
+    __syncthreads();
+    carry.x += s_tot.x;
+    carry.y += s_tot.y;
+    __syncthreads();
+  }
+  const int items_a = carry.x, slots = carry.y;
+  int2 carry_b = make_int2(0, 0);
+  for (int base = 0; base < U; base += kThreads) {
+    int u = base + tid;
+    int single = 0;
+    if (u < U) single = p.units[u].parts == 1;
+    int2 v = make_int2(single ? p.hkv : 0, 0);
+    int2 ex = block_scan2(v, s_tot);
+    if (u < U) p.prefix_b[u] = carry_b.x + ex.x;
+    __syncthreads();
+    carry_b.x += s_tot.x;
+    __syncthreads();
+  }
+  int num_items = items_a + carry_b.x;
+  if (num_items > p.max_items || slots > p.max_slots) {
+    // cannot happen for a workspace sized by pa_workspace_bytes; never write
+    // past the buffers
+    num_items = 0;
+    if (tid == 0) atomicOr(&s_err, PA_ERRF_PLAN_OVERFLOW);
+  }
+  __syncthreads();
+
+  // sweep 3: write the items
+  for (int j = tid; j < num_items; j += kThreads) {
+    int u, local;
+    if (j < items_a) {
+      u = upper_bound_minus1(p.prefix_a, U, j);
+      local = j - p.prefix_a[u];
+    } else {
+      u = upper_bound_minus1(p.prefix_b, U, j - items_a);
+      local = j - items_a - p.prefix_b[u];
+    }
+    UnitInfo ui = p.units[u];
+    int part = local / p.hkv, kvh = local % p.hkv;
+    int chunk = (ui.nblk + ui.parts - 1) / ui.parts;
+    WorkItem it;
+    it.unit = u;
+    it.kvh = kvh;
+    it.blk_begin = part * chunk;
+    it.blk_end = min(ui.nblk, it.blk_begin + chunk);
+    it.part = part;
+    it.parts = ui.parts;
+    it.slot = ui.parts > 1 ? ui.slot_base + part : -1;
+    it.pad = 0;
+    p.items[j] = it;
+  }
+  if (tid == 0) {
+    p.hdr[HDR_ERR] = s_err;
+    p.hdr[HDR_NUM_ITEMS] = (uint32_t)num_items;
+    p.hdr[HDR_SPLIT] = (uint32_t)W;
+    p.hdr[HDR_NUM_SLOTS] = (uint32_t)slots;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const PlanParams &pp, cudaStream_t s) {
+  plan_kernel<<<1, kThreads, 0, s>>>(pp);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -296,10 +296,12 @@ def _rand_bytes(seed: int, tag: int, chunk: int, shape, device, dtype=torch.uint
 def make_workload(name: str, device="cpu", *, B: Optional[int] = None,
                   seq_lens: Optional[Sequence[int]] = None, Q: Optional[int] = None,
                   seed: Optional[int] = None, poison: bool = True,
-                  chunk_blocks: int = 2048, kv_values: Optional[str] = None) -> Workload:
+                  chunk_blocks: int = 2048, kv_values: Optional[str] = None,
+                  Hq: Optional[int] = None, Hkv: Optional[int] = None,
+                  D: Optional[int] = None) -> Workload:
     """Builds a workload by its recipe name.  `B`, `seq_lens` and `Q`
     override the recipe for reduced-size parity cases (same distributions
-    and structure).  `kv_values` = "const_v" makes every valid V row of a
+    and structure); `Hq`, `Hkv`, `D` override the head shape.  `kv_values` = "const_v" makes every valid V row of a
     kv head the same vector (closed-form test input)."""
     s = spec(name)
     seed = 1000 + s["id"] if seed is None else seed
@@ -316,7 +318,9 @@ def make_workload(name: str, device="cpu", *, B: Optional[int] = None,
         need = sum((int(L) + 15) // 16 for L in lens.tolist())
         pool = ("permuted_subset", max(int(pool[1]), need))
     tables, NB = make_block_tables(pool, lens, gen)
-    Hq, Hkv, D = s["Hq"], s["Hkv"], s["D"]
+    Hq = s["Hq"] if Hq is None else Hq
+    Hkv = s["Hkv"] if Hkv is None else Hkv
+    D = s["D"] if D is None else D
     dt = s["dtype"]
     dev = torch.device(device)
 

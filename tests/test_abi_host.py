@@ -1,0 +1,116 @@
+"""C ABI checks that need no GPU: the library builds and loads, exports
+every entry point include/pa.h declares, and rejects bad arguments on the
+host (negative pa_status, nothing launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_decode_07_gb300 import build as pabuild
+from paged_kv_decode_07_gb300 import pa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    pabuild.build()
+    return pa.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "pa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_api():
+    fns = declared_functions()
+    for name in ("pa_decode", "pa_verify", "pa_merge", "pa_workspace_bytes",
+                 "pa_dequant_gather", "pa_read_error", "pa_status_string"):
+        assert name in fns
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    assert set(pa.EXPORTED) <= set(declared_functions())
+
+
+def test_status_strings(L):
+    assert pa.status_string(0) == "PA_OK"
+    assert pa.status_string(-1) == "PA_ERR_INVALID_ARG"
+    assert pa.status_string(-3) == "PA_ERR_WORKSPACE_TOO_SMALL"
+    assert L.pa_version() >= 100
+
+
+FAKE = 1 << 20   # a 16-byte aligned non-null address; never dereferenced on the host
+
+
+def kv_struct(dtype=0, D=256, hkv=4, nb=128, bs=16, scales=True):
+    s = pa._KvCache(dtype, nb, bs, hkv, D, FAKE, FAKE, FAKE if scales else None,
+                    FAKE if scales else None, 1.0, 1.0)
+    return s
+
+
+def prob_struct(B=2, Hq=24, Q=1, stride=8, max_len=100, out=FAKE, q=FAKE):
+    return pa._Problem(B, Hq, Q, q, FAKE, stride, FAKE, max_len, 0.0625, out, 0, None)
+
+
+def call(L, fn, kv, p, ws=FAKE, ws_bytes=1 << 30, opts=None):
+    o = opts if opts is not None else pa._Options(0, 0, 0, None, None)
+    return getattr(L, fn)(ctypes.byref(kv), ctypes.byref(p), ctypes.byref(o),
+                          ctypes.c_void_p(ws) if ws else None, ws_bytes, None)
+
+
+@pytest.mark.parametrize("fn", ["pa_decode", "pa_verify"])
+def test_invalid_arguments_are_rejected_on_the_host(L, fn):
+    assert call(L, fn, kv_struct(D=96), prob_struct()) == pa.PA_ERR_UNSUPPORTED
+    assert call(L, fn, kv_struct(bs=32), prob_struct()) == pa.PA_ERR_UNSUPPORTED
+    assert call(L, fn, kv_struct(dtype=7), prob_struct()) == pa.PA_ERR_INVALID_ARG
+    assert call(L, fn, kv_struct(dtype=1, scales=False), prob_struct()) == pa.PA_ERR_INVALID_ARG
+    assert call(L, fn, kv_struct(), prob_struct(Hq=25)) == pa.PA_ERR_INVALID_ARG     # Hq % Hkv
+    assert call(L, fn, kv_struct(hkv=1), prob_struct(Hq=16)) == pa.PA_ERR_UNSUPPORTED  # G > 8
+    assert call(L, fn, kv_struct(), prob_struct(q=None)) == pa.PA_ERR_INVALID_ARG
+    assert call(L, fn, kv_struct(), prob_struct(out=FAKE + 2)) == pa.PA_ERR_INVALID_ARG  # align
+    assert call(L, fn, kv_struct(), prob_struct(stride=0)) == pa.PA_ERR_INVALID_ARG
+    assert call(L, fn, kv_struct(), prob_struct(B=-1)) == pa.PA_ERR_INVALID_ARG
+    assert call(L, fn, kv_struct(), prob_struct(), ws=None) == pa.PA_ERR_INVALID_ARG
+    assert call(L, fn, kv_struct(), prob_struct(), ws_bytes=64) == pa.PA_ERR_WORKSPACE_TOO_SMALL
+    bad_opts = pa._Options(5, 0, 0, None, None)
+    assert call(L, fn, kv_struct(), prob_struct(), opts=bad_opts) == pa.PA_ERR_INVALID_ARG
+    # an empty batch is a no-op
+    assert call(L, fn, kv_struct(), prob_struct(B=0)) == pa.PA_OK
+
+
+def test_q_len_limits(L):
+    assert call(L, "pa_decode", kv_struct(), prob_struct(Q=2)) == pa.PA_ERR_UNSUPPORTED
+    assert call(L, "pa_verify", kv_struct(), prob_struct(Q=17)) == pa.PA_ERR_UNSUPPORTED
+
+
+def test_workspace_bytes_bounds(L):
+    kv = kv_struct()
+    small = L.pa_workspace_bytes(ctypes.byref(kv), ctypes.byref(prob_struct(max_len=1000)), None)
+    big = L.pa_workspace_bytes(ctypes.byref(kv), ctypes.byref(prob_struct(B=256, max_len=131072)),
+                               None)
+    assert 0 < small <= big
+    assert big < 256 << 20          # partials stay a small fraction of the KV pool
+    # forced tiny partitions need more
+    o = pa._Options(0, 1, 0, None, None)
+    forced = L.pa_workspace_bytes(ctypes.byref(kv), ctypes.byref(prob_struct(max_len=1000)),
+                                  ctypes.byref(o))
+    assert forced > 0
+    # invalid arguments -> 0
+    assert L.pa_workspace_bytes(ctypes.byref(kv_struct(D=96)), ctypes.byref(prob_struct()), None) == 0
+
+
+def test_merge_and_gather_argument_checks(L):
+    assert L.pa_merge(None, None, 1, 4, 6, ctypes.c_void_p(FAKE), 0, None, None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_merge(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 1, 0, 8,
+                      ctypes.c_void_p(FAKE), 0, None, None) == pa.PA_OK
+    kv = kv_struct()
+    assert L.pa_dequant_gather(ctypes.byref(kv), None, 8, ctypes.c_void_p(FAKE), 2, 10,
+                               ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), None,
+                               None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_read_error(None, None, None) == pa.PA_ERR_INVALID_ARG

@@ -1,0 +1,135 @@
+"""GPU parity of the CUDA path (through the C ABI) against the fp64 oracle.
+
+* every workload at reduced sizes that span several partitions and ragged
+  tails, compared element by element (fp32 output within the tolerance;
+  bf16 output equal to bf16_RNE of the fp32 output; LSE);
+* every workload at full size in the benchmark's launch configuration, on
+  sampled sequences the oracle computes one by one;
+* the dequant-only debug kernel bit-exact against the oracle's gather;
+* GQA group sizes and head dims the library supports.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_decode_07_gb300 import pa
+from paged_kv_decode_07_gb300 import workloads as W
+from tests.gpu_helpers import bf16_matches_fp32, compare, compare_lse, oracle_rows, run
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+REDUCED = {
+    "bf16_b1_l1000_d128": dict(),                                    # full size (tiny)
+    "int8_b32_l1k_32k_d256": dict(seq_lens=[1024, 3001, 1500, 2047, 17, 4101, 1, 16]),
+    "nvfp4_b4_l262k_d256": dict(seq_lens=[8195, 5000]),
+    "nvfp4_verify_q8_b4_ctx64k_d256": dict(seq_lens=[4104, 1008, 8, 9]),
+    "bf16_skewed_b256_l16_128k_d256": dict(seq_lens=[16, 17, 100, 1000, 5000, 20000, 31, 64,
+                                                     2048, 0, 130, 7777]),
+}
+
+
+def _fn(wl):
+    return "verify" if wl.Q > 1 else "decode"
+
+
+@pytest.mark.parametrize("name", list(REDUCED))
+def test_reduced_parity(name):
+    wl = W.make_workload(name, device=DEV, **REDUCED[name])
+    o32, lse, ws = run(wl, _fn(wl), out_fp32=True, return_lse=True)
+    ob, _ = run(wl, _fn(wl))
+    torch.cuda.synchronize()
+    assert pa.read_error(ws) == 0
+    ref_o, ref_l = oracle_rows(wl)
+    compare(o32, ref_o, name)
+    compare_lse(lse, ref_l, name)
+    assert bf16_matches_fp32(ob, o32), "bf16 output is not RNE of the fp32 output"
+
+
+FULL_SAMPLES = {
+    "int8_b32_l1k_32k_d256": 4,
+    "nvfp4_b4_l262k_d256": 2,
+    "nvfp4_verify_q8_b4_ctx64k_d256": 2,
+    "bf16_skewed_b256_l16_128k_d256": 6,
+}
+
+
+@pytest.mark.parametrize("name", list(FULL_SAMPLES))
+def test_full_size_sampled_parity(name):
+    wl = W.make_workload(name, device=DEV)
+    o32, lse, ws = run(wl, _fn(wl), out_fp32=True, return_lse=True)
+    torch.cuda.synchronize()
+    assert pa.read_error(ws) == 0
+    lens = wl.seq_lens.cpu()
+    order = torch.argsort(lens)
+    picks = {int(order[-1]), int(order[0]), 0, wl.B - 1}
+    g = torch.Generator().manual_seed(5)
+    while len(picks) < FULL_SAMPLES[name]:
+        picks.add(int(torch.randint(0, wl.B, (1,), generator=g)))
+    bs = sorted(picks)[: max(FULL_SAMPLES[name], 2)]
+    ref_o, ref_l = oracle_rows(wl, bs)
+    compare(o32[bs], ref_o, name)
+    compare_lse(lse[bs], ref_l, name)
+    del wl
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("dt", ["bf16", "int8", "nvfp4"])
+def test_dequant_gather_bit_exact(dt):
+    name = {"bf16": "bf16_skewed_b256_l16_128k_d256", "int8": "int8_b32_l1k_32k_d256",
+            "nvfp4": "nvfp4_b4_l262k_d256"}[dt]
+    lens = [33, 1, 200, 16, 0, 47]
+    wl = W.make_workload(name, device=DEV, seq_lens=lens)
+    kv = pa.KvCache.from_workload(wl)
+    maxl = max(lens) + 5
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    k, v = pa.dequant_gather(kv, wl.block_tables, wl.seq_lens, maxl, workspace=ws)
+    torch.cuda.synchronize()
+    assert pa.read_error(ws) == 0
+    h = W.host_arrays(wl)
+    cache = oracle.HostCache.from_host_arrays(h, wl.dtype, wl.k_global, wl.v_global)
+    rk, rv = oracle.gather(cache, h["block_tables"], h["seq_lens"], maxl)
+    kg, vg = k.cpu().numpy(), v.cpu().numpy()
+    assert np.array_equal(kg.view(np.uint32), rk.view(np.uint32))
+    assert np.array_equal(vg.view(np.uint32), rv.view(np.uint32))
+
+
+@pytest.mark.parametrize("dt", ["bf16", "int8", "nvfp4"])
+@pytest.mark.parametrize("shape", [(8, 8, 128), (16, 8, 128), (12, 2, 256), (4, 4, 256),
+                                   (32, 4, 256), (2, 1, 128)])
+def test_gqa_and_head_dim_variants(dt, shape):
+    Hq, Hkv, D = shape
+    name = {"bf16": "bf16_skewed_b256_l16_128k_d256", "int8": "int8_b32_l1k_32k_d256",
+            "nvfp4": "nvfp4_b4_l262k_d256"}[dt]
+    wl = W.make_workload(name, device=DEV, seq_lens=[700, 33, 1], Hq=Hq, Hkv=Hkv, D=D)
+    o32, lse, _ = run(wl, out_fp32=True, return_lse=True)
+    ref_o, ref_l = oracle_rows(wl)
+    compare(o32, ref_o, f"{dt} {shape}")
+    compare_lse(lse, ref_l, f"{dt} {shape}")
+
+
+@pytest.mark.parametrize("Q", [2, 5, 16])
+def test_verify_q_lens(Q):
+    wl = W.make_workload("nvfp4_verify_q8_b4_ctx64k_d256", device=DEV, seq_lens=[900, Q, 33], Q=Q)
+    o32, lse, _ = run(wl, "verify", out_fp32=True, return_lse=True)
+    ref_o, ref_l = oracle_rows(wl)
+    compare(o32, ref_o, f"verify Q={Q}")
+    compare_lse(lse, ref_l, f"verify Q={Q}")
+
+
+def test_merge_entry_point_matches_oracle():
+    g = torch.Generator(device="cpu").manual_seed(9)
+    S, R, D = 7, 50, 256
+    po = torch.randn(S, R, D, generator=g)
+    pl = torch.randn(S, R, generator=g) * 3
+    pl[2, :10] = -float("inf")
+    pl[:, 20] = -float("inf")                  # an all-empty row
+    out, lse = pa.merge(po.to(DEV), pl.to(DEV), out_fp32=True, return_lse=True)
+    ref_o, ref_l = oracle.merge(po.double().numpy(), pl.double().numpy())
+    np.testing.assert_allclose(out.cpu().double().numpy(), ref_o, atol=1e-5, rtol=0)
+    fin = np.isfinite(ref_l)
+    np.testing.assert_allclose(lse.cpu().double().numpy()[fin], ref_l[fin], atol=1e-5)
+    assert (lse.cpu().numpy()[~fin] == -np.inf).all()
+    ob = pa.merge(po.to(DEV), pl.to(DEV))
+    assert bf16_matches_fp32(ob, out)
