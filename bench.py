@@ -305,6 +305,9 @@ def run_ours(args, world, rank, local):
     # ---- device-timed region: inputs resident
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
+    for a, b in kev:          # torch creates the CUDA event on first record
+        a.record(stream)
+        b.record(stream)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(torch.cuda.current_device())
