@@ -143,6 +143,24 @@ size_t pa_workspace_bytes(const pa_kv_cache *kv, const pa_problem *prob, const p
 int pa_decode(const pa_kv_cache *kv, const pa_problem *prob, const pa_options *opt,
               void *ws, size_t ws_bytes, pa_stream_t stream);
 
+/* Decode without a caller-provided workspace, for callers that cannot
+ * allocate device memory (code whose framework owns every device
+ * allocation, plugins handed only their input and output buffers, hosts
+ * that forbid cudaMalloc after start-up).  The split-K workspace lives in a
+ * fixed device array of PA_NOALLOC_SCRATCH_BYTES inside the library, held
+ * by every GPU that loads it until the process exits; nothing is allocated
+ * per call.  The PagedAttention paper has no counterpart to this entry
+ * point.  Same arguments, semantics and results as pa_decode with default
+ * options.  Returns PA_ERR_WORKSPACE_TOO_SMALL, with nothing launched, when
+ * the call would need more workspace than PA_NOALLOC_SCRATCH_BYTES (about
+ * (batch + 300) * Hkv * G * D * 4 bytes for the default plan).  The
+ * first call on each device (with that device current) looks up the
+ * array's device address; make that first call before any stream capture.
+ * All calls share the array: calls that can overlap on the GPU race.  The
+ * device error flags of these calls cannot be read back. */
+#define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
+int pa_decode_noalloc(const pa_kv_cache *kv, const pa_problem *prob, pa_stream_t stream);
+
 /* Speculative verify (1 <= q_len <= 16), causal among the q_len new tokens
  * (query i sees keys t < seq_len - q_len + 1 + i).  Requires seq_len >=
  * q_len or 0; other rows set PA_ERRF_LEN_LT_QLEN. */
