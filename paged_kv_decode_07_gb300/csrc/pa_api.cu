@@ -11,6 +11,22 @@ cudaError_t launch_decode_simt_bf16(const AttnParams &p, int grid, cudaStream_t 
 cudaError_t launch_decode_simt_int8(const AttnParams &p, int grid, cudaStream_t s);
 cudaError_t launch_decode_simt_nvfp4(const AttnParams &p, int grid, cudaStream_t s);
 
+cudaError_t launch_decode_tc_int8(const AttnParams &p, int grid, cudaStream_t s);
+cudaError_t launch_decode_tc_nvfp4(const AttnParams &p, int grid, cudaStream_t s);
+
+cudaError_t launch_decode_tc(const AttnParams &p, int grid, cudaStream_t s) {
+  switch (p.kv.dtype) {
+    case PA_KV_INT8: return launch_decode_tc_int8(p, grid, s);
+    case PA_KV_NVFP4: return launch_decode_tc_nvfp4(p, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+int tc_supported(int dtype, int D, int R) {
+  return (dtype == PA_KV_INT8 || dtype == PA_KV_NVFP4) && (D == 128 || D == 256) && R >= 1 &&
+         R <= 8 && (R == 1 || R % 2 == 0);
+}
+
 cudaError_t launch_decode_simt(const AttnParams &p, int grid, cudaStream_t s) {
   switch (p.kv.dtype) {
     case PA_KV_BF16: return launch_decode_simt_bf16(p, grid, s);
@@ -153,11 +169,22 @@ int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *
   if (o && (o->split_blocks < 0 || o->target_items < 0)) return PA_ERR_INVALID_ARG;
   if (p->batch == 0) return PA_OK;
   const int G = p->num_q_heads / kv->num_kv_heads;
-  // the CUDA-core kernel runs verify as a virtual batch (one unit per query
-  // token); it is the only kernel built so far
-  if (kernel == 2) return PA_ERR_UNSUPPORTED;
+  // Kernel choice.  Both kernels run verify as a virtual batch (one unit per
+  // query token, its own key limit).  auto: tensor cores for the quantised
+  // formats (the CUDA cores cannot issue their dequant + 3,072 FMA per token
+  // and kv head at HBM speed), CUDA cores for bf16.
   const bool virt = true;
-  if (!simt_supported(kv->dtype, kv->head_dim, G)) return PA_ERR_UNSUPPORTED;
+  bool use_tc;
+  if (kernel == 2) {
+    if (!tc_supported(kv->dtype, kv->head_dim, G)) return PA_ERR_UNSUPPORTED;
+    use_tc = true;
+  } else if (kernel == 1) {
+    if (!simt_supported(kv->dtype, kv->head_dim, G)) return PA_ERR_UNSUPPORTED;
+    use_tc = false;
+  } else {
+    use_tc = tc_supported(kv->dtype, kv->head_dim, G);
+    if (!use_tc && !simt_supported(kv->dtype, kv->head_dim, G)) return PA_ERR_UNSUPPORTED;
+  }
   if (!ws) return PA_ERR_INVALID_ARG;
   if (!aligned16(ws)) return PA_ERR_INVALID_ARG;
   const Layout L = make_layout(kv, p, o, virt);
@@ -212,7 +239,9 @@ int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *
   if (o && o->event_begin &&
       cudaEventRecord(static_cast<cudaEvent_t>(o->event_begin), stream) != cudaSuccess)
     return PA_ERR_CUDA;
-  if (launch_decode_simt(ap, L.max_items, stream) != cudaSuccess) return PA_ERR_CUDA;
+  if ((use_tc ? launch_decode_tc(ap, L.max_items, stream)
+              : launch_decode_simt(ap, L.max_items, stream)) != cudaSuccess)
+    return PA_ERR_CUDA;
   if (o && o->event_end &&
       cudaEventRecord(static_cast<cudaEvent_t>(o->event_end), stream) != cudaSuccess)
     return PA_ERR_CUDA;

@@ -1,0 +1,456 @@
+// pa_decode_mma.cuh -- split-K paged decode attention on the tensor cores
+// (mma.sync m16n8k16, f16 operands, fp32 accumulation) for the int8 and
+// NVFP4 KV formats.
+//
+// Why tensor cores for decode: with GQA the G query heads of one kv head
+// share every key and value, so per (token, kv head) the scores and the PV
+// update are a dense [G x D] x [D x 16-token] contraction -- 3,072 FMA per
+// token and kv head at D = 256, G = 6.  Against 516 B (int8) or 288 B
+// (NVFP4) per token and kv head that is 11.9 / 21.3 FLOP per byte, more
+// than the CUDA cores can issue next to the dequant at HBM speed (the
+// counters of the CUDA-core kernel show it issue-bound).
+//
+// Work split is the CUDA-core kernel's (one CTA of 4 warps per work item,
+// each warp streams whole 16-token blocks through its own ring of shared
+// memory stages filled by 1-D bulk copies).  Per block a warp computes
+//   S^T [16 tokens x 8 heads] = K [16 x D] . Q^T [D x 8]      (M = tokens)
+//   O^T [D x 8 heads]        += V^T [D x 16] . P^T [16 x 8]   (M = head dim)
+// with G <= 8 query heads in the N = 8 columns.  Operand fragments are
+// built straight from the quantised codes in shared memory, dequantised in
+// registers to f16 (exact for both formats: int8 codes, and e2m1 * e4m3
+// products with at most 6 significant bits).  Because a dot product does
+// not care in which order it visits the head dim, each lane reads 16
+// contiguous bytes of a key row and the query fragments use the same
+// permuted head-dim order; for PV the head-dim rows are permuted the same
+// way and un-permuted when the output is written.  The scores' fragment
+// layout is turned into PV's B fragment with 8 shuffles per block.
+// Scales: int8 per-token scales multiply the score (K) and the
+// probability (V); the NVFP4 block scale multiplies the f16 codes (one
+// exact f16x2 multiply per pair); softmax_scale * log2 e and the NVFP4
+// global scales are applied in fp32 outside the MMAs, so q stays exact.
+#pragma once
+
+#include "pa_internal.cuh"
+
+namespace pa {
+namespace tc {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+
+template <int DT, int D>
+struct Geo {
+  static_assert(DT == PA_KV_INT8 || DT == PA_KV_NVFP4, "quantised formats only");
+  static constexpr int ROW = DT == PA_KV_INT8 ? D : D / 2;    // code bytes per token row
+  static constexpr int E = DT == PA_KV_INT8 ? 16 : 32;        // elements per 16 bytes
+  static constexpr int KG = D / (4 * E);                      // K chunks per lane
+  static constexpr int KS = E / 4;                            // k-steps per K chunk
+  static constexpr int VE = (8 * E <= D) ? E : D / 8;         // V elements per lane chunk
+  static constexpr int VB = DT == PA_KV_INT8 ? VE : VE / 2;   // V chunk bytes
+  static constexpr int VG = D / (8 * VE);                     // V chunk groups
+  static constexpr int SROW = DT == PA_KV_INT8 ? 2 : D / 16;  // scale bytes per token row
+  static constexpr int CODE = kBlock * ROW;
+  static constexpr int SC = kBlock * SROW;
+  static constexpr int STAGE = 2 * (CODE + SC);
+  static constexpr int NSTAGE = DT == PA_KV_INT8 ? 3 : 4;
+  static constexpr int WARP_BYTES = NSTAGE * STAGE;
+  static constexpr int SMEM = kWarps * WARP_BYTES;
+  static_assert(KG >= 1 && VG >= 1 && CODE % 16 == 0 && SC % 16 == 0, "geometry");
+  static_assert(WARP_BYTES >= 8 * D * 4, "stage area holds the warp's O for the merge");
+};
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  return __byte_perm(a, b, sel);
+}
+
+__device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// int8 codes -> f16x2, exact: (0x6400 | (code ^ 0x80)) is 1024 + code + 128.
+// `x` holds four codes already XORed with 0x80808080; pair 0 = bytes 0,1.
+__device__ __forceinline__ uint32_t s8pair_to_h2(uint32_t x, int pair) {
+  uint32_t h = prmt(x, 0x64646464u, pair ? 0x4342u : 0x4140u);
+  const uint32_t bias = 0x64806480u;   // (1152, 1152) in f16
+  __half2 r = __hsub2(*reinterpret_cast<__half2 *>(&h), *reinterpret_cast<const __half2 *>(&bias));
+  return *reinterpret_cast<uint32_t *>(&r);
+}
+
+// byte j (two E2M1 codes) of a word -> f16x2, exact
+__device__ __forceinline__ uint32_t e2m1_byte_to_h2(uint32_t w, int j) {
+  return e2m1x2_to_h2((w >> (8 * j)) & 0xffu);
+}
+
+template <int DT, int D, int R>
+__global__ void __launch_bounds__(kThreads, DT == PA_KV_NVFP4 ? 3 : 2)
+    decode_kernel(const AttnParams p) {
+  using Gm = Geo<DT, D>;
+  constexpr int KG = Gm::KG, KS = Gm::KS, VE = Gm::VE, VB = Gm::VB, VG = Gm::VG;
+  constexpr int NSTAGE = Gm::NSTAGE, ROW = Gm::ROW, SROW = Gm::SROW;
+  constexpr float kRescale = 8.0f;
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[kWarps][NSTAGE];
+  __shared__ float s_m[kWarps][8], s_l[kWarps][8];
+
+  const uint32_t num_items = p.hdr[HDR_NUM_ITEMS];
+  if (blockIdx.x >= num_items) return;
+  const WorkItem it = p.items[blockIdx.x];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = lane >> 2, c = lane & 3;
+  const int Q = p.Q;
+  const int b = p.virt ? it.unit / Q : it.unit;
+  const int qi = p.virt ? it.unit % Q : 0;
+  const int len = p.units[it.unit].len;
+  const int kvh = it.kvh;
+  const int Hkv = p.kv.hkv;
+
+  // ---- query fragments (B operand of S^T = K Q^T), head-dim order permuted
+  // like the key fragments: k-step (g, s), rows 2c..2c+1 <-> d = g*4E + c*E + 4s
+  // + {0,1}, rows 2c+8.. <-> + {2,3}.  Column n = r is query head r.
+  uint32_t qf[KG][KS][2];
+  {
+    const bool live = r < R;
+    const __nv_bfloat16 *qrow =
+        p.q + (((size_t)b * Q + qi) * p.Hq + (size_t)kvh * p.G + (live ? r : 0)) * D;
+#pragma unroll
+    for (int g = 0; g < KG; ++g)
+#pragma unroll
+      for (int s = 0; s < KS; ++s) {
+        const int d = g * 4 * Gm::E + c * Gm::E + 4 * s;
+        uint2 u = live ? *reinterpret_cast<const uint2 *>(qrow + d) : make_uint2(0, 0);
+        float2 x0 = bf16x2_to_f2(u.x), x1 = bf16x2_to_f2(u.y);
+        qf[g][s][0] = f2_to_h2(x0.x, x0.y);
+        qf[g][s][1] = f2_to_h2(x1.x, x1.y);
+      }
+  }
+  const float qscale = p.scale_log2 * (DT == PA_KV_NVFP4 ? p.kv.kg : 1.0f);
+
+  // ---- this warp's blocks
+  const int t_begin = it.blk_begin * kBlock;
+  const int t_end = min(len, it.blk_end * kBlock);
+  const int n_blk = t_end > t_begin ? (t_end - t_begin + kBlock - 1) / kBlock : 0;
+  const int n_local = n_blk > warp ? (n_blk - warp + kWarps - 1) / kWarps : 0;
+
+  uint8_t *wsm = smem + warp * Gm::WARP_BYTES;
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < NSTAGE; ++s) mbar_init(&bars[warp][s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  const int *trow = p.tables + (size_t)b * p.stride;
+  const uint64_t pol = policy_evict_first();
+  int tab_cache = -1, tab_chunk = -1;
+  uint32_t valid_bits = 0;
+  bool failed = false;
+
+  auto issue = [&](int j) {
+    const int chunk = j >> 5;
+    if (chunk != tab_chunk) {
+      const int jj = chunk * 32 + lane;
+      tab_cache = (jj < n_local) ? __ldg(trow + it.blk_begin + warp + jj * kWarps) : -1;
+      tab_chunk = chunk;
+    }
+    const int phys = __shfl_sync(0xffffffffu, tab_cache, j & 31);
+    const int s = j % NSTAGE;
+    const bool ok = phys >= 0 && phys < p.kv.num_blocks;
+    valid_bits = ok ? (valid_bits | (1u << s)) : (valid_bits & ~(1u << s));
+    if (lane == 0) {
+      uint64_t *bar = &bars[warp][s];
+      if (!ok) {
+        set_err(p.hdr, PA_ERRF_BAD_BLOCK_ID);
+        mbar_arrive(bar);
+      } else {
+        uint8_t *st = wsm + s * Gm::STAGE;
+        const size_t tile = (size_t)phys * Hkv + kvh;
+        mbar_arrive_expect_tx(bar, Gm::STAGE);
+        bulk_g2s(st, (const uint8_t *)p.kv.k + tile * Gm::CODE, Gm::CODE, bar, pol);
+        bulk_g2s(st + Gm::CODE, (const uint8_t *)p.kv.v + tile * Gm::CODE, Gm::CODE, bar, pol);
+        bulk_g2s(st + 2 * Gm::CODE, (const uint8_t *)p.kv.ks + tile * Gm::SC, Gm::SC, bar, pol);
+        bulk_g2s(st + 2 * Gm::CODE + Gm::SC, (const uint8_t *)p.kv.vs + tile * Gm::SC, Gm::SC, bar,
+                 pol);
+      }
+    }
+  };
+
+  // ---- state: columns 2c, 2c+1 (query heads) of this lane
+  float m_run[2] = {kNegInf, kNegInf};
+  float l_run[2] = {0.f, 0.f};
+  float o[VG][VE / 2][4];
+#pragma unroll
+  for (int g = 0; g < VG; ++g)
+#pragma unroll
+    for (int e = 0; e < VE / 2; ++e)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[g][e][k] = 0.f;
+
+  // P^T fragment sources: token 2c lives in lane 8c + r/2, token 2c+1 four lanes up
+  const int srcA = 8 * c + (r >> 1), srcB = srcA + 4;
+  const bool odd = r & 1;
+
+  const int prologue = min(NSTAGE, n_local);
+  for (int j = 0; j < prologue; ++j) issue(j);
+  int issued = prologue;
+
+  for (int j = 0; j < n_local; ++j) {
+    const int s = j % NSTAGE;
+    const bool arrived = mbar_wait(&bars[warp][s], (j / NSTAGE) & 1);
+    if (!__all_sync(0xffffffffu, arrived)) {
+      failed = true;
+      if (lane == 0) set_err(p.hdr, PA_ERRF_WAIT_TIMEOUT);
+      break;
+    }
+    if (valid_bits & (1u << s)) {
+      const uint8_t *st = wsm + s * Gm::STAGE;
+      const uint8_t *sK = st, *sV = st + Gm::CODE;
+      const uint8_t *sKs = st + 2 * Gm::CODE, *sVs = sKs + Gm::SC;
+      const int tok0 = t_begin + (warp + j * kWarps) * kBlock;
+      const int nvalid = min(kBlock, t_end - tok0);
+
+      // ---- S^T = K . Q^T
+      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int g = 0; g < KG; ++g) {
+        const int boff = g * 64 + c * 16;
+        uint4 k0 = *reinterpret_cast<const uint4 *>(sK + r * ROW + boff);
+        uint4 k1 = *reinterpret_cast<const uint4 *>(sK + (r + 8) * ROW + boff);
+        uint32_t w0[4] = {k0.x, k0.y, k0.z, k0.w}, w1[4] = {k1.x, k1.y, k1.z, k1.w};
+        if constexpr (DT == PA_KV_INT8) {
+#pragma unroll
+          for (int s2 = 0; s2 < KS; ++s2) {   // k-step s2 uses word s2 of each row
+            const uint32_t x0 = w0[s2] ^ 0x80808080u, x1 = w1[s2] ^ 0x80808080u;
+            mma16816(sacc, s8pair_to_h2(x0, 0), s8pair_to_h2(x1, 0), s8pair_to_h2(x0, 1),
+                     s8pair_to_h2(x1, 1), qf[g][s2][0], qf[g][s2][1]);
+          }
+        } else {
+          const int sb = (g * 4 * Gm::E + c * Gm::E) / 16;   // first 16-element scale block
+          const uint32_t sc00 = e4m3_to_h2_dup(sKs[r * SROW + sb]);
+          const uint32_t sc01 = e4m3_to_h2_dup(sKs[r * SROW + sb + 1]);
+          const uint32_t sc10 = e4m3_to_h2_dup(sKs[(r + 8) * SROW + sb]);
+          const uint32_t sc11 = e4m3_to_h2_dup(sKs[(r + 8) * SROW + sb + 1]);
+#pragma unroll
+          for (int s2 = 0; s2 < KS; ++s2) {   // elements 4 s2 .. 4 s2 + 3 = bytes 2 s2, 2 s2 + 1
+            const int wi = s2 >> 1, bj = (s2 & 1) * 2;
+            const uint32_t a_s = s2 < KS / 2 ? sc00 : sc01, b_s = s2 < KS / 2 ? sc10 : sc11;
+            mma16816(sacc, hmul2_u32(e2m1_byte_to_h2(w0[wi], bj), a_s),
+                     hmul2_u32(e2m1_byte_to_h2(w1[wi], bj), b_s),
+                     hmul2_u32(e2m1_byte_to_h2(w0[wi], bj + 1), a_s),
+                     hmul2_u32(e2m1_byte_to_h2(w1[wi], bj + 1), b_s), qf[g][s2][0], qf[g][s2][1]);
+          }
+        }
+      }
+      // scale, mask
+      float f0 = qscale, f1 = qscale;
+      if constexpr (DT == PA_KV_INT8) {
+        f0 *= fp16_bits_to_f(reinterpret_cast<const uint16_t *>(sKs)[r]);
+        f1 *= fp16_bits_to_f(reinterpret_cast<const uint16_t *>(sKs)[r + 8]);
+      }
+      const bool v0 = r < nvalid, v1 = r + 8 < nvalid;
+      float sc[4];
+      sc[0] = v0 ? sacc[0] * f0 : kNegInf;
+      sc[1] = v0 ? sacc[1] * f0 : kNegInf;
+      sc[2] = v1 ? sacc[2] * f1 : kNegInf;
+      sc[3] = v1 ? sacc[3] * f1 : kNegInf;
+
+      // ---- online softmax over the block's tokens, per column
+      float mx[2] = {fmaxf(sc[0], sc[2]), fmaxf(sc[1], sc[3])};
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 4));
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 8));
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 16));
+      }
+      const bool need = (mx[0] > m_run[0] + kRescale) || (mx[1] > m_run[1] + kRescale);
+      if (__any_sync(0xffffffffu, need)) {
+        float al[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float mn = fmaxf(m_run[h], mx[h]);
+          al[h] = (mn == kNegInf) ? 1.f : exp2f(m_run[h] - mn);
+          m_run[h] = mn;
+          l_run[h] *= al[h];
+        }
+#pragma unroll
+        for (int g = 0; g < VG; ++g)
+#pragma unroll
+          for (int e = 0; e < VE / 2; ++e) {
+            o[g][e][0] *= al[0];
+            o[g][e][1] *= al[1];
+            o[g][e][2] *= al[0];
+            o[g][e][3] *= al[1];
+          }
+      }
+      float pr[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) pr[k] = (sc[k] == kNegInf) ? 0.f : exp2f(sc[k] - m_run[k & 1]);
+      l_run[0] += pr[0] + pr[2];
+      l_run[1] += pr[1] + pr[3];
+      if constexpr (DT == PA_KV_INT8) {
+        const float vs0 = fp16_bits_to_f(reinterpret_cast<const uint16_t *>(sVs)[r]);
+        const float vs1 = fp16_bits_to_f(reinterpret_cast<const uint16_t *>(sVs)[r + 8]);
+        pr[0] = v0 ? pr[0] * vs0 : 0.f;
+        pr[1] = v0 ? pr[1] * vs0 : 0.f;
+        pr[2] = v1 ? pr[2] * vs1 : 0.f;
+        pr[3] = v1 ? pr[3] * vs1 : 0.f;
+      }
+      // ---- P^T fragment (tokens 2c, 2c+1 | 2c+8, 2c+9; column r)
+      float pa0 = __shfl_sync(0xffffffffu, pr[0], srcA), pa1 = __shfl_sync(0xffffffffu, pr[1], srcA);
+      float pb0 = __shfl_sync(0xffffffffu, pr[0], srcB), pb1 = __shfl_sync(0xffffffffu, pr[1], srcB);
+      float pc0 = __shfl_sync(0xffffffffu, pr[2], srcA), pc1 = __shfl_sync(0xffffffffu, pr[3], srcA);
+      float pd0 = __shfl_sync(0xffffffffu, pr[2], srcB), pd1 = __shfl_sync(0xffffffffu, pr[3], srcB);
+      const uint32_t B0 = f2_to_h2(odd ? pa1 : pa0, odd ? pb1 : pb0);
+      const uint32_t B1 = f2_to_h2(odd ? pc1 : pc0, odd ? pd1 : pd0);
+
+      // ---- O^T += V^T . P^T ; this lane's tokens 2c, 2c+1, 2c+8, 2c+9
+      const int tk[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+#pragma unroll
+      for (int g = 0; g < VG; ++g) {
+        const int boff = g * 8 * VB + r * VB;
+        uint32_t vw[4][VB / 4];
+        uint32_t vsc[4][2];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const bool ok = tk[t] < nvalid;   // poisoned tail slots must not reach the MMA
+          const uint8_t *src = sV + tk[t] * ROW + boff;
+          if constexpr (VB == 16) {
+            uint4 u = ok ? *reinterpret_cast<const uint4 *>(src) : make_uint4(0, 0, 0, 0);
+            vw[t][0] = u.x;
+            vw[t][1] = u.y;
+            vw[t][2] = u.z;
+            vw[t][3] = u.w;
+          } else {
+            uint2 u = ok ? *reinterpret_cast<const uint2 *>(src) : make_uint2(0, 0);
+            vw[t][0] = u.x;
+            vw[t][1] = u.y;
+          }
+          if constexpr (DT == PA_KV_NVFP4) {
+            const int sb = (g * 8 * VE + r * VE) / 16;
+            vsc[t][0] = ok ? e4m3_to_h2_dup(sVs[tk[t] * SROW + sb]) : 0u;
+            vsc[t][1] = (ok && VE > 16) ? e4m3_to_h2_dup(sVs[tk[t] * SROW + sb + 1]) : vsc[t][0];
+          } else {
+            vw[t][0] ^= 0x80808080u;   // int8 -> offset-binary for the f16 magic
+#pragma unroll
+            for (int q = 1; q < VB / 4; ++q) vw[t][q] ^= 0x80808080u;
+            (void)vsc;
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < VE / 2; ++e) {
+          uint32_t h[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            if constexpr (DT == PA_KV_NVFP4) {
+              h[t] = hmul2_u32(e2m1_byte_to_h2(vw[t][e >> 2], e & 3), vsc[t][e >= 8 ? 1 : 0]);
+            } else {
+              h[t] = s8pair_to_h2(vw[t][e >> 1], e & 1);   // a zeroed slot decodes to 0
+            }
+          }
+          mma16816(o[g][e], prmt(h[0], h[1], 0x5410), prmt(h[0], h[1], 0x7632),
+                   prmt(h[2], h[3], 0x5410), prmt(h[2], h[3], 0x7632), B0, B1);
+        }
+      }
+    }
+    __syncwarp();
+    if (issued < n_local) {
+      issue(issued);
+      ++issued;
+    }
+  }
+  if (failed) {
+    for (int j = 0; j < issued; ++j) (void)mbar_wait(&bars[warp][j % NSTAGE], (j / NSTAGE) & 1);
+  }
+
+  // ---- per-warp totals
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 4);
+    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 8);
+    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 16);
+  }
+  if (r == 0) {
+    s_m[warp][2 * c] = m_run[0];
+    s_m[warp][2 * c + 1] = m_run[1];
+    s_l[warp][2 * c] = l_run[0];
+    s_l[warp][2 * c + 1] = l_run[1];
+  }
+  float *ow = reinterpret_cast<float *>(wsm);   // [8 heads][D]
+#pragma unroll
+  for (int g = 0; g < VG; ++g)
+#pragma unroll
+    for (int e = 0; e < VE / 2; ++e) {
+      const int d = g * 8 * VE + r * VE + 2 * e;
+      *reinterpret_cast<float2 *>(ow + (2 * c) * D + d) = make_float2(o[g][e][0], o[g][e][2]);
+      *reinterpret_cast<float2 *>(ow + (2 * c + 1) * D + d) = make_float2(o[g][e][1], o[g][e][3]);
+    }
+  __syncthreads();
+
+  // ---- merge the warps and write (rows h < R)
+  const float vg = DT == PA_KV_NVFP4 ? p.kv.vg : 1.0f;
+  const int G = p.G;
+  for (int idx = threadIdx.x; idx < R * D; idx += kThreads) {
+    const int h = idx / D, d = idx % D;
+    float M = kNegInf;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_m[w][h]);
+    float L = 0.f, acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float mw = s_m[w][h];
+      const float f = (mw == kNegInf) ? 0.f : exp2f(mw - M);
+      L += f * s_l[w][h];
+      acc += f * reinterpret_cast<const float *>(smem + w * Gm::WARP_BYTES)[h * D + d];
+    }
+    const float out = L > 0.f ? acc / L * vg : 0.f;
+    const float lse = L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : kNegInf;
+    if (it.parts <= 1) {
+      const size_t row = ((size_t)b * Q + qi) * p.Hq + (size_t)kvh * G + h;
+      if (p.out_fp32)
+        reinterpret_cast<float *>(p.out)[row * D + d] = out;
+      else
+        reinterpret_cast<__nv_bfloat16 *>(p.out)[row * D + d] = __float2bfloat16_rn(out);
+      if (d == 0 && p.lse_out) p.lse_out[row] = lse;
+    } else {
+      const size_t prow = ((size_t)it.slot * Hkv + kvh) * p.R + h;
+      p.part_o[prow * D + d] = out;
+      if (d == 0) p.part_lse[prow] = lse;
+    }
+  }
+}
+
+template <int DT, int D, int R>
+cudaError_t launch_one(const AttnParams &p, int grid, cudaStream_t s) {
+  using Gm = Geo<DT, D>;
+  auto kern = decode_kernel<DT, D, R>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, Gm::SMEM, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_dtype(const AttnParams &p, int grid, cudaStream_t s) {
+  const int D = p.kv.D, R = p.R;
+#define PA_TC_CASE(DD, RR) \
+  if (D == DD && R == RR) return launch_one<DT, DD, RR>(p, grid, s);
+  PA_TC_CASE(128, 1) PA_TC_CASE(128, 2) PA_TC_CASE(128, 4) PA_TC_CASE(128, 6)
+  PA_TC_CASE(128, 8) PA_TC_CASE(256, 1) PA_TC_CASE(256, 2) PA_TC_CASE(256, 4)
+  PA_TC_CASE(256, 6) PA_TC_CASE(256, 8)
+#undef PA_TC_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace tc
+}  // namespace pa

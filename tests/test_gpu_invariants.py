@@ -24,34 +24,36 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 NAMES = {"bf16": "bf16_skewed_b256_l16_128k_d256", "int8": "int8_b32_l1k_32k_d256",
          "nvfp4": "nvfp4_b4_l262k_d256"}
+# (dtype, kernel): 1 = CUDA-core kernel, 2 = tensor-core kernel
+DK = [("bf16", 1), ("int8", 1), ("int8", 2), ("nvfp4", 1), ("nvfp4", 2)]
 LENS = [3000, 17, 1, 900, 0, 4099]
 
 
-@pytest.mark.parametrize("dt", list(NAMES))
-def test_block_permutation_bitwise(dt):
+@pytest.mark.parametrize("dt,kernel", DK)
+def test_block_permutation_bitwise(dt, kernel):
     wl = W.make_workload(NAMES[dt], device=DEV, seq_lens=LENS)
     wp = W.permute_pool(wl, seed=3)
-    a, _ = run(wl, out_fp32=True)
-    b, _ = run(wp, out_fp32=True)
+    a, _ = run(wl, out_fp32=True, kernel=kernel)
+    b, _ = run(wp, out_fp32=True, kernel=kernel)
     assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("dt", list(NAMES))
-def test_determinism_bitwise(dt):
+@pytest.mark.parametrize("dt,kernel", DK)
+def test_determinism_bitwise(dt, kernel):
     wl = W.make_workload(NAMES[dt], device=DEV, seq_lens=LENS)
-    a, la, _ = run(wl, out_fp32=True, return_lse=True)
-    b, lb, _ = run(wl, out_fp32=True, return_lse=True)
+    a, la, _ = run(wl, out_fp32=True, return_lse=True, kernel=kernel)
+    b, lb, _ = run(wl, out_fp32=True, return_lse=True, kernel=kernel)
     assert torch.equal(a, b) and torch.equal(la, lb)
 
 
-@pytest.mark.parametrize("dt", list(NAMES))
-def test_split_settings_agree(dt):
+@pytest.mark.parametrize("dt,kernel", DK)
+def test_split_settings_agree(dt, kernel):
     wl = W.make_workload(NAMES[dt], device=DEV, seq_lens=LENS)
     ref, _ = oracle_rows(wl)
-    auto, _ = run(wl, out_fp32=True)
-    single, ws1 = run(wl, out_fp32=True, split_blocks=1 << 20)
-    tiny, ws2 = run(wl, out_fp32=True, split_blocks=1)
-    few, _ = run(wl, out_fp32=True, target_items=7)
+    auto, _ = run(wl, out_fp32=True, kernel=kernel)
+    single, ws1 = run(wl, out_fp32=True, split_blocks=1 << 20, kernel=kernel)
+    tiny, ws2 = run(wl, out_fp32=True, split_blocks=1, kernel=kernel)
+    few, _ = run(wl, out_fp32=True, target_items=7, kernel=kernel)
     for o, tag in ((auto, "auto"), (single, "single"), (tiny, "tiny"), (few, "few")):
         compare(o, ref, f"{dt} {tag}")
     assert pa.header(ws1)[3] == 0            # no partial slots when nothing splits
@@ -67,15 +69,15 @@ def test_padded_rows_zero_and_neg_inf():
     assert pa.read_error(ws) == 0
 
 
-@pytest.mark.parametrize("dt", list(NAMES))
-def test_bad_block_id_is_skipped_and_flagged(dt):
+@pytest.mark.parametrize("dt,kernel", DK)
+def test_bad_block_id_is_skipped_and_flagged(dt, kernel):
     wl = W.make_workload(NAMES[dt], device=DEV, seq_lens=[400, 50])
     NB = wl.num_blocks
     bad = wl.block_tables.clone()
     bad[0, 3] = -5            # a middle block of sequence 0
     bad[1, 1] = NB + 7        # a block past the end of the pool
     wl_bad = W.Workload(**{**wl.__dict__, "block_tables": bad})
-    o, ws = run(wl_bad, out_fp32=True)
+    o, ws = run(wl_bad, out_fp32=True, kernel=kernel)
     torch.cuda.synchronize()
     assert pa.read_error(ws) & pa.PA_ERRF_BAD_BLOCK_ID
     # expected: attention over the keys without those blocks (decode has no

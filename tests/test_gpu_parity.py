@@ -34,11 +34,19 @@ def _fn(wl):
     return "verify" if wl.Q > 1 else "decode"
 
 
-@pytest.mark.parametrize("name", list(REDUCED))
-def test_reduced_parity(name):
+def _kernels(dtype):
+    """0 = auto; 1 = CUDA-core kernel; 2 = tensor-core kernel (quantised formats)."""
+    return [0, 1, 2] if dtype in ("int8", "nvfp4") else [0, 1]
+
+
+REDUCED_CASES = [(n, k) for n in REDUCED for k in _kernels(W.spec(n)["dtype"])]
+
+
+@pytest.mark.parametrize("name,kernel", REDUCED_CASES)
+def test_reduced_parity(name, kernel):
     wl = W.make_workload(name, device=DEV, **REDUCED[name])
-    o32, lse, ws = run(wl, _fn(wl), out_fp32=True, return_lse=True)
-    ob, _ = run(wl, _fn(wl))
+    o32, lse, ws = run(wl, _fn(wl), out_fp32=True, return_lse=True, kernel=kernel)
+    ob, _ = run(wl, _fn(wl), kernel=kernel)
     torch.cuda.synchronize()
     assert pa.read_error(ws) == 0
     ref_o, ref_l = oracle_rows(wl)
@@ -95,24 +103,26 @@ def test_dequant_gather_bit_exact(dt):
     assert np.array_equal(vg.view(np.uint32), rv.view(np.uint32))
 
 
-@pytest.mark.parametrize("dt", ["bf16", "int8", "nvfp4"])
+@pytest.mark.parametrize("dt,kernel", [("bf16", 1), ("int8", 1), ("int8", 2), ("nvfp4", 1),
+                                       ("nvfp4", 2)])
 @pytest.mark.parametrize("shape", [(8, 8, 128), (16, 8, 128), (12, 2, 256), (4, 4, 256),
                                    (32, 4, 256), (2, 1, 128)])
-def test_gqa_and_head_dim_variants(dt, shape):
+def test_gqa_and_head_dim_variants(dt, kernel, shape):
     Hq, Hkv, D = shape
     name = {"bf16": "bf16_skewed_b256_l16_128k_d256", "int8": "int8_b32_l1k_32k_d256",
             "nvfp4": "nvfp4_b4_l262k_d256"}[dt]
     wl = W.make_workload(name, device=DEV, seq_lens=[700, 33, 1], Hq=Hq, Hkv=Hkv, D=D)
-    o32, lse, _ = run(wl, out_fp32=True, return_lse=True)
+    o32, lse, _ = run(wl, out_fp32=True, return_lse=True, kernel=kernel)
     ref_o, ref_l = oracle_rows(wl)
     compare(o32, ref_o, f"{dt} {shape}")
     compare_lse(lse, ref_l, f"{dt} {shape}")
 
 
 @pytest.mark.parametrize("Q", [2, 5, 16])
-def test_verify_q_lens(Q):
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_verify_q_lens(Q, kernel):
     wl = W.make_workload("nvfp4_verify_q8_b4_ctx64k_d256", device=DEV, seq_lens=[900, Q, 33], Q=Q)
-    o32, lse, _ = run(wl, "verify", out_fp32=True, return_lse=True)
+    o32, lse, _ = run(wl, "verify", out_fp32=True, return_lse=True, kernel=kernel)
     ref_o, ref_l = oracle_rows(wl)
     compare(o32, ref_o, f"verify Q={Q}")
     compare_lse(lse, ref_l, f"verify Q={Q}")
