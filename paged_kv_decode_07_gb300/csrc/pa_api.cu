@@ -276,7 +276,7 @@ int pa_verify(const pa_kv_cache *kv, const pa_problem *prob, const pa_options *o
 
 int pa_merge(const float *part_out, const float *part_lse, int32_t S, int32_t R, int32_t D,
              void *out, int32_t out_fp32, float *lse_out, pa_stream_t stream) {
-  if (S < 0 || R < 0 || D < 4 || D % 4) return PA_ERR_INVALID_ARG;
+  if (S < 0 || R < 0 || D < 4 || D % 4 || D > 1024) return PA_ERR_INVALID_ARG;
   if (R == 0) return PA_OK;
   if (!out || (S > 0 && (!part_out || !part_lse))) return PA_ERR_INVALID_ARG;
   if (!aligned16(out) || (part_out && !aligned16(part_out)) || (part_lse && !aligned4(part_lse)))

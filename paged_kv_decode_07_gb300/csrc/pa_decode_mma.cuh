@@ -30,10 +30,61 @@
 // global scales are applied in fp32 outside the MMAs, so q stays exact.
 #pragma once
 
+#include <cuda.h>
+
+#include <cstring>
+#include <mutex>
+
 #include "pa_internal.cuh"
 
 namespace pa {
 namespace tc {
+
+// ---- 2-D TMA over the pool viewed as [NB * Hkv * 16 token rows, row bytes]
+// with 16-row x 128-byte boxes and the 128-byte swizzle: within every 1024
+// bytes the 16-byte chunk index of a row is XORed with (row % 8), which makes
+// the fragment reads below conflict-free.
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// rows of `row_bytes` (a multiple of 128), boxes of 16 rows x 128 bytes
+inline bool make_row_map(CUtensorMap *m, const void *base, uint64_t row_bytes, uint64_t rows) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {128, (cuuint32_t)kBlock};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+__device__ __forceinline__ void tma_rows(void *dst, const CUtensorMap *map, int x, int y,
+                                         uint64_t *bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
@@ -49,12 +100,14 @@ struct Geo {
   static constexpr int VB = DT == PA_KV_INT8 ? VE : VE / 2;   // V chunk bytes
   static constexpr int VG = D / (8 * VE);                     // V chunk groups
   static constexpr int SROW = DT == PA_KV_INT8 ? 2 : D / 16;  // scale bytes per token row
+  static constexpr bool SW = ROW % 128 == 0;                  // TMA tensor copies + swizzle
   static constexpr int CODE = kBlock * ROW;
   static constexpr int SC = kBlock * SROW;
-  static constexpr int STAGE = 2 * (CODE + SC);
-  static constexpr int NSTAGE = DT == PA_KV_INT8 ? 3 : 4;
+  static constexpr int PAYLOAD = 2 * (CODE + SC);
+  static constexpr int STAGE = SW ? (PAYLOAD + 1023) / 1024 * 1024 : PAYLOAD;
+  static constexpr int NSTAGE = 3;
   static constexpr int WARP_BYTES = NSTAGE * STAGE;
-  static constexpr int SMEM = kWarps * WARP_BYTES;
+  static constexpr int SMEM = kWarps * WARP_BYTES + (SW ? 1024 : 0);
   static_assert(KG >= 1 && VG >= 1 && CODE % 16 == 0 && SC % 16 == 0, "geometry");
   static_assert(WARP_BYTES >= 8 * D * 4, "stage area holds the warp's O for the merge");
 };
@@ -91,15 +144,25 @@ __device__ __forceinline__ uint32_t e2m1_byte_to_h2(uint32_t w, int j) {
   return e2m1x2_to_h2((w >> (8 * j)) & 0xffu);
 }
 
+// byte offset of (row, byte) in a tile stored as 16-row x 128-byte boxes
+// with the 128-byte swizzle (boxes of 2 KB, one per 128 bytes of row)
+__device__ __forceinline__ int sw_off(int row, int byte) {
+  return (byte >> 7) * (kBlock * 128) + row * 128 + ((((byte >> 4) & 7) ^ (row & 7)) << 4) +
+         (byte & 15);
+}
+
 template <int DT, int D, int R>
 __global__ void __launch_bounds__(kThreads, DT == PA_KV_NVFP4 ? 3 : 2)
-    decode_kernel(const AttnParams p) {
+    decode_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV) {
   using Gm = Geo<DT, D>;
   constexpr int KG = Gm::KG, KS = Gm::KS, VE = Gm::VE, VB = Gm::VB, VG = Gm::VG;
   constexpr int NSTAGE = Gm::NSTAGE, ROW = Gm::ROW, SROW = Gm::SROW;
   constexpr float kRescale = 8.0f;
 
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  // swizzled boxes need 1024-byte alignment
+  uint8_t *smem = Gm::SW ? smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023) : smem_raw;
   __shared__ __align__(8) uint64_t bars[kWarps][NSTAGE];
   __shared__ float s_m[kWarps][8], s_l[kWarps][8];
 
@@ -176,9 +239,18 @@ __global__ void __launch_bounds__(kThreads, DT == PA_KV_NVFP4 ? 3 : 2)
       } else {
         uint8_t *st = wsm + s * Gm::STAGE;
         const size_t tile = (size_t)phys * Hkv + kvh;
-        mbar_arrive_expect_tx(bar, Gm::STAGE);
-        bulk_g2s(st, (const uint8_t *)p.kv.k + tile * Gm::CODE, Gm::CODE, bar, pol);
-        bulk_g2s(st + Gm::CODE, (const uint8_t *)p.kv.v + tile * Gm::CODE, Gm::CODE, bar, pol);
+        mbar_arrive_expect_tx(bar, Gm::PAYLOAD);
+        if constexpr (Gm::SW) {
+          const int y = (int)(tile * kBlock);
+#pragma unroll
+          for (int x = 0; x < ROW; x += 128) {
+            tma_rows(st + x * kBlock, &tmK, x, y, bar, pol);
+            tma_rows(st + Gm::CODE + x * kBlock, &tmV, x, y, bar, pol);
+          }
+        } else {
+          bulk_g2s(st, (const uint8_t *)p.kv.k + tile * Gm::CODE, Gm::CODE, bar, pol);
+          bulk_g2s(st + Gm::CODE, (const uint8_t *)p.kv.v + tile * Gm::CODE, Gm::CODE, bar, pol);
+        }
         bulk_g2s(st + 2 * Gm::CODE, (const uint8_t *)p.kv.ks + tile * Gm::SC, Gm::SC, bar, pol);
         bulk_g2s(st + 2 * Gm::CODE + Gm::SC, (const uint8_t *)p.kv.vs + tile * Gm::SC, Gm::SC, bar,
                  pol);
@@ -225,8 +297,9 @@ __global__ void __launch_bounds__(kThreads, DT == PA_KV_NVFP4 ? 3 : 2)
 #pragma unroll
       for (int g = 0; g < KG; ++g) {
         const int boff = g * 64 + c * 16;
-        uint4 k0 = *reinterpret_cast<const uint4 *>(sK + r * ROW + boff);
-        uint4 k1 = *reinterpret_cast<const uint4 *>(sK + (r + 8) * ROW + boff);
+        const int koff = Gm::SW ? sw_off(r, boff) : r * ROW + boff;   // row r + 8: same swizzle
+        uint4 k0 = *reinterpret_cast<const uint4 *>(sK + koff);
+        uint4 k1 = *reinterpret_cast<const uint4 *>(sK + koff + 8 * (Gm::SW ? 128 : ROW));
         uint32_t w0[4] = {k0.x, k0.y, k0.z, k0.w}, w1[4] = {k1.x, k1.y, k1.z, k1.w};
         if constexpr (DT == PA_KV_INT8) {
 #pragma unroll
@@ -324,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, DT == PA_KV_NVFP4 ? 3 : 2)
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           const bool ok = tk[t] < nvalid;   // poisoned tail slots must not reach the MMA
-          const uint8_t *src = sV + tk[t] * ROW + boff;
+          const uint8_t *src = sV + (Gm::SW ? sw_off(tk[t], boff) : tk[t] * ROW + boff);
           if constexpr (VB == 16) {
             uint4 u = ok ? *reinterpret_cast<const uint4 *>(src) : make_uint4(0, 0, 0, 0);
             vw[t][0] = u.x;
@@ -434,9 +507,17 @@ template <int DT, int D, int R>
 cudaError_t launch_one(const AttnParams &p, int grid, cudaStream_t s) {
   using Gm = Geo<DT, D>;
   auto kern = decode_kernel<DT, D, R>;
+  CUtensorMap tk, tv;
+  std::memset(&tk, 0, sizeof tk);
+  std::memset(&tv, 0, sizeof tv);
+  if constexpr (Gm::SW) {
+    const uint64_t rows = (uint64_t)p.kv.num_blocks * p.kv.hkv * kBlock;
+    if (!make_row_map(&tk, p.kv.k, Gm::ROW, rows) || !make_row_map(&tv, p.kv.v, Gm::ROW, rows))
+      return cudaErrorInvalidValue;
+  }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, Gm::SMEM, s>>>(p);
+  kern<<<grid, kThreads, Gm::SMEM, s>>>(p, tk, tv);
   return cudaGetLastError();
 }
 

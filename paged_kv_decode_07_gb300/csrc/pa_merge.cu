@@ -3,15 +3,14 @@
 //
 // For one output row with partials (o_p, lse_p), lse natural-log and -inf
 // for an empty partial:  M = max lse_p,  w_p = exp(lse_p - M),
-// out = sum w_p o_p / sum w_p,  lse = M + ln sum w_p.  One warp per row;
-// lanes split the head dim in float4 chunks, so each partial row is read
+// out = sum w_p o_p / sum w_p,  lse = M + ln sum w_p.  One CTA per row;
+// threads split the head dim in float4 chunks, so each partial row is read
 // once, coalesced.
 #include "pa_internal.cuh"
 
 namespace pa {
 namespace {
 
-constexpr int kWarpsPerCta = 8;
 
 
 __device__ __forceinline__ void store4(void *out, int out_fp32, size_t off, float4 v) {
@@ -26,53 +25,101 @@ __device__ __forceinline__ void store4(void *out, int out_fp32, size_t off, floa
   }
 }
 
-// Merges `parts` partials of one row.  po points at partial 0 of the row,
-// consecutive partials `pstride` floats apart; pl likewise with lstride.
+// Merges `parts` partials of one row with one CTA of kThreads threads.
+// po points at partial 0 of the row, consecutive partials `pstride` floats
+// apart; pl likewise with lstride.  The weights exp(lse_p - M) are computed
+// once per partial into shared memory (chunks of kChunk), then every thread
+// accumulates its float4 columns over the chunk, four partials per step so
+// that the loads of one step are in flight together.
+constexpr int kThreads = 64;
+constexpr int kChunk = 512;
+
 __device__ void merge_row(const float *po, size_t pstride, const float *pl, size_t lstride,
                           int parts, int D, void *out, int out_fp32, size_t out_off,
                           float *lse_out, size_t lse_off) {
-  const int lane = threadIdx.x & 31;
+  __shared__ float s_w[kChunk];
+  __shared__ float s_red[kThreads / 32];
+  __shared__ float s_M;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   float M = kNegInf;
-  for (int q = lane; q < parts; q += 32) M = fmaxf(M, pl[(size_t)q * lstride]);
+  for (int q = tid; q < parts; q += kThreads) M = fmaxf(M, pl[(size_t)q * lstride]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) s_red[warp] = M;
+  __syncthreads();
+  if (tid == 0) {
+    float m = s_red[0];
+    for (int w = 1; w < kThreads / 32; ++w) m = fmaxf(m, s_red[w]);
+    s_M = m;
+  }
+  __syncthreads();
+  M = s_M;
   if (M == kNegInf) {
-    for (int d = lane * 4; d < D; d += 128) store4(out, out_fp32, out_off + d, make_float4(0, 0, 0, 0));
-    if (lse_out && lane == 0) lse_out[lse_off] = kNegInf;
+    for (int d = tid * 4; d < D; d += kThreads * 4)
+      store4(out, out_fp32, out_off + d, make_float4(0, 0, 0, 0));
+    if (lse_out && tid == 0) lse_out[lse_off] = kNegInf;
     return;
   }
+  constexpr int kCols = 4;   // float4 column groups per thread (D <= 1024)
+  float4 acc[kCols];
+#pragma unroll
+  for (int k = 0; k < kCols; ++k) acc[k] = make_float4(0, 0, 0, 0);
   float wsum = 0.f;
-  for (int d0 = 0; d0 < D; d0 += 128) {
-    const int d = d0 + lane * 4;
-    float4 acc = make_float4(0, 0, 0, 0);
-    float ws = 0.f;
-    for (int q = 0; q < parts; ++q) {
-      const float l = pl[(size_t)q * lstride];
-      if (l == kNegInf) continue;
-      const float w = __expf(l - M);
-      ws += w;
-      if (d < D) {
-        float4 v = *reinterpret_cast<const float4 *>(po + (size_t)q * pstride + d);
-        acc.x += w * v.x;
-        acc.y += w * v.y;
-        acc.z += w * v.z;
-        acc.w += w * v.w;
+  for (int q0 = 0; q0 < parts; q0 += kChunk) {
+    const int n = min(kChunk, parts - q0);
+    __syncthreads();
+    for (int q = tid; q < n; q += kThreads) {
+      const float l = pl[(size_t)(q0 + q) * lstride];
+      s_w[q] = (l == kNegInf) ? 0.f : __expf(l - M);
+    }
+    __syncthreads();
+    for (int q = 0; q < n; ++q) wsum += s_w[q];
+#pragma unroll
+    for (int k = 0; k < kCols; ++k) {
+      const int d = (k * kThreads + tid) * 4;
+      if (d >= D) break;
+      const float *base = po + (size_t)q0 * pstride + d;
+      int q = 0;
+      for (; q + 4 <= n; q += 4) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = *reinterpret_cast<const float4 *>(base + (size_t)(q + u) * pstride);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float w = s_w[q + u];
+          if (w != 0.f) {   // an empty partial may hold anything
+            acc[k].x += w * v[u].x;
+            acc[k].y += w * v[u].y;
+            acc[k].z += w * v[u].z;
+            acc[k].w += w * v[u].w;
+          }
+        }
+      }
+      for (; q < n; ++q) {
+        const float w = s_w[q];
+        if (w == 0.f) continue;
+        float4 v = *reinterpret_cast<const float4 *>(base + (size_t)q * pstride);
+        acc[k].x += w * v.x;
+        acc[k].y += w * v.y;
+        acc[k].z += w * v.z;
+        acc[k].w += w * v.w;
       }
     }
-    wsum = ws;
-    if (d < D) {
-      const float inv = 1.f / ws;
-      store4(out, out_fp32, out_off + d, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
-    }
   }
-  if (lse_out && lane == 0) lse_out[lse_off] = M + __logf(wsum);
+  const float inv = 1.f / wsum;
+#pragma unroll
+  for (int k = 0; k < kCols; ++k) {
+    const int d = (k * kThreads + tid) * 4;
+    if (d >= D) break;
+    store4(out, out_fp32, out_off + d,
+           make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv));
+  }
+  if (lse_out && tid == 0) lse_out[lse_off] = M + __logf(wsum);
 }
 
-// rows of a planned call: (b, i, hq)
-__global__ void __launch_bounds__(kWarpsPerCta * 32) merge_plan_kernel(const AttnParams p) {
-  const int row = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-  const int rows = p.B * p.Q * p.Hq;
-  if (row >= rows) return;
+// rows of a planned call: (b, i, hq), one CTA each
+__global__ void __launch_bounds__(kThreads) merge_plan_kernel(const AttnParams p) {
+  const int row = blockIdx.x;
   const int hq = row % p.Hq;
   const int bi = row / p.Hq;
   const int i = bi % p.Q, b = bi / p.Q;
@@ -85,10 +132,9 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) merge_plan_kernel(const Att
   // parts == 0: nothing to attend.  A plan that did not fit the workspace
   // (flagged by the planner; no item ran) must not read past the slots.
   if (ui.parts == 0 || ui.slot_base < 0 || ui.slot_base + ui.parts > p.max_slots) {
-    const int lane = threadIdx.x & 31;
-    for (int d = lane * 4; d < D; d += 128)
+    for (int d = threadIdx.x * 4; d < D; d += kThreads * 4)
       store4(p.out, p.out_fp32, (size_t)row * D + d, make_float4(0, 0, 0, 0));
-    if (p.lse_out && lane == 0) p.lse_out[row] = kNegInf;
+    if (p.lse_out && threadIdx.x == 0) p.lse_out[row] = kNegInf;
     return;
   }
   const size_t slot_rows = (size_t)p.kv.hkv * p.R;
@@ -98,11 +144,10 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) merge_plan_kernel(const Att
 }
 
 // public pa_merge: part_out [S, R, D], part_lse [S, R]
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
+__global__ void __launch_bounds__(kThreads)
     merge_dense_kernel(const float *po, const float *pl, int S, int R, int D, void *out,
                        int out_fp32, float *lse_out) {
-  const int row = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-  if (row >= R) return;
+  const int row = blockIdx.x;
   merge_row(po + (size_t)row * D, (size_t)R * D, pl + row, (size_t)R, S, D, out, out_fp32,
             (size_t)row * D, lse_out, row);
 }
@@ -110,17 +155,17 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
 }  // namespace
 
 cudaError_t launch_merge_plan(const AttnParams &p, cudaStream_t s) {
-  const int rows = p.B * p.Q * p.Hq;
+  const long long rows = (long long)p.B * p.Q * p.Hq;
   if (rows == 0) return cudaSuccess;
-  merge_plan_kernel<<<(rows + kWarpsPerCta - 1) / kWarpsPerCta, kWarpsPerCta * 32, 0, s>>>(p);
+  if (rows > 0x7fffffffLL) return cudaErrorInvalidValue;
+  merge_plan_kernel<<<(unsigned)rows, kThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_merge_dense(const float *po, const float *pl, int S, int R, int D, void *out,
                                int out_fp32, float *lse_out, cudaStream_t s) {
   if (R == 0) return cudaSuccess;
-  merge_dense_kernel<<<(R + kWarpsPerCta - 1) / kWarpsPerCta, kWarpsPerCta * 32, 0, s>>>(
-      po, pl, S, R, D, out, out_fp32, lse_out);
+  merge_dense_kernel<<<R, kThreads, 0, s>>>(po, pl, S, R, D, out, out_fp32, lse_out);
   return cudaGetLastError();
 }
 
