@@ -153,7 +153,7 @@ int pa_decode(const pa_kv_cache *kv, const pa_problem *prob, const pa_options *o
  * point.  Same arguments, semantics and results as pa_decode with default
  * options.  Returns PA_ERR_WORKSPACE_TOO_SMALL, with nothing launched, when
  * the call would need more workspace than PA_NOALLOC_SCRATCH_BYTES (about
- * (batch + 300) * Hkv * G * D * 4 bytes for the default plan).  The
+ * (2 * batch + 300) * Hkv * G * D * 4 bytes for the default plan).  The
  * first call on each device (with that device current) looks up the
  * array's device address; make that first call before any stream capture.
  * All calls share the array: calls that can overlap on the GPU race.  The

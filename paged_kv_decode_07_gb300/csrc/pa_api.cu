@@ -80,8 +80,10 @@ Layout make_layout(const pa_kv_cache *kv, const pa_problem *p, const pa_options 
   } else {
     const int target = (o && o->target_items > 0) ? std::min(o->target_items, kMaxTargetItems)
                                                   : kMaxTargetItems;
-    items = (long long)target + (long long)Hkv * L.U;
-    slots = (long long)ceil_div(target, Hkv) + L.U + 1;
+    // one partition per unit beyond the target, plus one more per unit for
+    // sequences whose query rows share the longest row's partition bounds
+    items = (long long)target + 2LL * Hkv * L.U;
+    slots = (long long)ceil_div(target, Hkv) + 2LL * L.U + 1;
     // never more partitions than blocks
     items = std::min(items, (long long)Hkv * L.U * std::max(1, maxblk));
     slots = std::min(slots, (long long)L.U * std::max(1, maxblk));

@@ -139,9 +139,23 @@ __device__ __forceinline__ uint32_t s8pair_to_h2(uint32_t x, int pair) {
   return *reinterpret_cast<uint32_t *>(&r);
 }
 
-// byte j (two E2M1 codes) of a word -> f16x2, exact
-__device__ __forceinline__ uint32_t e2m1_byte_to_h2(uint32_t w, int j) {
-  return e2m1x2_to_h2((w >> (8 * j)) & 0xffu);
+// the four bytes (eight E2M1 codes) of a word -> four f16x2, exact; byte j
+// -> h[j], low nibble in the low half.  The word is unpacked into byte
+// registers once instead of shifting and masking per byte.
+__device__ __forceinline__ void e2m1x8_to_h2x4(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+// two E4M3 bytes -> f16x2 (lo, hi), exact
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t lo, uint32_t hi) {
+  uint32_t r;
+  uint16_t pair = (uint16_t)(lo | (hi << 8));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(pair));
+  return r;
 }
 
 // byte offset of (row, byte) in a tile stored as 16-row x 128-byte boxes
@@ -315,13 +329,16 @@ __global__ void __launch_bounds__(kThreads, DT == PA_KV_NVFP4 ? 3 : 2)
           const uint32_t sc10 = e4m3_to_h2_dup(sKs[(r + 8) * SROW + sb]);
           const uint32_t sc11 = e4m3_to_h2_dup(sKs[(r + 8) * SROW + sb + 1]);
 #pragma unroll
-          for (int s2 = 0; s2 < KS; ++s2) {   // elements 4 s2 .. 4 s2 + 3 = bytes 2 s2, 2 s2 + 1
-            const int wi = s2 >> 1, bj = (s2 & 1) * 2;
-            const uint32_t a_s = s2 < KS / 2 ? sc00 : sc01, b_s = s2 < KS / 2 ? sc10 : sc11;
-            mma16816(sacc, hmul2_u32(e2m1_byte_to_h2(w0[wi], bj), a_s),
-                     hmul2_u32(e2m1_byte_to_h2(w1[wi], bj), b_s),
-                     hmul2_u32(e2m1_byte_to_h2(w0[wi], bj + 1), a_s),
-                     hmul2_u32(e2m1_byte_to_h2(w1[wi], bj + 1), b_s), qf[g][s2][0], qf[g][s2][1]);
+          for (int wi = 0; wi < 4; ++wi) {   // word wi = k-steps 2 wi, 2 wi + 1
+            uint32_t h0[4], h1[4];
+            e2m1x8_to_h2x4(w0[wi], h0);
+            e2m1x8_to_h2x4(w1[wi], h1);
+            const uint32_t a_s = wi < 2 ? sc00 : sc01, b_s = wi < 2 ? sc10 : sc11;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)   // k-step 2 wi + hh = bytes 2 hh, 2 hh + 1
+              mma16816(sacc, hmul2_u32(h0[2 * hh], a_s), hmul2_u32(h1[2 * hh], b_s),
+                       hmul2_u32(h0[2 * hh + 1], a_s), hmul2_u32(h1[2 * hh + 1], b_s),
+                       qf[g][2 * wi + hh][0], qf[g][2 * wi + hh][1]);
           }
         }
       }
@@ -393,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, DT == PA_KV_NVFP4 ? 3 : 2)
       for (int g = 0; g < VG; ++g) {
         const int boff = g * 8 * VB + r * VB;
         uint32_t vw[4][VB / 4];
-        uint32_t vsc[4][2];
+        uint32_t vsb[4][2];   // NVFP4: raw E4M3 scale bytes of the lane's 1-2 blocks
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           const bool ok = tk[t] < nvalid;   // poisoned tail slots must not reach the MMA
@@ -411,28 +428,48 @@ __global__ void __launch_bounds__(kThreads, DT == PA_KV_NVFP4 ? 3 : 2)
           }
           if constexpr (DT == PA_KV_NVFP4) {
             const int sb = (g * 8 * VE + r * VE) / 16;
-            vsc[t][0] = ok ? e4m3_to_h2_dup(sVs[tk[t] * SROW + sb]) : 0u;
-            vsc[t][1] = (ok && VE > 16) ? e4m3_to_h2_dup(sVs[tk[t] * SROW + sb + 1]) : vsc[t][0];
+            vsb[t][0] = ok ? sVs[tk[t] * SROW + sb] : 0u;
+            vsb[t][1] = (ok && VE > 16) ? sVs[tk[t] * SROW + sb + 1] : vsb[t][0];
           } else {
-            vw[t][0] ^= 0x80808080u;   // int8 -> offset-binary for the f16 magic
 #pragma unroll
-            for (int q = 1; q < VB / 4; ++q) vw[t][q] ^= 0x80808080u;
-            (void)vsc;
+            for (int q = 0; q < VB / 4; ++q) vw[t][q] ^= 0x80808080u;   // offset-binary
+            (void)vsb;
           }
         }
+        if constexpr (DT == PA_KV_NVFP4) {
+          // Token pairs (2c, 2c+1) and (2c+8, 2c+9): interleave their nibbles so
+          // that byte e of X holds (token a, token b) at head-dim row r and
+          // byte e of Y the same at row r + 8 -- each cvt then yields an A
+          // register directly.
+          uint32_t sp[2][2];
 #pragma unroll
-        for (int e = 0; e < VE / 2; ++e) {
-          uint32_t h[4];
+          for (int pr2 = 0; pr2 < 2; ++pr2)
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            if constexpr (DT == PA_KV_NVFP4) {
-              h[t] = hmul2_u32(e2m1_byte_to_h2(vw[t][e >> 2], e & 3), vsc[t][e >= 8 ? 1 : 0]);
-            } else {
-              h[t] = s8pair_to_h2(vw[t][e >> 1], e & 1);   // a zeroed slot decodes to 0
+            for (int k = 0; k < 2; ++k) sp[pr2][k] = e4m3x2_to_h2(vsb[2 * pr2][k], vsb[2 * pr2 + 1][k]);
+#pragma unroll
+          for (int wq = 0; wq < VB / 4; ++wq) {
+            uint32_t xa[4], ya[4], xb[4], yb[4];
+            e2m1x8_to_h2x4((vw[0][wq] & 0x0F0F0F0Fu) | ((vw[1][wq] << 4) & 0xF0F0F0F0u), xa);
+            e2m1x8_to_h2x4(((vw[0][wq] >> 4) & 0x0F0F0F0Fu) | (vw[1][wq] & 0xF0F0F0F0u), ya);
+            e2m1x8_to_h2x4((vw[2][wq] & 0x0F0F0F0Fu) | ((vw[3][wq] << 4) & 0xF0F0F0F0u), xb);
+            e2m1x8_to_h2x4(((vw[2][wq] >> 4) & 0x0F0F0F0Fu) | (vw[3][wq] & 0xF0F0F0F0u), yb);
+#pragma unroll
+            for (int j2 = 0; j2 < 4; ++j2) {
+              const int e = wq * 4 + j2;
+              const int k = e >= 8 ? 1 : 0;
+              mma16816(o[g][e], hmul2_u32(xa[j2], sp[0][k]), hmul2_u32(ya[j2], sp[0][k]),
+                       hmul2_u32(xb[j2], sp[1][k]), hmul2_u32(yb[j2], sp[1][k]), B0, B1);
             }
           }
-          mma16816(o[g][e], prmt(h[0], h[1], 0x5410), prmt(h[0], h[1], 0x7632),
-                   prmt(h[2], h[3], 0x5410), prmt(h[2], h[3], 0x7632), B0, B1);
+        } else {
+#pragma unroll
+          for (int e = 0; e < VE / 2; ++e) {
+            uint32_t h[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) h[t] = s8pair_to_h2(vw[t][e >> 1], e & 1);   // zeroed slot -> 0
+            mma16816(o[g][e], prmt(h[0], h[1], 0x5410), prmt(h[0], h[1], 0x7632),
+                     prmt(h[2], h[3], 0x5410), prmt(h[2], h[3], 0x7632), B0, B1);
+          }
         }
       }
     }

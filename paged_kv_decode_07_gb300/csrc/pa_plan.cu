@@ -25,6 +25,12 @@ namespace {
 
 constexpr int kThreads = 1024;
 
+// A group is one sequence: in virtual mode with q_len > 1 its q_len units
+// share partition boundaries (taken from the group's longest unit), and its
+// items are ordered (part, query row, kv head) so the q_len reads of the
+// same key blocks run back to back and hit L2.
+__device__ __forceinline__ int group_size(const PlanParams &p) { return p.virt ? p.Q : 1; }
+
 __device__ __forceinline__ int unit_len(const PlanParams &p, int u, uint32_t &err) {
   int b = p.virt ? u / p.Q : u;
   int i = p.virt ? u % p.Q : p.Q - 1;
@@ -106,7 +112,9 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
   }
   __syncthreads();
 
-  // sweep 1: total key blocks
+  const int GS = group_size(p);
+  const int NG = p.B;                    // groups = sequences
+  // sweep 1: total key blocks over all units (the work the kernel streams)
   uint32_t err = 0;
   unsigned long long tot = 0;
   for (int u = tid; u < U; u += kThreads) {
@@ -133,25 +141,30 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
   __syncthreads();
   const int W = s_W;
 
-  // sweep 2: multi-part units (items + slots), then single-part units
+  // sweep 2: per group, partitions from its longest unit; multi-part groups
+  // get items and slots first, single-part groups after
   int2 carry = make_int2(0, 0);
-  for (int base = 0; base < U; base += kThreads) {
-    int u = base + tid;
+  for (int base = 0; base < NG; base += kThreads) {
+    const int g = base + tid;
     uint32_t e2 = 0;
-    int n = u < U ? unit_len(p, u, e2) : 0;
-    int nblk = (n + kBlock - 1) / kBlock;
-    int parts = nblk ? (nblk + W - 1) / W : 0;
-    int multi = parts > 1;
-    int2 v = make_int2(multi ? parts * p.hkv : 0, multi ? parts : 0);
+    int nmax = 0;
+    if (g < NG)
+      for (int i = 0; i < GS; ++i) nmax = max(nmax, unit_len(p, g * GS + i, e2));
+    const int nblk = (nmax + kBlock - 1) / kBlock;
+    const int parts = nblk ? (nblk + W - 1) / W : 0;
+    const int multi = parts > 1;
+    int2 v = make_int2(multi ? parts * GS * p.hkv : 0, multi ? parts * GS : 0);
     int2 ex = block_scan2(v, s_tot);
-    if (u < U) {
-      p.prefix_a[u] = carry.x + ex.x;
-      UnitInfo ui;
-      ui.parts = parts;
-      ui.slot_base = multi ? carry.y + ex.y : -1;
-      ui.nblk = nblk;
-      ui.len = n;
-      p.units[u] = ui;
+    if (g < NG) {
+      p.prefix_a[g] = carry.x + ex.x;
+      for (int i = 0; i < GS; ++i) {
+        UnitInfo ui;
+        ui.parts = parts;
+        ui.slot_base = multi ? carry.y + ex.y + i * parts : -1;
+        ui.nblk = nblk;
+        ui.len = unit_len(p, g * GS + i, e2);
+        p.units[g * GS + i] = ui;
+      }
     }
     __syncthreads();
     carry.x += s_tot.x;
@@ -160,13 +173,13 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
   }
   const int items_a = carry.x, slots = carry.y;
   int2 carry_b = make_int2(0, 0);
-  for (int base = 0; base < U; base += kThreads) {
-    int u = base + tid;
+  for (int base = 0; base < NG; base += kThreads) {
+    const int g = base + tid;
     int single = 0;
-    if (u < U) single = p.units[u].parts == 1;
-    int2 v = make_int2(single ? p.hkv : 0, 0);
+    if (g < NG) single = p.units[g * GS].parts == 1;
+    int2 v = make_int2(single ? GS * p.hkv : 0, 0);
     int2 ex = block_scan2(v, s_tot);
-    if (u < U) p.prefix_b[u] = carry_b.x + ex.x;
+    if (g < NG) p.prefix_b[g] = carry_b.x + ex.x;
     __syncthreads();
     carry_b.x += s_tot.x;
     __syncthreads();
@@ -180,19 +193,22 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
   }
   __syncthreads();
 
-  // sweep 3: write the items
+  // sweep 3: write the items, (part, query row, kv head) within a group
+  const int per_part = GS * p.hkv;
   for (int j = tid; j < num_items; j += kThreads) {
-    int u, local;
+    int g, local;
     if (j < items_a) {
-      u = upper_bound_minus1(p.prefix_a, U, j);
-      local = j - p.prefix_a[u];
+      g = upper_bound_minus1(p.prefix_a, NG, j);
+      local = j - p.prefix_a[g];
     } else {
-      u = upper_bound_minus1(p.prefix_b, U, j - items_a);
-      local = j - items_a - p.prefix_b[u];
+      g = upper_bound_minus1(p.prefix_b, NG, j - items_a);
+      local = j - items_a - p.prefix_b[g];
     }
-    UnitInfo ui = p.units[u];
-    int part = local / p.hkv, kvh = local % p.hkv;
-    int chunk = (ui.nblk + ui.parts - 1) / ui.parts;
+    const int part = local / per_part, rem = local % per_part;
+    const int i = rem / p.hkv, kvh = rem % p.hkv;
+    const int u = g * GS + i;
+    const UnitInfo ui = p.units[u];
+    const int chunk = (ui.nblk + ui.parts - 1) / ui.parts;
     WorkItem it;
     it.unit = u;
     it.kvh = kvh;
