@@ -27,6 +27,22 @@ int tc_supported(int dtype, int D, int R) {
          R <= 8 && (R == 1 || R % 2 == 0);
 }
 
+cudaError_t launch_verify_int8(const AttnParams &p, int grid, cudaStream_t s);
+cudaError_t launch_verify_nvfp4(const AttnParams &p, int grid, cudaStream_t s);
+
+cudaError_t launch_verify_dense(const AttnParams &p, int grid, cudaStream_t s) {
+  switch (p.kv.dtype) {
+    case PA_KV_INT8: return launch_verify_int8(p, grid, s);
+    case PA_KV_NVFP4: return launch_verify_nvfp4(p, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+// dense verify tile: quantised formats, D = 256, q_len * G <= 48
+int dense_supported(int dtype, int D, int Q, int G) {
+  return (dtype == PA_KV_INT8 || dtype == PA_KV_NVFP4) && D == 256 && Q > 1 && Q * G <= 48;
+}
+
 cudaError_t launch_decode_simt(const AttnParams &p, int grid, cudaStream_t s) {
   switch (p.kv.dtype) {
     case PA_KV_BF16: return launch_decode_simt_bf16(p, grid, s);
@@ -167,26 +183,30 @@ int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *
   st = check_problem(kv, p, verify ? kMaxQLen : 1);
   if (st) return st;
   const int kernel = o ? o->kernel : 0;
-  if (kernel < 0 || kernel > 2) return PA_ERR_INVALID_ARG;
+  if (kernel < 0 || kernel > 3) return PA_ERR_INVALID_ARG;
   if (o && (o->split_blocks < 0 || o->target_items < 0)) return PA_ERR_INVALID_ARG;
   if (p->batch == 0) return PA_OK;
   const int G = p->num_q_heads / kv->num_kv_heads;
-  // Kernel choice.  Both kernels run verify as a virtual batch (one unit per
-  // query token, its own key limit).  auto: tensor cores for the quantised
-  // formats (the CUDA cores cannot issue their dequant + 3,072 FMA per token
-  // and kv head at HBM speed), CUDA cores for bf16.
-  const bool virt = true;
-  bool use_tc;
-  if (kernel == 2) {
+  // Kernel choice.  auto: tensor cores for the quantised formats (the CUDA
+  // cores cannot issue their dequant + 3,072 FMA per token and kv head at
+  // HBM speed), CUDA cores for bf16.  Verify (q_len > 1) on the tensor cores
+  // runs as one dense tile of q_len * G rows when supported; otherwise every
+  // kernel runs it as a virtual batch (one unit per query token).
+  const int Q = p->q_len;
+  bool use_tc, dense = false;
+  if (kernel == 2 || kernel == 3) {
     if (!tc_supported(kv->dtype, kv->head_dim, G)) return PA_ERR_UNSUPPORTED;
     use_tc = true;
+    dense = kernel == 2 && dense_supported(kv->dtype, kv->head_dim, Q, G);
   } else if (kernel == 1) {
     if (!simt_supported(kv->dtype, kv->head_dim, G)) return PA_ERR_UNSUPPORTED;
     use_tc = false;
   } else {
     use_tc = tc_supported(kv->dtype, kv->head_dim, G);
     if (!use_tc && !simt_supported(kv->dtype, kv->head_dim, G)) return PA_ERR_UNSUPPORTED;
+    dense = use_tc && dense_supported(kv->dtype, kv->head_dim, Q, G);
   }
+  const bool virt = !dense;
   if (!ws) return PA_ERR_INVALID_ARG;
   if (!aligned16(ws)) return PA_ERR_INVALID_ARG;
   const Layout L = make_layout(kv, p, o, virt);
@@ -241,8 +261,9 @@ int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *
   if (o && o->event_begin &&
       cudaEventRecord(static_cast<cudaEvent_t>(o->event_begin), stream) != cudaSuccess)
     return PA_ERR_CUDA;
-  if ((use_tc ? launch_decode_tc(ap, L.max_items, stream)
-              : launch_decode_simt(ap, L.max_items, stream)) != cudaSuccess)
+  if ((dense ? launch_verify_dense(ap, L.max_items, stream)
+             : use_tc ? launch_decode_tc(ap, L.max_items, stream)
+                      : launch_decode_simt(ap, L.max_items, stream)) != cudaSuccess)
     return PA_ERR_CUDA;
   if (o && o->event_end &&
       cudaEventRecord(static_cast<cudaEvent_t>(o->event_end), stream) != cudaSuccess)

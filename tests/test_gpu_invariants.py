@@ -140,3 +140,28 @@ def test_two_shards_merged_equal_single_call():
     full, _ = run(wl, out_fp32=True)
     np.testing.assert_allclose(merged.cpu().numpy(), full.reshape(-1, wl.D).cpu().numpy(),
                                atol=2e-5, rtol=0)
+
+
+@pytest.mark.parametrize("dt", ["nvfp4", "int8"])
+def test_dense_verify_invariants(dt):
+    """Dense-tile verify: bitwise block-permutation invariance and
+    determinism; forced single / tiny partitions agree with the oracle; a bad
+    block id is skipped and flagged."""
+    name = "nvfp4_verify_q8_b4_ctx64k_d256" if dt == "nvfp4" else "int8_b32_l1k_32k_d256"
+    wl = W.make_workload(name, device=DEV, seq_lens=[1500, 8, 300], Q=8)
+    a, la, ws = run(wl, "verify", out_fp32=True, return_lse=True, kernel=2)
+    b, lb, _ = run(wl, "verify", out_fp32=True, return_lse=True, kernel=2)
+    assert torch.equal(a, b) and torch.equal(la, lb)
+    c, _ = run(W.permute_pool(wl, seed=5), "verify", out_fp32=True, kernel=2)
+    assert torch.equal(a, c)
+    ref, _ = oracle_rows(wl)
+    for kw in (dict(split_blocks=1 << 20), dict(split_blocks=1), dict(target_items=5)):
+        o, _ = run(wl, "verify", out_fp32=True, kernel=2, **kw)
+        compare(o, ref, f"dense verify {dt} {kw}")
+    bad = wl.block_tables.clone()
+    bad[0, 7] = -1
+    o, ws = run(W.Workload(**{**wl.__dict__, "block_tables": bad}), "verify", out_fp32=True,
+                kernel=2)
+    torch.cuda.synchronize()
+    assert pa.read_error(ws) & pa.PA_ERRF_BAD_BLOCK_ID
+    assert torch.isfinite(o).all()

@@ -35,8 +35,9 @@ def _fn(wl):
 
 
 def _kernels(dtype):
-    """0 = auto; 1 = CUDA-core kernel; 2 = tensor-core kernel (quantised formats)."""
-    return [0, 1, 2] if dtype in ("int8", "nvfp4") else [0, 1]
+    """0 = auto; 1 = CUDA-core kernel; 2 = tensor-core kernel (verify: dense
+    tile); 3 = tensor-core kernel with verify as one unit per query token."""
+    return [0, 1, 2, 3] if dtype in ("int8", "nvfp4") else [0, 1]
 
 
 REDUCED_CASES = [(n, k) for n in REDUCED for k in _kernels(W.spec(n)["dtype"])]
@@ -118,10 +119,12 @@ def test_gqa_and_head_dim_variants(dt, kernel, shape):
     compare_lse(lse, ref_l, f"{dt} {shape}")
 
 
-@pytest.mark.parametrize("Q", [2, 5, 16])
-@pytest.mark.parametrize("kernel", [1, 2])
-def test_verify_q_lens(Q, kernel):
-    wl = W.make_workload("nvfp4_verify_q8_b4_ctx64k_d256", device=DEV, seq_lens=[900, Q, 33], Q=Q)
+@pytest.mark.parametrize("Q", [2, 5, 8, 16])
+@pytest.mark.parametrize("kernel", [1, 2, 3])
+@pytest.mark.parametrize("dt", ["nvfp4", "int8"])
+def test_verify_q_lens(Q, kernel, dt):
+    name = "nvfp4_verify_q8_b4_ctx64k_d256" if dt == "nvfp4" else "int8_b32_l1k_32k_d256"
+    wl = W.make_workload(name, device=DEV, seq_lens=[900, Q, 33, 3000], Q=Q)
     o32, lse, _ = run(wl, "verify", out_fp32=True, return_lse=True, kernel=kernel)
     ref_o, ref_l = oracle_rows(wl)
     compare(o32, ref_o, f"verify Q={Q}")
