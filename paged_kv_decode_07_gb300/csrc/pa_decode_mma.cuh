@@ -105,7 +105,8 @@ struct Geo {
   static constexpr int SC = kBlock * SROW;
   static constexpr int PAYLOAD = 2 * (CODE + SC);
   static constexpr int STAGE = SW ? (PAYLOAD + 1023) / 1024 * 1024 : PAYLOAD;
-  static constexpr int NSTAGE = 3;
+  // int8: 2 stages so that 3 CTAs (12 warps) fit per SM; NVFP4: 3 stages
+  static constexpr int NSTAGE = DT == PA_KV_INT8 ? 2 : 3;
   static constexpr int WARP_BYTES = NSTAGE * STAGE;
   static constexpr int SMEM = kWarps * WARP_BYTES + (SW ? 1024 : 0);
   static_assert(KG >= 1 && VG >= 1 && CODE % 16 == 0 && SC % 16 == 0, "geometry");
@@ -166,7 +167,7 @@ __device__ __forceinline__ int sw_off(int row, int byte) {
 }
 
 template <int DT, int D, int R>
-__global__ void __launch_bounds__(kThreads, DT == PA_KV_NVFP4 ? 3 : 2)
+__global__ void __launch_bounds__(kThreads, 3)
     decode_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV) {
   using Gm = Geo<DT, D>;

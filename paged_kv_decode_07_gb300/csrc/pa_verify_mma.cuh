@@ -54,7 +54,10 @@ struct Geo {
   static constexpr int NSTAGE = 8;
   static constexpr int NC = 8 * NT;                       // columns (rows of Q)
   static constexpr int EPO = NT / 2;                      // entries per owner lane per token
-  static constexpr int SBUF = kWarps * kWarps * kBlock * 2 * NT * 4;   // partial scores
+  // partial scores [src warp][token][owner][EST]: EST = 2 NT + 2 floats makes
+  // the 16 float2 stores of a half-warp hit 32 distinct banks
+  static constexpr int EST = 2 * NT + 2;
+  static constexpr int SBUF = kWarps * kBlock * kWarps * EST * 4;
   static constexpr int PBUF = NC * kBlock * 2;            // P, f16 [col][16 tokens]
   static constexpr int SMEM = NSTAGE * STAGE + SBUF + PBUF + 1024;
 };
@@ -233,8 +236,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     // ---- 2. reduce-scatter the partials: owner of column pair index c is warp c
     {
-      float *dst0 = sbuf + (((c * kWarps + warp) * kBlock + r) * 2 * NT);
-      float *dst1 = sbuf + (((c * kWarps + warp) * kBlock + r + 8) * 2 * NT);
+      constexpr int EST = Gm::EST;
+      float *dst0 = sbuf + (((warp * kBlock + r) * kWarps + c) * EST);
+      float *dst1 = sbuf + (((warp * kBlock + r + 8) * kWarps + c) * EST);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         *reinterpret_cast<float2 *>(dst0 + 2 * nt) = make_float2(sp[nt][0], sp[nt][1]);
@@ -259,8 +263,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       float a0 = 0.f, a1 = 0.f;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        a0 += sbuf[((warp * kWarps + w) * kBlock + r) * 2 * NT + e];
-        a1 += sbuf[((warp * kWarps + w) * kBlock + r + 8) * 2 * NT + e];
+        a0 += sbuf[((w * kBlock + r) * kWarps + warp) * Gm::EST + e];
+        a1 += sbuf[((w * kBlock + r + 8) * kWarps + warp) * Gm::EST + e];
       }
       sc[k][0] = a0;
       sc[k][1] = a1;
