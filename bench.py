@@ -77,10 +77,14 @@ def kernel_source_hash() -> str:
 def profiled_traffic(workload: str):
     """dram bytes per launch of the attention kernel from the committed ncu
     summary for this workload, or None if absent or taken on other source."""
-    path = os.path.join(ROOT, "profiles", f"decode_{workload}.md")
-    try:
-        lines = open(path).read().splitlines()
-    except OSError:
+    lines = None
+    for kind in ("decode", "verify"):
+        try:
+            lines = open(os.path.join(ROOT, "profiles", f"{kind}_{workload}.md")).read().splitlines()
+            break
+        except OSError:
+            continue
+    if lines is None:
         return None
     vals = {}
     for ln in lines:
