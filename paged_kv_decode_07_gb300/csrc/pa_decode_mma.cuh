@@ -181,6 +181,8 @@ __global__ void __launch_bounds__(kThreads, 3)
   __shared__ __align__(8) uint64_t bars[kWarps][NSTAGE];
   __shared__ float s_m[kWarps][8], s_l[kWarps][8];
 
+  griddep_launch();   // the merge may start launching once every CTA has begun
+  griddep_wait();     // the plan of this call is complete
   const uint32_t num_items = p.hdr[HDR_NUM_ITEMS];
   if (blockIdx.x >= num_items) return;
   const WorkItem it = p.items[blockIdx.x];
@@ -555,8 +557,7 @@ cudaError_t launch_one(const AttnParams &p, int grid, cudaStream_t s) {
   }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, Gm::SMEM, s>>>(p, tk, tv);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, kThreads, Gm::SMEM, s, p, tk, tv);
 }
 
 template <int DT>

@@ -109,6 +109,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p)
   __shared__ __align__(16) float red[kWarps][8];
   __shared__ float s_m[kWarps][8], s_l[kWarps][8];
 
+  griddep_launch();   // the merge may start launching once every CTA has begun
+  griddep_wait();     // the plan of this call is complete
   const uint32_t num_items = p.hdr[HDR_NUM_ITEMS];
   if (blockIdx.x >= num_items) return;
   const WorkItem it = p.items[blockIdx.x];
@@ -483,8 +485,7 @@ cudaError_t launch_one(const AttnParams &p, int grid, cudaStream_t s) {
   auto kern = decode_kernel<DT, D, R>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, Gm::SMEM, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, kThreads, Gm::SMEM, s, p);
 }
 
 template <int DT>

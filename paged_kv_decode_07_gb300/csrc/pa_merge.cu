@@ -119,6 +119,7 @@ __device__ void merge_row(const float *po, size_t pstride, const float *pl, size
 
 // rows of a planned call: (b, i, hq), one CTA each
 __global__ void __launch_bounds__(kThreads) merge_plan_kernel(const AttnParams p) {
+  griddep_wait();   // the attention kernel's outputs and partials are complete
   const int row = blockIdx.x;
   const int hq = row % p.Hq;
   const int bi = row / p.Hq;
@@ -158,8 +159,7 @@ cudaError_t launch_merge_plan(const AttnParams &p, cudaStream_t s) {
   const long long rows = (long long)p.B * p.Q * p.Hq;
   if (rows == 0) return cudaSuccess;
   if (rows > 0x7fffffffLL) return cudaErrorInvalidValue;
-  merge_plan_kernel<<<(unsigned)rows, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(merge_plan_kernel, (unsigned)rows, kThreads, 0, s, p);
 }
 
 cudaError_t launch_merge_dense(const float *po, const float *pl, int S, int R, int D, void *out,

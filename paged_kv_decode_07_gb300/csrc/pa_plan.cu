@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
   __shared__ uint32_t s_err;
   __shared__ int2 s_tot;
   __shared__ int s_W;
+  griddep_launch();   // the attention kernel may launch now; it waits for this grid to finish
   const int tid = threadIdx.x;
   const int U = p.virt ? p.B * p.Q : p.B;
   if (tid == 0) {

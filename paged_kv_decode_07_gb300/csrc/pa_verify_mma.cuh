@@ -80,6 +80,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ float s_l[NC], s_m[NC];
   __shared__ int s_fail;
 
+  griddep_launch();   // the merge may start launching once every CTA has begun
+  griddep_wait();     // the plan of this call is complete
   const uint32_t num_items = p.hdr[HDR_NUM_ITEMS];
   if (blockIdx.x >= num_items) return;
   const WorkItem it = p.items[blockIdx.x];
@@ -456,8 +458,7 @@ cudaError_t launch_one(const AttnParams &p, int grid, cudaStream_t s) {
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, Gm::SMEM, s>>>(p, tk, tv);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, kThreads, Gm::SMEM, s, p, tk, tv);
 }
 
 inline int n_tiles(int R) {
