@@ -122,9 +122,9 @@ typedef struct pa_problem {
 /* Optional knobs; pass NULL for defaults. */
 typedef struct pa_options {
   int32_t kernel;          /* 0 auto; 1 CUDA-core (SIMT) kernel; 2 tensor-core kernel
-                              (verify: one dense tile of q_len * G rows when the format is
-                              int8/NVFP4, head_dim 256 and q_len * G <= 48); 3 tensor-core
-                              kernel with verify run as one unit per query token */
+                              (verify: dense tiles of 16 of the q_len * G rows when the
+                              format is int8/NVFP4 and head_dim 256); 3 tensor-core kernel
+                              with verify run as one unit per query token */
   int32_t split_blocks;    /* 0 auto; >0 = fixed number of 16-token blocks per partition
                               (a value >= the longest sequence's block count disables
                               split-K) */

@@ -38,9 +38,11 @@ cudaError_t launch_verify_dense(const AttnParams &p, int grid, cudaStream_t s) {
   return cudaErrorInvalidValue;
 }
 
-// dense verify tile: quantised formats, D = 256, q_len * G <= 48
+// dense verify tiles (row groups of 16 of the q_len * G rows): quantised
+// formats, D = 256
 int dense_supported(int dtype, int D, int Q, int G) {
-  return (dtype == PA_KV_INT8 || dtype == PA_KV_NVFP4) && D == 256 && Q > 1 && Q * G <= 48;
+  (void)G;
+  return (dtype == PA_KV_INT8 || dtype == PA_KV_NVFP4) && D == 256 && Q > 1;
 }
 
 cudaError_t launch_decode_simt(const AttnParams &p, int grid, cudaStream_t s) {
@@ -81,12 +83,17 @@ int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
 // Workspace regions for one plan mode.  `target` is the item target the
 // call uses (auto: the maximum, so the bound holds for any choice).
-Layout make_layout(const pa_kv_cache *kv, const pa_problem *p, const pa_options *o, bool virt) {
+// verify row groups: up to kMaxRowGroup rows (a multiple of 16) per group
+int group_rows(int Q, int G) { return std::min(kMaxRowGroup, (Q * G + 15) / 16 * 16); }
+int row_groups(int Q, int G) { return (Q * G + group_rows(Q, G) - 1) / group_rows(Q, G); }
+
+// mode: 1 virtual (unit per query token), 2 row groups of up to 48 rows
+Layout make_layout(const pa_kv_cache *kv, const pa_problem *p, const pa_options *o, int mode) {
   Layout L;
   const int B = p->batch, Q = p->q_len, Hkv = kv->num_kv_heads;
   const int G = p->num_q_heads / Hkv;
-  L.U = virt ? B * Q : B;
-  L.R = virt ? G : Q * G;
+  L.U = mode == 1 ? B * Q : B * row_groups(Q, G);
+  L.R = mode == 1 ? G : group_rows(Q, G);
   const int maxblk = ceil_div(std::max(p->max_seq_len, 0), kBlock);
   long long items, slots;
   if (o && o->split_blocks > 0) {
@@ -206,10 +213,11 @@ int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *
     if (!use_tc && !simt_supported(kv->dtype, kv->head_dim, G)) return PA_ERR_UNSUPPORTED;
     dense = use_tc && dense_supported(kv->dtype, kv->head_dim, Q, G);
   }
-  const bool virt = !dense;
+  const int mode = dense ? 2 : 1;   // dense verify runs as row groups of up to 48 rows
+  const int RG = dense ? row_groups(Q, G) : 1;
   if (!ws) return PA_ERR_INVALID_ARG;
   if (!aligned16(ws)) return PA_ERR_INVALID_ARG;
-  const Layout L = make_layout(kv, p, o, virt);
+  const Layout L = make_layout(kv, p, o, mode);
   if (ws_bytes < L.total) return PA_ERR_WORKSPACE_TOO_SMALL;
 
   uint8_t *w = static_cast<uint8_t *>(ws);
@@ -218,7 +226,8 @@ int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *
   pp.seq_lens = p->seq_lens;
   pp.B = p->batch;
   pp.Q = p->q_len;
-  pp.virt = virt;
+  pp.virt = mode;
+  pp.RG = RG;
   pp.hkv = kv->num_kv_heads;
   pp.capacity = (int)std::min<long long>((long long)p->block_table_stride * kBlock, 1LL << 30);
   pp.target_items = (o && o->target_items > 0) ? std::min(o->target_items, kMaxTargetItems) : 1184;
@@ -254,7 +263,8 @@ int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *
   ap.part_lse = reinterpret_cast<float *>(w + L.part_lse);
   ap.max_items = L.max_items;
   ap.max_slots = L.max_slots;
-  ap.virt = virt;
+  ap.virt = mode;
+  ap.RG = RG;
   ap.R = L.R;
 
   if (launch_plan(pp, stream) != cudaSuccess) return PA_ERR_CUDA;
@@ -282,8 +292,9 @@ size_t pa_workspace_bytes(const pa_kv_cache *kv, const pa_problem *prob, const p
     return 0;
   if (prob->num_q_heads < 1 || prob->num_q_heads % kv->num_kv_heads) return 0;
   if (opt && (opt->split_blocks < 0 || opt->target_items < 0)) return 0;
-  const Layout a = make_layout(kv, prob, opt, true);
-  const Layout b = make_layout(kv, prob, opt, false);
+  const Layout a = make_layout(kv, prob, opt, 1);
+  if (prob->q_len == 1) return a.total;   // decode never uses the row-group layout
+  const Layout b = make_layout(kv, prob, opt, 2);
   return std::max(a.total, b.total);
 }
 

@@ -36,9 +36,12 @@ struct KvView {
   float kg, vg;
 };
 
-// A plan "unit" is a (sequence, query-row group).  Virtual mode: one unit
-// per (b, i) query token with its own key limit; dense mode: one unit per
-// sequence holding all q_len rows.
+// A plan "unit" is a (sequence, query-row group).  Mode 1 (virtual): one
+// unit per (b, i) query token with its own key limit; mode 0 (dense): one
+// unit per sequence holding all q_len * G rows; mode 2 (row groups): one
+// unit per (b, group of R consecutive rows of the q_len * G), R a multiple
+// of 16 up to kMaxRowGroup.
+constexpr int kMaxRowGroup = 48;
 struct UnitInfo {      // int4 in the workspace
   int parts;           // partitions (0 = nothing to attend)
   int slot_base;       // first partial slot (parts > 1), else -1
@@ -71,13 +74,15 @@ struct AttnParams {
   float *part_lse;          // [slot][Hkv][R]
   int max_items;
   int max_slots;
-  int virt;                 // 1 = virtual mode (unit = b*Q + i), 0 = dense mode
-  int R;                    // rows per item: G (virtual) or Q*G (dense)
+  int virt;                 // plan mode: 1 virtual, 0 dense, 2 row groups
+  int R;                    // rows per item: G (virtual), Q*G (dense), rows per group (mode 2)
+  int RG;                   // row groups per sequence (mode 2), else 1
 };
 
 struct PlanParams {
   const int *seq_lens;
   int B, Q, virt, hkv;
+  int RG;                   // row groups per sequence (mode 2), else 1
   int capacity;             // 16 * stride
   int target_items, split_blocks, min_split_blocks;
   int max_items, max_slots;

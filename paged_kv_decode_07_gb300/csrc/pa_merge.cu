@@ -125,8 +125,18 @@ __global__ void __launch_bounds__(kThreads) merge_plan_kernel(const AttnParams p
   const int bi = row / p.Hq;
   const int i = bi % p.Q, b = bi / p.Q;
   const int g = hq % p.G, kvh = hq / p.G;
-  const int u = p.virt ? b * p.Q + i : b;
-  const int r = p.virt ? g : i * p.G + g;
+  int u, r;
+  if (p.virt == 1) {
+    u = b * p.Q + i;
+    r = g;
+  } else if (p.virt == 2) {
+    const int gr = i * p.G + g;   // row of the sequence's q_len * G
+    u = b * p.RG + gr / p.R;
+    r = gr % p.R;
+  } else {
+    u = b;
+    r = i * p.G + g;
+  }
   const UnitInfo ui = p.units[u];
   const int D = p.kv.D;
   if (ui.parts == 1) return;   // written by the attention kernel

@@ -29,11 +29,13 @@ constexpr int kThreads = 1024;
 // share partition boundaries (taken from the group's longest unit), and its
 // items are ordered (part, query row, kv head) so the q_len reads of the
 // same key blocks run back to back and hit L2.
-__device__ __forceinline__ int group_size(const PlanParams &p) { return p.virt ? p.Q : 1; }
+__device__ __forceinline__ int group_size(const PlanParams &p) {
+  return p.virt == 1 ? p.Q : (p.virt == 2 ? p.RG : 1);
+}
 
 __device__ __forceinline__ int unit_len(const PlanParams &p, int u, uint32_t &err) {
-  int b = p.virt ? u / p.Q : u;
-  int i = p.virt ? u % p.Q : p.Q - 1;
+  const int b = u / group_size(p);
+  const int i = p.virt == 1 ? u % p.Q : p.Q - 1;   // row groups see up to the last query
   int L = p.seq_lens[b];
   if (L < 0) {
     err |= PA_ERRF_NEG_LEN;
@@ -106,7 +108,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
   __shared__ int s_W;
   griddep_launch();   // the attention kernel may launch now; it waits for this grid to finish
   const int tid = threadIdx.x;
-  const int U = p.virt ? p.B * p.Q : p.B;
+  const int U = p.B * group_size(p);
   if (tid == 0) {
     s_total = 0;
     s_err = 0;

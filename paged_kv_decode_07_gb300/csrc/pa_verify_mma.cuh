@@ -1,6 +1,8 @@
-// pa_verify_mma.cuh -- speculative verify as one dense tensor-core tile per
-// (sequence, kv head, key range): Q query tokens x G heads = R rows (R <= 48)
-// share every key block, so the scores S^T [16 tokens x R] = K Q^T and the
+// pa_verify_mma.cuh -- speculative verify as dense tensor-core tiles per
+// (sequence, row group, kv head, key range): the Q query tokens x G heads
+// rows share every key block; groups hold up to 48 rows (beyond that the
+// planner keeps a sequence's groups adjacent so their key reads hit L2).
+// The scores S^T [16 tokens x R] = K Q^T and the
 // update O^T [D x R] += V^T P^T are dense contractions ("vLLM All-NVFP4
 // DFlash2 for Blackwell", "What makes this stack different": DFlash2 K=7, 8
 // query tokens per verify step; causal among the new tokens: the virtual
@@ -44,7 +46,7 @@ constexpr int DS = D / kWarps;   // head-dim slice per warp
 template <int DT, int NT>
 struct Geo {
   static_assert(DT == PA_KV_INT8 || DT == PA_KV_NVFP4, "quantised formats");
-  static_assert(NT % 2 == 0 && NT <= 6, "even n-tile count, R <= 48");
+  static_assert(NT % 2 == 0 && NT <= 6, "even n-tile count");
   static constexpr int ROW = DT == PA_KV_INT8 ? D : D / 2;
   static constexpr int SROW = DT == PA_KV_INT8 ? 2 : D / 16;
   static constexpr int CODE = kBlock * ROW;
@@ -63,7 +65,7 @@ struct Geo {
 };
 
 template <int DT, int NT>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, NT == 2 ? 4 : 2)
     verify_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV) {
   using Gm = Geo<DT, NT>;
@@ -88,7 +90,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = lane >> 2, c = lane & 3;
-  const int b = it.unit, kvh = it.kvh, Q = p.Q, G = p.G, R = p.R, Hkv = p.kv.hkv;
+  // unit = (sequence, row group): rows ro .. ro + R - 1 of the sequence's Q * G
+  const int b = it.unit / p.RG, ro = (it.unit % p.RG) * p.R;
+  const int kvh = it.kvh, Q = p.Q, G = p.G, Hkv = p.kv.hkv;
+  const int R = min(p.R, Q * G - ro);   // live rows of this group
   const int L = p.units[it.unit].len;   // keys of the sequence (the last row's limit)
 
   // ---- Q fragments of this warp's head-dim slice, all n-tiles
@@ -97,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   for (int nt = 0; nt < NT; ++nt) {
     const int n = nt * 8 + r;
     const bool live = n < R;
-    const int qi = live ? n / G : 0, g = live ? n % G : 0;
+    const int qi = live ? (ro + n) / G : 0, g = live ? (ro + n) % G : 0;
     const __nv_bfloat16 *qrow = p.q + (((size_t)b * Q + qi) * p.Hq + (size_t)kvh * G + g) * D;
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
@@ -117,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   for (int k = 0; k < EPO; ++k) {
     const int e = c * EPO + k;
     ocol[k] = (e >> 1) * 8 + 2 * warp + (e & 1);
-    const int qi = ocol[k] / G;
+    const int qi = (ro + ocol[k]) / G;
     olim[k] = ocol[k] < R ? L - Q + 1 + qi : 0;   // keys visible to that query row
   }
   float m_run[EPO], l_run[EPO];
@@ -419,9 +424,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (n >= R) continue;
       const float Lr = s_l[n];
       const float inv = Lr > 0.f ? vg / Lr : 0.f;
-      const int qi = n / G, g = n % G;
+      const int qi = (ro + n) / G, g = (ro + n) % G;
       const size_t orow = ((size_t)b * Q + qi) * p.Hq + (size_t)kvh * G + g;
-      const size_t prow = ((size_t)it.slot * Hkv + kvh) * R + n;
+      const size_t prow = ((size_t)it.slot * Hkv + kvh) * p.R + n;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int d = warp * DS + r * 8 + 2 * e;
@@ -461,17 +466,12 @@ cudaError_t launch_one(const AttnParams &p, int grid, cudaStream_t s) {
   return launch_pdl(kern, grid, kThreads, Gm::SMEM, s, p, tk, tv);
 }
 
-inline int n_tiles(int R) {
-  const int nt = (R + 7) / 8;
-  return nt + (nt & 1);
-}
-
 template <int DT>
 cudaError_t launch_dtype(const AttnParams &p, int grid, cudaStream_t s) {
-  switch (n_tiles(p.R)) {
-    case 2: return launch_one<DT, 2>(p, grid, s);
-    case 4: return launch_one<DT, 4>(p, grid, s);
-    case 6: return launch_one<DT, 6>(p, grid, s);
+  switch (p.R) {   // rows per group -> n-tiles of 8 columns
+    case 16: return launch_one<DT, 2>(p, grid, s);
+    case 32: return launch_one<DT, 4>(p, grid, s);
+    case 48: return launch_one<DT, 6>(p, grid, s);
   }
   return cudaErrorInvalidValue;
 }
