@@ -43,6 +43,8 @@ def kv_bytes_per_token_head(dtype: str, D: int) -> int:
         return 2 * D * 2
     if dtype == "int8":
         return 2 * (D + 2)
+    if dtype == "fp8":
+        return 2 * D
     return 2 * (D // 2 + D // 16)
 
 
@@ -393,7 +395,7 @@ def run_ours(args, world, rank, local):
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": {"bf16": "bf16", "int8": "int8", "nvfp4": "nvfp4"}[wl.dtype] + "-kv/fp32-acc",
+            "dtype": wl.dtype + "-kv/fp32-acc",
             "data": "synthetic",
             "config": {"workload": args.workload, "batch": wl.B, "q_len": wl.Q,
                        "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": wl.D,

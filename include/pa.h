@@ -35,6 +35,11 @@
  *                 DFlash2 for Blackwell", "What makes this stack
  *                 different": NVFP4 KV cache; UE4M3 block scales: "vLLM
  *                 Fork with focus on GB10 Homelabs", "Acknowledgments").
+ *   PA_KV_FP8   : k/v uint8 [NB, Hkv, 16, D], FP8-E4M3 codes; no scale tensors;
+ *                 k/v_global_scale fp32 per tensor; value = e4m3(code) * global
+ *                 (FP8 KV with inline dequant: "vLLM Fork with focus on GB10
+ *                 Homelabs", "Acknowledgments"; "vLLM All-NVFP4 DFlash2 for
+ *                 Blackwell", "What makes this stack different").
  *
  * Conventions for every entry point:
  *   - Pointers are DEVICE pointers unless marked (host).  Every data
@@ -77,7 +82,7 @@ typedef enum {
   PA_ERR_CUDA = -4                  /* a CUDA runtime call or launch failed */
 } pa_status;
 
-typedef enum { PA_KV_BF16 = 0, PA_KV_INT8 = 1, PA_KV_NVFP4 = 2 } pa_kv_dtype;
+typedef enum { PA_KV_BF16 = 0, PA_KV_INT8 = 1, PA_KV_NVFP4 = 2, PA_KV_FP8 = 3 } pa_kv_dtype;
 
 /* Device error flags (pa_read_error). */
 #define PA_ERRF_BAD_BLOCK_ID      0x1u  /* table entry outside [0, num_blocks): block skipped */
@@ -96,9 +101,9 @@ typedef struct pa_kv_cache {
   int32_t head_dim;       /* D */
   const void *k_cache;    /* layouts: see the format list above */
   const void *v_cache;
-  const void *k_scale;    /* NULL for bf16 */
+  const void *k_scale;    /* NULL for bf16 and FP8 */
   const void *v_scale;
-  float k_global_scale;   /* (host) NVFP4 per-tensor scale; ignored otherwise */
+  float k_global_scale;   /* (host) NVFP4 / FP8 per-tensor scale; ignored otherwise */
   float v_global_scale;
 } pa_kv_cache;
 
@@ -186,7 +191,7 @@ int pa_merge(const float *part_out, const float *part_lse, int32_t S, int32_t R,
  * attention kernels do, writing fp32 k_out / v_out [B, Hkv, max_seq_len, D]
  * (positions t >= seq_len, and blocks with an out-of-range id, are 0).
  * The values are bit-exact: bf16 widened; int8 (float)code * (float)scale;
- * NVFP4 fp32_round((e2m1 * e4m3) * global).  ws may be NULL; if given (>=
+ * NVFP4 fp32_round((e2m1 * e4m3) * global); FP8 fp32_round(e4m3 * global).  ws may be NULL; if given (>=
  * 256 bytes) its header receives the device error flags. */
 int pa_dequant_gather(const pa_kv_cache *kv, const int32_t *block_tables,
                       int32_t block_table_stride, const int32_t *seq_lens, int32_t batch,

@@ -25,7 +25,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-DTYPES = {"bf16": 0, "int8": 1, "nvfp4": 2}
+DTYPES = {"bf16": 0, "int8": 1, "nvfp4": 2, "fp8": 3}
 
 
 def build(force: bool = False) -> str:

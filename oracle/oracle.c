@@ -44,6 +44,9 @@
  *           "Acknowledgments").  Element 2i of a byte pair is the low
  *           nibble.  e2m1 * e4m3 is exact in fp32, so the value is one
  *           fp32 rounding of the product with g -- block scale first.
+ *   FP8   : value = RN_fp32( e4m3(code) * g ), one fp32 g per cache tensor
+ *           (FP8 KV with inline dequant, "vLLM Fork with focus on GB10
+ *           Homelabs", "Acknowledgments").
  *   The fp32 dequantised value is widened to double for the attention.
  *
  * Build: gcc -O2 -std=c11 -fPIC -shared -ffp-contract=off -pthread
@@ -55,7 +58,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { OR_BF16 = 0, OR_INT8 = 1, OR_NVFP4 = 2 };
+enum { OR_BF16 = 0, OR_INT8 = 1, OR_NVFP4 = 2, OR_FP8 = 3 };
 
 typedef struct {
   int32_t dtype;
@@ -131,6 +134,11 @@ static float dequant(const oracle_cache *c, int which, int64_t blk, int head, in
       float prod = (float)(oracle_e2m1_value(code) * oracle_e4m3_value(sc));
       float g = which ? c->v_global : c->k_global;
       return prod * g;
+    }
+    case OR_FP8: {
+      float e = (float)oracle_e4m3_value(((const uint8_t *)data)[row * D + d]);
+      float g = which ? c->v_global : c->k_global;
+      return e * g;
     }
   }
   return NAN;

@@ -10,30 +10,36 @@ namespace pa {
 cudaError_t launch_decode_simt_bf16(const AttnParams &p, int grid, cudaStream_t s);
 cudaError_t launch_decode_simt_int8(const AttnParams &p, int grid, cudaStream_t s);
 cudaError_t launch_decode_simt_nvfp4(const AttnParams &p, int grid, cudaStream_t s);
+cudaError_t launch_decode_simt_fp8(const AttnParams &p, int grid, cudaStream_t s);
 
 cudaError_t launch_decode_tc_int8(const AttnParams &p, int grid, cudaStream_t s);
 cudaError_t launch_decode_tc_nvfp4(const AttnParams &p, int grid, cudaStream_t s);
+cudaError_t launch_decode_tc_fp8(const AttnParams &p, int grid, cudaStream_t s);
 
 cudaError_t launch_decode_tc(const AttnParams &p, int grid, cudaStream_t s) {
   switch (p.kv.dtype) {
     case PA_KV_INT8: return launch_decode_tc_int8(p, grid, s);
     case PA_KV_NVFP4: return launch_decode_tc_nvfp4(p, grid, s);
+    case PA_KV_FP8: return launch_decode_tc_fp8(p, grid, s);
   }
   return cudaErrorInvalidValue;
 }
 
 int tc_supported(int dtype, int D, int R) {
-  return (dtype == PA_KV_INT8 || dtype == PA_KV_NVFP4) && (D == 128 || D == 256) && R >= 1 &&
+  return (dtype == PA_KV_INT8 || dtype == PA_KV_NVFP4 || dtype == PA_KV_FP8) &&
+         (D == 128 || D == 256) && R >= 1 &&
          R <= 8 && (R == 1 || R % 2 == 0);
 }
 
 cudaError_t launch_verify_int8(const AttnParams &p, int grid, cudaStream_t s);
 cudaError_t launch_verify_nvfp4(const AttnParams &p, int grid, cudaStream_t s);
+cudaError_t launch_verify_fp8(const AttnParams &p, int grid, cudaStream_t s);
 
 cudaError_t launch_verify_dense(const AttnParams &p, int grid, cudaStream_t s) {
   switch (p.kv.dtype) {
     case PA_KV_INT8: return launch_verify_int8(p, grid, s);
     case PA_KV_NVFP4: return launch_verify_nvfp4(p, grid, s);
+    case PA_KV_FP8: return launch_verify_fp8(p, grid, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -42,7 +48,7 @@ cudaError_t launch_verify_dense(const AttnParams &p, int grid, cudaStream_t s) {
 // formats, D = 256
 int dense_supported(int dtype, int D, int Q, int G) {
   (void)G;
-  return (dtype == PA_KV_INT8 || dtype == PA_KV_NVFP4) && D == 256 && Q > 1;
+  return (dtype == PA_KV_INT8 || dtype == PA_KV_NVFP4 || dtype == PA_KV_FP8) && D == 256 && Q > 1;
 }
 
 cudaError_t launch_decode_simt(const AttnParams &p, int grid, cudaStream_t s) {
@@ -50,6 +56,7 @@ cudaError_t launch_decode_simt(const AttnParams &p, int grid, cudaStream_t s) {
     case PA_KV_BF16: return launch_decode_simt_bf16(p, grid, s);
     case PA_KV_INT8: return launch_decode_simt_int8(p, grid, s);
     case PA_KV_NVFP4: return launch_decode_simt_nvfp4(p, grid, s);
+    case PA_KV_FP8: return launch_decode_simt_fp8(p, grid, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -134,17 +141,17 @@ Layout make_layout(const pa_kv_cache *kv, const pa_problem *p, const pa_options 
 
 int check_kv(const pa_kv_cache *kv) {
   if (!kv) return PA_ERR_INVALID_ARG;
-  if (kv->dtype < PA_KV_BF16 || kv->dtype > PA_KV_NVFP4) return PA_ERR_INVALID_ARG;
+  if (kv->dtype < PA_KV_BF16 || kv->dtype > PA_KV_FP8) return PA_ERR_INVALID_ARG;
   if (kv->block_size != kBlock) return PA_ERR_UNSUPPORTED;
   if (kv->head_dim != 128 && kv->head_dim != 256) return PA_ERR_UNSUPPORTED;
   if (kv->num_kv_heads < 1 || kv->num_blocks < 1) return PA_ERR_INVALID_ARG;
   if (!kv->k_cache || !kv->v_cache) return PA_ERR_INVALID_ARG;
   if (!aligned16(kv->k_cache) || !aligned16(kv->v_cache)) return PA_ERR_INVALID_ARG;
-  if (kv->dtype != PA_KV_BF16) {
+  if (kv->dtype == PA_KV_INT8 || kv->dtype == PA_KV_NVFP4) {
     if (!kv->k_scale || !kv->v_scale) return PA_ERR_INVALID_ARG;
     if (!aligned16(kv->k_scale) || !aligned16(kv->v_scale)) return PA_ERR_INVALID_ARG;
   }
-  if (kv->dtype == PA_KV_NVFP4 &&
+  if ((kv->dtype == PA_KV_NVFP4 || kv->dtype == PA_KV_FP8) &&
       (!std::isfinite(kv->k_global_scale) || !std::isfinite(kv->v_global_scale)))
     return PA_ERR_INVALID_ARG;
   return PA_OK;
@@ -178,8 +185,9 @@ KvView view_of(const pa_kv_cache *kv) {
   v.v = kv->v_cache;
   v.ks = kv->k_scale;
   v.vs = kv->v_scale;
-  v.kg = kv->dtype == PA_KV_NVFP4 ? kv->k_global_scale : 1.0f;
-  v.vg = kv->dtype == PA_KV_NVFP4 ? kv->v_global_scale : 1.0f;
+  const bool global = kv->dtype == PA_KV_NVFP4 || kv->dtype == PA_KV_FP8;
+  v.kg = global ? kv->k_global_scale : 1.0f;
+  v.vg = global ? kv->v_global_scale : 1.0f;
   return v;
 }
 

@@ -1,6 +1,6 @@
 // pa_decode_mma.cuh -- split-K paged decode attention on the tensor cores
-// (mma.sync m16n8k16, f16 operands, fp32 accumulation) for the int8 and
-// NVFP4 KV formats.
+// (mma.sync m16n8k16, f16 operands, fp32 accumulation) for the int8,
+// NVFP4 and FP8-E4M3 KV formats.
 //
 // Why tensor cores for decode: with GQA the G query heads of one kv head
 // share every key and value, so per (token, kv head) the scores and the PV
@@ -17,8 +17,9 @@
 //   O^T [D x 8 heads]        += V^T [D x 16] . P^T [16 x 8]   (M = head dim)
 // with G <= 8 query heads in the N = 8 columns.  Operand fragments are
 // built straight from the quantised codes in shared memory, dequantised in
-// registers to f16 (exact for both formats: int8 codes, and e2m1 * e4m3
-// products with at most 6 significant bits).  Because a dot product does
+// registers to f16 (exact for all three formats: int8 codes, e2m1 * e4m3
+// products with at most 6 significant bits, and E4M3 values, whose range
+// 2^-9 .. 448 and 4 significant bits f16 holds).  Because a dot product does
 // not care in which order it visits the head dim, each lane reads 16
 // contiguous bytes of a key row and the query fragments use the same
 // permuted head-dim order; for PV the head-dim rows are permuted the same
@@ -26,8 +27,9 @@
 // layout is turned into PV's B fragment with 8 shuffles per block.
 // Scales: int8 per-token scales multiply the score (K) and the
 // probability (V); the NVFP4 block scale multiplies the f16 codes (one
-// exact f16x2 multiply per pair); softmax_scale * log2 e and the NVFP4
-// global scales are applied in fp32 outside the MMAs, so q stays exact.
+// exact f16x2 multiply per pair); softmax_scale * log2 e and the NVFP4 /
+// FP8 per-tensor scales are applied in fp32 outside the MMAs, so q stays
+// exact.
 #pragma once
 
 #include <cuda.h>
@@ -91,22 +93,25 @@ constexpr int kThreads = kWarps * 32;
 
 template <int DT, int D>
 struct Geo {
-  static_assert(DT == PA_KV_INT8 || DT == PA_KV_NVFP4, "quantised formats only");
-  static constexpr int ROW = DT == PA_KV_INT8 ? D : D / 2;    // code bytes per token row
-  static constexpr int E = DT == PA_KV_INT8 ? 16 : 32;        // elements per 16 bytes
+  static_assert(DT == PA_KV_INT8 || DT == PA_KV_NVFP4 || DT == PA_KV_FP8,
+                "quantised formats only");
+  static constexpr bool BYTE_CODES = DT != PA_KV_NVFP4;       // one byte per element
+  static constexpr int ROW = BYTE_CODES ? D : D / 2;          // code bytes per token row
+  static constexpr int E = BYTE_CODES ? 16 : 32;              // elements per 16 bytes
   static constexpr int KG = D / (4 * E);                      // K chunks per lane
   static constexpr int KS = E / 4;                            // k-steps per K chunk
   static constexpr int VE = (8 * E <= D) ? E : D / 8;         // V elements per lane chunk
-  static constexpr int VB = DT == PA_KV_INT8 ? VE : VE / 2;   // V chunk bytes
+  static constexpr int VB = BYTE_CODES ? VE : VE / 2;        // V chunk bytes
   static constexpr int VG = D / (8 * VE);                     // V chunk groups
-  static constexpr int SROW = DT == PA_KV_INT8 ? 2 : D / 16;  // scale bytes per token row
+  // scale bytes per token row (FP8 has only the per-tensor scale)
+  static constexpr int SROW = DT == PA_KV_INT8 ? 2 : (DT == PA_KV_NVFP4 ? D / 16 : 0);
   static constexpr bool SW = ROW % 128 == 0;                  // TMA tensor copies + swizzle
   static constexpr int CODE = kBlock * ROW;
   static constexpr int SC = kBlock * SROW;
   static constexpr int PAYLOAD = 2 * (CODE + SC);
   static constexpr int STAGE = SW ? (PAYLOAD + 1023) / 1024 * 1024 : PAYLOAD;
-  // int8: 2 stages so that 3 CTAs (12 warps) fit per SM; NVFP4: 3 stages
-  static constexpr int NSTAGE = DT == PA_KV_INT8 ? 2 : 3;
+  // byte formats: 2 stages so that 3 CTAs (12 warps) fit per SM; NVFP4: 3
+  static constexpr int NSTAGE = BYTE_CODES ? 2 : 3;
   static constexpr int WARP_BYTES = NSTAGE * STAGE;
   static constexpr int SMEM = kWarps * WARP_BYTES + (SW ? 1024 : 0);
   static_assert(KG >= 1 && VG >= 1 && CODE % 16 == 0 && SC % 16 == 0, "geometry");
@@ -215,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         qf[g][s][1] = f2_to_h2(x1.x, x1.y);
       }
   }
-  const float qscale = p.scale_log2 * (DT == PA_KV_NVFP4 ? p.kv.kg : 1.0f);
+  const float qscale = p.scale_log2 * (has_global_scale(DT) ? p.kv.kg : 1.0f);
 
   // ---- this warp's blocks
   const int t_begin = it.blk_begin * kBlock;
@@ -268,9 +273,11 @@ __global__ void __launch_bounds__(kThreads, 3)
           bulk_g2s(st, (const uint8_t *)p.kv.k + tile * Gm::CODE, Gm::CODE, bar, pol);
           bulk_g2s(st + Gm::CODE, (const uint8_t *)p.kv.v + tile * Gm::CODE, Gm::CODE, bar, pol);
         }
-        bulk_g2s(st + 2 * Gm::CODE, (const uint8_t *)p.kv.ks + tile * Gm::SC, Gm::SC, bar, pol);
-        bulk_g2s(st + 2 * Gm::CODE + Gm::SC, (const uint8_t *)p.kv.vs + tile * Gm::SC, Gm::SC, bar,
-                 pol);
+        if constexpr (Gm::SC > 0) {
+          bulk_g2s(st + 2 * Gm::CODE, (const uint8_t *)p.kv.ks + tile * Gm::SC, Gm::SC, bar, pol);
+          bulk_g2s(st + 2 * Gm::CODE + Gm::SC, (const uint8_t *)p.kv.vs + tile * Gm::SC, Gm::SC,
+                   bar, pol);
+        }
       }
     }
   };
@@ -325,6 +332,12 @@ __global__ void __launch_bounds__(kThreads, 3)
             mma16816(sacc, s8pair_to_h2(x0, 0), s8pair_to_h2(x1, 0), s8pair_to_h2(x0, 1),
                      s8pair_to_h2(x1, 1), qf[g][s2][0], qf[g][s2][1]);
           }
+        } else if constexpr (DT == PA_KV_FP8) {
+#pragma unroll
+          for (int s2 = 0; s2 < KS; ++s2)   // bytes 0,1 of word s2 -> k rows 2c, 2c+1
+            mma16816(sacc, e4m3x2_u16_to_h2(w0[s2]), e4m3x2_u16_to_h2(w1[s2]),
+                     e4m3x2_u16_to_h2(w0[s2] >> 16), e4m3x2_u16_to_h2(w1[s2] >> 16),
+                     qf[g][s2][0], qf[g][s2][1]);
         } else {
           const int sb = (g * 4 * Gm::E + c * Gm::E) / 16;   // first 16-element scale block
           const uint32_t sc00 = e4m3_to_h2_dup(sKs[r * SROW + sb]);
@@ -433,9 +446,11 @@ __global__ void __launch_bounds__(kThreads, 3)
             const int sb = (g * 8 * VE + r * VE) / 16;
             vsb[t][0] = ok ? sVs[tk[t] * SROW + sb] : 0u;
             vsb[t][1] = (ok && VE > 16) ? sVs[tk[t] * SROW + sb + 1] : vsb[t][0];
-          } else {
+          } else if constexpr (DT == PA_KV_INT8) {
 #pragma unroll
             for (int q = 0; q < VB / 4; ++q) vw[t][q] ^= 0x80808080u;   // offset-binary
+            (void)vsb;
+          } else {
             (void)vsb;
           }
         }
@@ -463,6 +478,19 @@ __global__ void __launch_bounds__(kThreads, 3)
               mma16816(o[g][e], hmul2_u32(xa[j2], sp[0][k]), hmul2_u32(ya[j2], sp[0][k]),
                        hmul2_u32(xb[j2], sp[1][k]), hmul2_u32(yb[j2], sp[1][k]), B0, B1);
             }
+          }
+        } else if constexpr (DT == PA_KV_FP8) {
+          // Interleave the bytes of token pairs (2c, 2c+1) and (2c+8, 2c+9) so
+          // that each 16-bit half is (token a, token b) at one head-dim row:
+          // one cvt per A register.  Element pair e = bytes 2(e%2), 2(e%2)+1
+          // of word e/2.
+#pragma unroll
+          for (int e = 0; e < VE / 2; ++e) {
+            const uint32_t sel = (e & 1) ? 0x7362u : 0x5140u;
+            const uint32_t xa = prmt(vw[0][e >> 1], vw[1][e >> 1], sel);
+            const uint32_t xb = prmt(vw[2][e >> 1], vw[3][e >> 1], sel);
+            mma16816(o[g][e], e4m3x2_u16_to_h2(xa), e4m3x2_u16_to_h2(xa >> 16),
+                     e4m3x2_u16_to_h2(xb), e4m3x2_u16_to_h2(xb >> 16), B0, B1);
           }
         } else {
 #pragma unroll
@@ -511,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   __syncthreads();
 
   // ---- merge the warps and write (rows h < R)
-  const float vg = DT == PA_KV_NVFP4 ? p.kv.vg : 1.0f;
+  const float vg = has_global_scale(DT) ? p.kv.vg : 1.0f;
   const int G = p.G;
   for (int idx = threadIdx.x; idx < R * D; idx += kThreads) {
     const int h = idx / D, d = idx % D;

@@ -51,9 +51,10 @@ struct Geo {
   static constexpr int TB = (D == 256) ? 2 : 1;  // log2(LPR) - 3
   static constexpr int TOK = 8 * RG;           // tokens per warp iteration (one stage)
   static constexpr int IPB = kBlock / TOK;     // iterations per 16-token block
-  static constexpr int ROW_BYTES = DT == PA_KV_BF16 ? 2 * D : (DT == PA_KV_INT8 ? D : D / 2);
+  static constexpr int ROW_BYTES =
+      DT == PA_KV_BF16 ? 2 * D : ((DT == PA_KV_INT8 || DT == PA_KV_FP8) ? D : D / 2);
   static constexpr int CODE_BYTES = TOK * ROW_BYTES;
-  static constexpr int SROW_BYTES = DT == PA_KV_BF16 ? 0 : (DT == PA_KV_INT8 ? 2 : D / 16);
+  static constexpr int SROW_BYTES = DT == PA_KV_INT8 ? 2 : (DT == PA_KV_NVFP4 ? D / 16 : 0);
   static constexpr int SCALE_BYTES = TOK * SROW_BYTES;
   static constexpr int STAGE = 2 * (CODE_BYTES + SCALE_BYTES);
   static constexpr int NSTAGE = DT == PA_KV_NVFP4 ? 6 : 3;
@@ -63,7 +64,8 @@ struct Geo {
 };
 
 // 8 consecutive head-dim values of token row t of a stage, as 4 float2.
-// int8: raw codes (scale applied by the caller); NVFP4: e2m1 * block scale.
+// int8: raw codes (scale applied by the caller); NVFP4: e2m1 * block scale;
+// FP8: e4m3 values (the per-tensor scale is folded into q and the output).
 template <int DT, int D>
 __device__ __forceinline__ void load8(const uint8_t *codes, const uint8_t *scales, int t, int dl,
                                       float2 (&f)[4]) {
@@ -74,6 +76,12 @@ __device__ __forceinline__ void load8(const uint8_t *codes, const uint8_t *scale
     f[1] = bf16x2_to_f2(u.y);
     f[2] = bf16x2_to_f2(u.z);
     f[3] = bf16x2_to_f2(u.w);
+  } else if constexpr (DT == PA_KV_FP8) {
+    uint2 u = *reinterpret_cast<const uint2 *>(codes + t * G_::ROW_BYTES + dl * 8);
+    f[0] = h2u_to_f2(e4m3x2_u16_to_h2(u.x));
+    f[1] = h2u_to_f2(e4m3x2_u16_to_h2(u.x >> 16));
+    f[2] = h2u_to_f2(e4m3x2_u16_to_h2(u.y));
+    f[3] = h2u_to_f2(e4m3x2_u16_to_h2(u.y >> 16));
   } else if constexpr (DT == PA_KV_INT8) {
     uint2 u = *reinterpret_cast<const uint2 *>(codes + t * G_::ROW_BYTES + dl * 8);
     float x[8];
@@ -128,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p)
   // ---- query slice in registers, pre-scaled
   float2 q2[R][4];
   {
-    float qs = p.scale_log2 * (DT == PA_KV_NVFP4 ? p.kv.kg : 1.0f);
+    float qs = p.scale_log2 * (has_global_scale(DT) ? p.kv.kg : 1.0f);
     const __nv_bfloat16 *qb = p.q + (((size_t)b * Q + qi) * p.Hq + (size_t)kvh * p.G) * D + dl * 8;
 #pragma unroll
     for (int h = 0; h < R; ++h) {
@@ -188,11 +196,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p)
         const size_t tile = (size_t)phys * Hkv + kvh;
         const size_t code_off = tile * kBlock * Gm::ROW_BYTES + (size_t)sub * Gm::CODE_BYTES;
         uint32_t bytes = 2 * Gm::CODE_BYTES;
-        if constexpr (DT != PA_KV_BF16) bytes += 2 * Gm::SCALE_BYTES;
+        if constexpr (has_scale_tensors(DT)) bytes += 2 * Gm::SCALE_BYTES;
         mbar_arrive_expect_tx(bar, bytes);
         bulk_g2s(st, (const uint8_t *)p.kv.k + code_off, Gm::CODE_BYTES, bar, pol);
         bulk_g2s(st + Gm::CODE_BYTES, (const uint8_t *)p.kv.v + code_off, Gm::CODE_BYTES, bar, pol);
-        if constexpr (DT != PA_KV_BF16) {
+        if constexpr (has_scale_tensors(DT)) {
           const size_t sc_off = tile * kBlock * Gm::SROW_BYTES + (size_t)sub * Gm::SCALE_BYTES;
           bulk_g2s(st + 2 * Gm::CODE_BYTES, (const uint8_t *)p.kv.ks + sc_off, Gm::SCALE_BYTES, bar,
                    pol);
@@ -447,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p)
   __syncthreads();
 
   // ---- merge the warps and write
-  const float vg = DT == PA_KV_NVFP4 ? p.kv.vg : 1.0f;
+  const float vg = has_global_scale(DT) ? p.kv.vg : 1.0f;
   const int G = p.G;
   for (int idx = threadIdx.x; idx < R * D; idx += kThreads) {
     const int h = idx / D, d = idx % D;

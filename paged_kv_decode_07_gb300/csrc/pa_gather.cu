@@ -5,6 +5,7 @@
 //   bf16  : widened exactly.
 //   int8  : (float)code * (float)scale_fp16                  (exact product)
 //   NVFP4 : ((e2m1 * e4m3) computed in f16, exact) * global (one fp32 round)
+//   FP8   : e4m3 (exact in f16) * global                     (one fp32 round)
 // PagedAttention addressing (Kwon et al., cited on "vLLM Fork with focus on
 // GB10 Homelabs", "About"): token t of sequence b is slot t % 16 of block
 // block_tables[b][t / 16].
@@ -63,6 +64,17 @@ __global__ void gather_kernel(KvView kv, const int *tables, int stride, const in
           const float s = fp16_bits_to_f(reinterpret_cast<const uint16_t *>(sc)[row]);
 #pragma unroll
           for (int j = 0; j < 8; ++j) f[j] = f[j] * s;
+        } else if (kv.dtype == PA_KV_FP8) {
+          uint2 u = *reinterpret_cast<const uint2 *>(reinterpret_cast<const uint8_t *>(data) +
+                                                     row * D + d0);
+          const float g = which ? kv.vg : kv.kg;
+          uint32_t w2[2] = {u.x, u.y};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float2 x = h2u_to_f2(e4m3x2_u16_to_h2(w2[j >> 1] >> (16 * (j & 1))));
+            f[2 * j] = x.x * g;
+            f[2 * j + 1] = x.y * g;
+          }
         } else {
           uint32_t u = *reinterpret_cast<const uint32_t *>(reinterpret_cast<const uint8_t *>(data) +
                                                            row * (D / 2) + d0 / 2);

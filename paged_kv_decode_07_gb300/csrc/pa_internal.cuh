@@ -221,6 +221,20 @@ __device__ __forceinline__ uint32_t e4m3_to_h2_dup(uint32_t byte) {
   return r;
 }
 
+// two E4M3 codes (low 16 bits, element 0 in the low byte) -> f16x2, exact
+__device__ __forceinline__ uint32_t e4m3x2_u16_to_h2(uint32_t v) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)v));
+  return r;
+}
+
+__device__ __forceinline__ constexpr bool has_scale_tensors(int dt) {
+  return dt == PA_KV_INT8 || dt == PA_KV_NVFP4;
+}
+__device__ __forceinline__ constexpr bool has_global_scale(int dt) {
+  return dt == PA_KV_NVFP4 || dt == PA_KV_FP8;
+}
+
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
   return *reinterpret_cast<uint32_t *>(&r);

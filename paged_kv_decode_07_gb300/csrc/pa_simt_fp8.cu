@@ -1,0 +1,10 @@
+// pa_simt_fp8.cu -- instantiations of the CUDA-core decode kernel for the
+// FP8-E4M3 KV format (one translation unit per format so they compile in
+// parallel).
+#include "pa_decode_simt.cuh"
+
+namespace pa {
+cudaError_t launch_decode_simt_fp8(const AttnParams &p, int grid, cudaStream_t s) {
+  return simt::launch_dtype<PA_KV_FP8>(p, grid, s);
+}
+}  // namespace pa

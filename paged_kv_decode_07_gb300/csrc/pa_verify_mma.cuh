@@ -45,10 +45,10 @@ constexpr int DS = D / kWarps;   // head-dim slice per warp
 
 template <int DT, int NT>
 struct Geo {
-  static_assert(DT == PA_KV_INT8 || DT == PA_KV_NVFP4, "quantised formats");
+  static_assert(DT == PA_KV_INT8 || DT == PA_KV_NVFP4 || DT == PA_KV_FP8, "quantised formats");
   static_assert(NT % 2 == 0 && NT <= 6, "even n-tile count");
-  static constexpr int ROW = DT == PA_KV_INT8 ? D : D / 2;
-  static constexpr int SROW = DT == PA_KV_INT8 ? 2 : D / 16;
+  static constexpr int ROW = DT == PA_KV_NVFP4 ? D / 2 : D;
+  static constexpr int SROW = DT == PA_KV_INT8 ? 2 : (DT == PA_KV_NVFP4 ? D / 16 : 0);
   static constexpr int CODE = kBlock * ROW;
   static constexpr int SC = kBlock * SROW;
   static constexpr int PAYLOAD = 2 * (CODE + SC);
@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, NT == 2 ? 4 : 2)
       qf[nt][s][1] = f2_to_h2(x1.x, x1.y);
     }
   }
-  const float qscale = p.scale_log2 * (DT == PA_KV_NVFP4 ? p.kv.kg : 1.0f);
+  const float qscale = p.scale_log2 * (has_global_scale(DT) ? p.kv.kg : 1.0f);
 
   // owner side: this lane finishes entries e = c*EPO + k (k < EPO) of every
   // token pair (r, r+8) in warp `warp`'s column set: column = (e/2)*8 + 2*warp + e%2
@@ -178,8 +178,11 @@ __global__ void __launch_bounds__(kThreads, NT == 2 ? 4 : 2)
       tma_rows(st + x * kBlock, &tmK, x, y, bar, pol);
       tma_rows(st + Gm::CODE + x * kBlock, &tmV, x, y, bar, pol);
     }
-    bulk_g2s(st + 2 * Gm::CODE, (const uint8_t *)p.kv.ks + tile * Gm::SC, Gm::SC, bar, pol);
-    bulk_g2s(st + 2 * Gm::CODE + Gm::SC, (const uint8_t *)p.kv.vs + tile * Gm::SC, Gm::SC, bar, pol);
+    if constexpr (Gm::SC > 0) {
+      bulk_g2s(st + 2 * Gm::CODE, (const uint8_t *)p.kv.ks + tile * Gm::SC, Gm::SC, bar, pol);
+      bulk_g2s(st + 2 * Gm::CODE + Gm::SC, (const uint8_t *)p.kv.vs + tile * Gm::SC, Gm::SC, bar,
+               pol);
+    }
   };
   int issued = 0;
   if (tid == 0) {
@@ -232,9 +235,19 @@ __global__ void __launch_bounds__(kThreads, NT == 2 ? 4 : 2)
         uint32_t w0[4] = {k0.x, k0.y, k0.z, k0.w}, w1[4] = {k1.x, k1.y, k1.z, k1.w};
 #pragma unroll
         for (int s2 = 0; s2 < 4; ++s2) {
-          const uint32_t x0 = w0[s2] ^ 0x80808080u, x1 = w1[s2] ^ 0x80808080u;
-          const uint32_t a0 = s8pair_to_h2(x0, 0), a1 = s8pair_to_h2(x1, 0);
-          const uint32_t a2 = s8pair_to_h2(x0, 1), a3 = s8pair_to_h2(x1, 1);
+          uint32_t a0, a1, a2, a3;
+          if constexpr (DT == PA_KV_INT8) {
+            const uint32_t x0 = w0[s2] ^ 0x80808080u, x1 = w1[s2] ^ 0x80808080u;
+            a0 = s8pair_to_h2(x0, 0);
+            a1 = s8pair_to_h2(x1, 0);
+            a2 = s8pair_to_h2(x0, 1);
+            a3 = s8pair_to_h2(x1, 1);
+          } else {   // FP8: bytes 0,1 -> k rows 2c, 2c+1; bytes 2,3 -> 2c+8, 2c+9
+            a0 = e4m3x2_u16_to_h2(w0[s2]);
+            a1 = e4m3x2_u16_to_h2(w1[s2]);
+            a2 = e4m3x2_u16_to_h2(w0[s2] >> 16);
+            a3 = e4m3x2_u16_to_h2(w1[s2] >> 16);
+          }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
             mma16816(sp[nt], a0, a1, a2, a3, qf[nt][s2][0], qf[nt][s2][1]);
@@ -380,16 +393,30 @@ __global__ void __launch_bounds__(kThreads, NT == 2 ? 4 : 2)
         for (int t = 0; t < 4; ++t) {
           const bool ok = tk[t] < nvalid;
           uint2 u = ok ? *reinterpret_cast<const uint2 *>(sV + sw_off(tk[t], vb)) : make_uint2(0, 0);
-          vw[t][0] = u.x ^ 0x80808080u;
-          vw[t][1] = u.y ^ 0x80808080u;
+          const uint32_t flip = DT == PA_KV_INT8 ? 0x80808080u : 0u;   // int8: offset-binary
+          vw[t][0] = u.x ^ flip;
+          vw[t][1] = u.y ^ flip;
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          uint32_t h[4];
+          uint32_t a0, a1, a2, a3;
+          if constexpr (DT == PA_KV_INT8) {
+            uint32_t h[4];
 #pragma unroll
-          for (int t = 0; t < 4; ++t) h[t] = s8pair_to_h2(vw[t][e >> 1], e & 1);
-          const uint32_t a0 = prmt(h[0], h[1], 0x5410), a1 = prmt(h[0], h[1], 0x7632);
-          const uint32_t a2 = prmt(h[2], h[3], 0x5410), a3 = prmt(h[2], h[3], 0x7632);
+            for (int t = 0; t < 4; ++t) h[t] = s8pair_to_h2(vw[t][e >> 1], e & 1);
+            a0 = prmt(h[0], h[1], 0x5410);
+            a1 = prmt(h[0], h[1], 0x7632);
+            a2 = prmt(h[2], h[3], 0x5410);
+            a3 = prmt(h[2], h[3], 0x7632);
+          } else {   // FP8: interleave the bytes of each token pair, one cvt per register
+            const uint32_t sel = (e & 1) ? 0x7362u : 0x5140u;
+            const uint32_t xa = prmt(vw[0][e >> 1], vw[1][e >> 1], sel);
+            const uint32_t xb = prmt(vw[2][e >> 1], vw[3][e >> 1], sel);
+            a0 = e4m3x2_u16_to_h2(xa);
+            a1 = e4m3x2_u16_to_h2(xa >> 16);
+            a2 = e4m3x2_u16_to_h2(xb);
+            a3 = e4m3x2_u16_to_h2(xb >> 16);
+          }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma16816(o[e][nt], a0, a1, a2, a3, B[nt][0], B[nt][1]);
         }
@@ -415,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, NT == 2 ? 4 : 2)
     }
   }
   __syncthreads();
-  const float vg = DT == PA_KV_NVFP4 ? p.kv.vg : 1.0f;
+  const float vg = has_global_scale(DT) ? p.kv.vg : 1.0f;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll

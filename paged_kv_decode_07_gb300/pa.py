@@ -24,8 +24,8 @@ PA_ERR_UNSUPPORTED = -2
 PA_ERR_WORKSPACE_TOO_SMALL = -3
 PA_ERR_CUDA = -4
 
-PA_KV_BF16, PA_KV_INT8, PA_KV_NVFP4 = 0, 1, 2
-DTYPE_CODES = {"bf16": PA_KV_BF16, "int8": PA_KV_INT8, "nvfp4": PA_KV_NVFP4}
+PA_KV_BF16, PA_KV_INT8, PA_KV_NVFP4, PA_KV_FP8 = 0, 1, 2, 3
+DTYPE_CODES = {"bf16": PA_KV_BF16, "int8": PA_KV_INT8, "nvfp4": PA_KV_NVFP4, "fp8": PA_KV_FP8}
 
 PA_ERRF_BAD_BLOCK_ID = 0x1
 PA_ERRF_LEN_OVER_CAPACITY = 0x2

@@ -46,6 +46,12 @@ WORKLOADS = {
     "nvfp4_verify_q8_b4_ctx64k_d256": dict(
         id=4, dtype="nvfp4", B=4, Q=8, Hq=24, Hkv=4, D=256,
         lens=("fixed", 65536 + 8), pool=("shuffled",)),
+    "fp8_b32_l1k_32k_d256": dict(
+        id=6, dtype="fp8", B=32, Q=1, Hq=24, Hkv=4, D=256,
+        lens=("uniform", 1024, 32768), pool=("shuffled",)),
+    "fp8_verify_q8_b4_ctx64k_d256": dict(
+        id=7, dtype="fp8", B=4, Q=8, Hq=24, Hkv=4, D=256,
+        lens=("fixed", 65536 + 8), pool=("shuffled",)),
     "bf16_skewed_b256_l16_128k_d256": dict(
         id=5, dtype="bf16", B=256, Q=1, Hq=24, Hkv=4, D=256,
         lens=("loguniform", 16, 131072), pool=("interleaved",)),
@@ -137,6 +143,16 @@ def quantize_int8_rows(x: torch.Tensor):
     return code.to(torch.int8), s16
 
 
+def quantize_fp8(x: torch.Tensor, g: float) -> torch.Tensor:
+    """x fp32, g fp32 per-tensor scale -> E4M3 codes (uint8) of x / g,
+    round-to-nearest-even, saturating at 448, sign in bit 7."""
+    g32 = torch.tensor(g, dtype=torch.float32, device=x.device)
+    y = x / g32 if g > 0 else torch.zeros_like(x)
+    code = e4m3_encode_rne_satfinite(y.abs())
+    neg = (y < 0) & (code != 0)
+    return (code | (neg.to(torch.uint8) << 7)).to(torch.uint8)
+
+
 def quantize_nvfp4_rows(x: torch.Tensor, g: float):
     """x [..., D] fp32, g fp32 global scale -> (packed codes uint8 [..., D/2],
     block scales uint8 (E4M3) [..., D/16]).  Element 2i is the low nibble."""
@@ -163,7 +179,7 @@ def quantize_nvfp4_rows(x: torch.Tensor, g: float):
 @dataclass
 class Workload:
     name: str
-    dtype: str                     # "bf16" | "int8" | "nvfp4"
+    dtype: str                     # "bf16" | "int8" | "nvfp4" | "fp8"
     B: int
     Q: int
     Hq: int
@@ -173,7 +189,7 @@ class Workload:
     seq_lens: torch.Tensor         # int32 [B]
     block_tables: torch.Tensor     # int32 [B, stride]
     q: torch.Tensor                # bf16 [B, Q, Hq, D]
-    k_cache: torch.Tensor          # bf16/int8 [NB,Hkv,16,D] or uint8 [NB,Hkv,16,D/2]
+    k_cache: torch.Tensor          # bf16/int8/fp8 [NB,Hkv,16,D] or uint8 [NB,Hkv,16,D/2]
     v_cache: torch.Tensor
     k_scale: Optional[torch.Tensor] = None   # fp16 [NB,Hkv,16] | uint8 [NB,Hkv,16,D/16]
     v_scale: Optional[torch.Tensor] = None
@@ -406,6 +422,28 @@ def make_workload(name: str, device="cpu", *, B: Optional[int] = None,
             scales.append(sc)
         k, v = caches
         wl_kwargs = dict(k_scale=scales[0], v_scale=scales[1], k_global=gs[0], v_global=gs[1])
+    elif dt == "fp8":
+        amaxes = []
+        for tag in (1, 2):
+            am = torch.zeros((), dtype=torch.float32, device=dev)
+            for ci, (b0, b1) in enumerate(chunks):
+                x = gen_x(tag, ci, b0, b1)
+                m = valid_mask(b0, b1).view(-1, 1, BLOCK_SIZE, 1)
+                am = torch.maximum(am, torch.where(m, x.abs(), torch.zeros_like(x)).amax())
+            amaxes.append(float(am.item()))
+        gs = [float(torch.tensor(a / E4M3_MAX, dtype=torch.float32)) for a in amaxes]
+        caches = []
+        for ti, tag in enumerate((1, 2)):
+            out = torch.empty((NB,) + shape_full, dtype=torch.uint8, device=dev)
+            for ci, (b0, b1) in enumerate(chunks):
+                c = quantize_fp8(gen_x(tag, ci, b0, b1), gs[ti])
+                if poison:
+                    m = valid_mask(b0, b1).view(-1, 1, BLOCK_SIZE, 1)
+                    c = torch.where(m, c, _rand_bytes(seed, tag + 10, ci, c.shape, dev))
+                out[b0:b1] = c
+            caches.append(out)
+        k, v = caches
+        wl_kwargs = dict(k_global=gs[0], v_global=gs[1])
     else:
         raise ValueError(dt)
 

@@ -15,7 +15,8 @@ DEV = "cuda"
 
 @pytest.mark.parametrize("name,fn", [("int8_b32_l1k_32k_d256", "decode"),
                                      ("bf16_skewed_b256_l16_128k_d256", "decode"),
-                                     ("nvfp4_verify_q8_b4_ctx64k_d256", "verify")])
+                                     ("nvfp4_verify_q8_b4_ctx64k_d256", "verify"),
+                                     ("fp8_verify_q8_b4_ctx64k_d256", "verify")])
 def test_capture_and_replay_with_new_inputs(name, fn):
     lens = [2000, 517, 33, 1200]
     wl = W.make_workload(name, device=DEV, seq_lens=lens)

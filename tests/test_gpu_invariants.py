@@ -23,9 +23,11 @@ from tests.gpu_helpers import compare, oracle_rows, run
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 NAMES = {"bf16": "bf16_skewed_b256_l16_128k_d256", "int8": "int8_b32_l1k_32k_d256",
-         "nvfp4": "nvfp4_b4_l262k_d256"}
+         "nvfp4": "nvfp4_b4_l262k_d256", "fp8": "fp8_b32_l1k_32k_d256"}
+VERIFY_NAMES = {"nvfp4": "nvfp4_verify_q8_b4_ctx64k_d256", "int8": "int8_b32_l1k_32k_d256",
+                "fp8": "fp8_verify_q8_b4_ctx64k_d256"}
 # (dtype, kernel): 1 = CUDA-core kernel, 2 = tensor-core kernel
-DK = [("bf16", 1), ("int8", 1), ("int8", 2), ("nvfp4", 1), ("nvfp4", 2)]
+DK = [("bf16", 1), ("int8", 1), ("int8", 2), ("nvfp4", 1), ("nvfp4", 2), ("fp8", 1), ("fp8", 2)]
 LENS = [3000, 17, 1, 900, 0, 4099]
 
 
@@ -142,13 +144,12 @@ def test_two_shards_merged_equal_single_call():
                                atol=2e-5, rtol=0)
 
 
-@pytest.mark.parametrize("dt", ["nvfp4", "int8"])
+@pytest.mark.parametrize("dt", ["nvfp4", "int8", "fp8"])
 def test_dense_verify_invariants(dt):
     """Dense-tile verify: bitwise block-permutation invariance and
     determinism; forced single / tiny partitions agree with the oracle; a bad
     block id is skipped and flagged."""
-    name = "nvfp4_verify_q8_b4_ctx64k_d256" if dt == "nvfp4" else "int8_b32_l1k_32k_d256"
-    wl = W.make_workload(name, device=DEV, seq_lens=[1500, 8, 300], Q=8)
+    wl = W.make_workload(VERIFY_NAMES[dt], device=DEV, seq_lens=[1500, 8, 300], Q=8)
     a, la, ws = run(wl, "verify", out_fp32=True, return_lse=True, kernel=2)
     b, lb, _ = run(wl, "verify", out_fp32=True, return_lse=True, kernel=2)
     assert torch.equal(a, b) and torch.equal(la, lb)

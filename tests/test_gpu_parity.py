@@ -25,6 +25,8 @@ REDUCED = {
     "int8_b32_l1k_32k_d256": dict(seq_lens=[1024, 3001, 1500, 2047, 17, 4101, 1, 16]),
     "nvfp4_b4_l262k_d256": dict(seq_lens=[8195, 5000]),
     "nvfp4_verify_q8_b4_ctx64k_d256": dict(seq_lens=[4104, 1008, 8, 9]),
+    "fp8_b32_l1k_32k_d256": dict(seq_lens=[1024, 3001, 1500, 2047, 17, 4101, 1, 16]),
+    "fp8_verify_q8_b4_ctx64k_d256": dict(seq_lens=[4104, 1008, 8, 9]),
     "bf16_skewed_b256_l16_128k_d256": dict(seq_lens=[16, 17, 100, 1000, 5000, 20000, 31, 64,
                                                      2048, 0, 130, 7777]),
 }
@@ -37,7 +39,7 @@ def _fn(wl):
 def _kernels(dtype):
     """0 = auto; 1 = CUDA-core kernel; 2 = tensor-core kernel (verify: dense
     tile); 3 = tensor-core kernel with verify as one unit per query token."""
-    return [0, 1, 2, 3] if dtype in ("int8", "nvfp4") else [0, 1]
+    return [0, 1, 2, 3] if dtype in ("int8", "nvfp4", "fp8") else [0, 1]
 
 
 REDUCED_CASES = [(n, k) for n in REDUCED for k in _kernels(W.spec(n)["dtype"])]
@@ -60,6 +62,8 @@ FULL_SAMPLES = {
     "int8_b32_l1k_32k_d256": 4,
     "nvfp4_b4_l262k_d256": 2,
     "nvfp4_verify_q8_b4_ctx64k_d256": 2,
+    "fp8_b32_l1k_32k_d256": 4,
+    "fp8_verify_q8_b4_ctx64k_d256": 2,
     "bf16_skewed_b256_l16_128k_d256": 6,
 }
 
@@ -84,10 +88,15 @@ def test_full_size_sampled_parity(name):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("dt", ["bf16", "int8", "nvfp4"])
+DECODE_NAMES = {"bf16": "bf16_skewed_b256_l16_128k_d256", "int8": "int8_b32_l1k_32k_d256",
+                "nvfp4": "nvfp4_b4_l262k_d256", "fp8": "fp8_b32_l1k_32k_d256"}
+VERIFY_NAMES = {"nvfp4": "nvfp4_verify_q8_b4_ctx64k_d256", "int8": "int8_b32_l1k_32k_d256",
+                "fp8": "fp8_verify_q8_b4_ctx64k_d256"}
+
+
+@pytest.mark.parametrize("dt", ["bf16", "int8", "nvfp4", "fp8"])
 def test_dequant_gather_bit_exact(dt):
-    name = {"bf16": "bf16_skewed_b256_l16_128k_d256", "int8": "int8_b32_l1k_32k_d256",
-            "nvfp4": "nvfp4_b4_l262k_d256"}[dt]
+    name = DECODE_NAMES[dt]
     lens = [33, 1, 200, 16, 0, 47]
     wl = W.make_workload(name, device=DEV, seq_lens=lens)
     kv = pa.KvCache.from_workload(wl)
@@ -105,14 +114,13 @@ def test_dequant_gather_bit_exact(dt):
 
 
 @pytest.mark.parametrize("dt,kernel", [("bf16", 1), ("int8", 1), ("int8", 2), ("nvfp4", 1),
-                                       ("nvfp4", 2)])
+                                       ("nvfp4", 2), ("fp8", 1), ("fp8", 2)])
 @pytest.mark.parametrize("shape", [(8, 8, 128), (16, 8, 128), (12, 2, 256), (4, 4, 256),
                                    (32, 4, 256), (2, 1, 128)])
 def test_gqa_and_head_dim_variants(dt, kernel, shape):
     Hq, Hkv, D = shape
-    name = {"bf16": "bf16_skewed_b256_l16_128k_d256", "int8": "int8_b32_l1k_32k_d256",
-            "nvfp4": "nvfp4_b4_l262k_d256"}[dt]
-    wl = W.make_workload(name, device=DEV, seq_lens=[700, 33, 1], Hq=Hq, Hkv=Hkv, D=D)
+    wl = W.make_workload(DECODE_NAMES[dt], device=DEV, seq_lens=[700, 33, 1], Hq=Hq, Hkv=Hkv,
+                         D=D)
     o32, lse, _ = run(wl, out_fp32=True, return_lse=True, kernel=kernel)
     ref_o, ref_l = oracle_rows(wl)
     compare(o32, ref_o, f"{dt} {shape}")
@@ -121,10 +129,9 @@ def test_gqa_and_head_dim_variants(dt, kernel, shape):
 
 @pytest.mark.parametrize("Q", [2, 5, 8, 16])
 @pytest.mark.parametrize("kernel", [1, 2, 3])
-@pytest.mark.parametrize("dt", ["nvfp4", "int8"])
+@pytest.mark.parametrize("dt", ["nvfp4", "int8", "fp8"])
 def test_verify_q_lens(Q, kernel, dt):
-    name = "nvfp4_verify_q8_b4_ctx64k_d256" if dt == "nvfp4" else "int8_b32_l1k_32k_d256"
-    wl = W.make_workload(name, device=DEV, seq_lens=[900, Q, 33, 3000], Q=Q)
+    wl = W.make_workload(VERIFY_NAMES[dt], device=DEV, seq_lens=[900, Q, 33, 3000], Q=Q)
     o32, lse, _ = run(wl, "verify", out_fp32=True, return_lse=True, kernel=kernel)
     ref_o, ref_l = oracle_rows(wl)
     compare(o32, ref_o, f"verify Q={Q}")

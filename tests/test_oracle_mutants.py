@@ -40,6 +40,7 @@ MUTANTS = {
     "merge_weight_dropped": ("+= w * part_o[((int64_t)p * R + r) * D + d];",
                              "+= part_o[((int64_t)p * R + r) * D + d];"),
     "fp16_subnormal_exponent": ("v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
+    "fp8_global_scale_dropped": ("return e * g;", "return e;"),
 }
 
 
@@ -47,7 +48,7 @@ def _checks():
     yield pins.test_fp16_decoder_exhaustive, ()
     yield pins.test_e4m3_decoder_exhaustive, ()
     yield pins.test_e2m1_decoder_table, ()
-    for dt in ("bf16", "int8", "nvfp4"):
+    for dt in ("bf16", "int8", "nvfp4", "fp8"):
         yield pins.test_gather_bit_exact_vs_numpy_decode, (dt,)
         for Q in (1, 3):
             yield pins.test_attention_matches_dense_brute_force, (dt, Q)

@@ -116,6 +116,18 @@ def test_int8_quantiser_bounds():
     assert bool((err <= s * 0.5 + 1e-6 + (x.abs() - 127 * s).clamp(min=0)).all())
 
 
+def test_fp8_quantiser_on_grid_roundtrip_and_sign():
+    g = 0.25
+    codes = torch.arange(0, 256, dtype=torch.int64)
+    codes = codes[(codes & 0x7F) != 0x7F]            # no NaN
+    vals = torch.from_numpy(codes.to(torch.uint8).numpy()).view(torch.float8_e4m3fn).float() * g
+    enc = W.quantize_fp8(vals, g)
+    dec = torch.from_numpy(enc.numpy()).view(torch.float8_e4m3fn).float() * g
+    assert torch.equal(dec, vals)                   # +-0 compare equal
+    big = W.quantize_fp8(torch.tensor([1e9, -1e9]), g)
+    assert big.tolist() == [0x7E, 0xFE]
+
+
 def test_nvfp4_quantiser_on_grid_roundtrip():
     # values exactly e2m1 * e4m3(s) * g with the block amax = 6 s g round-trip
     g = 0.5
@@ -147,6 +159,11 @@ def np_decode(wl, which):
     if wl.dtype == "int8":
         with np.errstate(invalid="ignore", over="ignore"):   # poisoned slots
             return data.astype(np.float32) * sc.view(np.float16).astype(np.float32)[..., None]
+    if wl.dtype == "fp8":
+        e = torch.from_numpy(data).view(torch.float8_e4m3fn).float().numpy()
+        g = np.float32(wl.k_global if which == 0 else wl.v_global)
+        with np.errstate(invalid="ignore"):
+            return e * g
     lo = (data & 0xF).astype(np.int64)
     hi = (data >> 4).astype(np.int64)
     codes = np.stack([lo, hi], axis=-1).reshape(*data.shape[:-1], data.shape[-1] * 2)
@@ -194,10 +211,12 @@ SMALL = {
     "bf16": ("bf16_b1_l1000_d128", [37, 1, 64, 16]),
     "int8": ("int8_b32_l1k_32k_d256", [33, 17, 1, 50]),
     "nvfp4": ("nvfp4_b4_l262k_d256", [40, 16, 1, 29]),
+    "fp8": ("fp8_b32_l1k_32k_d256", [21, 1, 48, 17]),
 }
+ALL = ["bf16", "int8", "nvfp4", "fp8"]
 
 
-@pytest.mark.parametrize("dt", ["bf16", "int8", "nvfp4"])
+@pytest.mark.parametrize("dt", ALL)
 def test_gather_bit_exact_vs_numpy_decode(dt):
     name, lens = SMALL[dt]
     wl = W.make_workload(name, seq_lens=lens)
@@ -212,7 +231,7 @@ def test_gather_bit_exact_vs_numpy_decode(dt):
         assert not k[b, :, L:, :].any() and not v[b, :, L:, :].any()
 
 
-@pytest.mark.parametrize("dt", ["bf16", "int8", "nvfp4"])
+@pytest.mark.parametrize("dt", ALL)
 @pytest.mark.parametrize("Q", [1, 3])
 def test_attention_matches_dense_brute_force(dt, Q):
     name, lens = SMALL[dt]
@@ -224,7 +243,7 @@ def test_attention_matches_dense_brute_force(dt, Q):
     np.testing.assert_allclose(lse, ref_l, rtol=0, atol=1e-12)
 
 
-@pytest.mark.parametrize("dt", ["bf16", "int8", "nvfp4"])
+@pytest.mark.parametrize("dt", ALL)
 def test_seq_len_one_returns_that_value(dt):
     name, _ = SMALL[dt]
     wl = W.make_workload(name, seq_lens=[1, 1])
@@ -239,7 +258,7 @@ def test_seq_len_one_returns_that_value(dt):
     assert np.isfinite(lse).all()
 
 
-@pytest.mark.parametrize("dt", ["bf16", "int8", "nvfp4"])
+@pytest.mark.parametrize("dt", ALL)
 def test_zero_query_gives_mean_of_v(dt):
     name, lens = SMALL[dt]
     wl = W.make_workload(name, seq_lens=lens)
@@ -264,7 +283,7 @@ def test_constant_v_gives_that_constant():
             np.testing.assert_allclose(out[b, 0, h], V[blk, h // G, 0], atol=1e-12)
 
 
-@pytest.mark.parametrize("dt", ["bf16", "int8", "nvfp4"])
+@pytest.mark.parametrize("dt", ALL)
 def test_physical_block_permutation_is_bitwise_invariant(dt):
     name, lens = SMALL[dt]
     wl = W.make_workload(name, seq_lens=lens)
@@ -275,7 +294,7 @@ def test_physical_block_permutation_is_bitwise_invariant(dt):
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
-@pytest.mark.parametrize("dt", ["bf16", "int8", "nvfp4"])
+@pytest.mark.parametrize("dt", ALL)
 def test_split_and_merge_equals_unsplit(dt):
     name, _ = SMALL[dt]
     lens = [200, 97, 16]
