@@ -67,6 +67,8 @@ def _load(path):
                                 ctypes.c_double, P, P, P, i32, i32]
     L.oracle_merge.restype = None
     L.oracle_merge.argtypes = [P, P, i32, i32, i32, P, P]
+    L.oracle_append.restype = ctypes.c_int
+    L.oracle_append.argtypes = [P, P, P, i32, P]
     return L
 
 
@@ -180,6 +182,22 @@ def merge(part_o, part_lse):
     lse = np.zeros(R)
     lib().oracle_merge(_ptr(po), _ptr(pl), S, R, D, _ptr(out), _ptr(lse))
     return out, lse
+
+
+def append(cache: HostCache, k_bits, v_bits, slot_mapping) -> int:
+    """Quantise-on-write of new tokens into the cache arrays, in place.
+    k_bits / v_bits: uint16 bf16 bits [T, Hkv, D]; slot_mapping int64 [T]
+    (-1 = padded row, nothing written).  Returns the number of rows skipped
+    for a slot outside [-1, num_blocks * 16)."""
+    k = np.ascontiguousarray(k_bits, dtype=np.uint16)
+    v = np.ascontiguousarray(v_bits, dtype=np.uint16)
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    T = sm.shape[0]
+    assert k.shape == v.shape and k.shape[0] == T
+    assert k.shape[1:] == (cache.num_kv_heads, cache.head_dim)
+    for a in cache.arrays:
+        assert a is None or a.flags.writeable
+    return lib().oracle_append(ctypes.byref(cache.struct), _ptr(k), _ptr(v), T, _ptr(sm))
 
 
 def attend_workload(wl, *, items=None, nthreads=None, key_begin=None, key_end=None):

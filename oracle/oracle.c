@@ -49,6 +49,14 @@
  *           Homelabs", "Acknowledgments").
  *   The fp32 dequantised value is widened to double for the attention.
  *
+ *   KV append (quantise-on-write): new K / V rows of a step go to the
+ *   slots that a slot mapping names, slot = block * block_size + offset;
+ *   a padded row carries slot -1 and writes nothing ("vLLM-SM70", "Known
+ *   limitations": padded drafter rows once wrote K/V into other requests'
+ *   slots).  The encoders invert the decoders above, rounding to the
+ *   nearest point of each format's grid with ties to the even code
+ *   (oracle_append below).
+ *
  * Build: gcc -O2 -std=c11 -fPIC -shared -ffp-contract=off -pthread
  *        (no fast-math: the fp32 dequant must round exactly once).
  */
@@ -353,4 +361,139 @@ void oracle_merge(const double *part_o, const double *part_lse, int32_t S, int32
     for (int d = 0; d < D; ++d) out[(int64_t)r * D + d] /= wsum;
     lse[r] = M + log(wsum);
   }
+}
+
+/* ------------------------------------------------------------ KV append */
+
+/* Nearest of the grid values val(0) < val(1) < ... < val(n-1) to a >= 0,
+ * ties to the even code; a beyond the last value gives the last code
+ * (saturation).  Binary search for the last code not above a, then the
+ * nearer of it and its successor. */
+static int round_to_grid(double a, double (*val)(int), int n) {
+  if (a >= val(n - 1)) return n - 1;
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) / 2;
+    if (val(mid) <= a) lo = mid; else hi = mid - 1;
+  }
+  double below = a - val(lo), above = val(lo + 1) - a;
+  if (below < above) return lo;
+  if (above < below) return lo + 1;
+  return (lo & 1) ? lo + 1 : lo;
+}
+
+/* non-negative grids: E4M3 codes 0..126 (127 is NaN), E2M1 codes 0..7, and
+ * binary16 codes 0..0x7C00 with the infinity code standing at 2^16, where
+ * IEEE round-to-nearest-even sends everything from 65520 up */
+static double e4m3_grid(int c) { return oracle_e4m3_value((uint8_t)c); }
+static double e2m1_grid(int c) { return oracle_e2m1_value((uint8_t)c); }
+static double fp16_grid(int c) { return c == 0x7C00 ? 65536.0 : oracle_fp16_value((uint16_t)c); }
+
+/* round half to even of a double holding an fp32 quotient */
+static double round_half_even(double q) {
+  double f = floor(q), frac = q - f;
+  if (frac > 0.5) return f + 1.0;
+  if (frac < 0.5) return f;
+  return fmod(f, 2.0) == 0.0 ? f : f + 1.0;
+}
+
+/* Encode one (token, kv head) row of D bf16 values into cache row `row` of
+ * tensor `which` (0 K, 1 V).  Formats (readings of the pages' formats):
+ *   bf16  : the bits are copied.
+ *   int8  : s = fp16_RNE(amax / 127) with amax / 127 in fp32; code =
+ *           clamp(RNE(x / s), -127, 127) with x / s in fp32; s = 0 gives 0.
+ *   FP8   : y = x / g in fp32; code = nearest E4M3 to |y| (saturating at
+ *           448), sign bit when y < 0 and the magnitude code is not 0;
+ *           g <= 0 gives 0.
+ *   NVFP4 : per 16 elements t = amax16 / (g * 6) in fp32 (g * 6 rounded
+ *           first); scale = nearest E4M3 to t; sg = e4m3(scale) * g in
+ *           fp32; y = x / sg in fp32 (0 when sg = 0); code = nearest E2M1
+ *           to |y| (saturating at 6) with the sign of y in bit 3; element
+ *           2i in the low nibble. */
+static void encode_row(const oracle_cache *c, int which, int64_t row, const uint16_t *src) {
+  const int D = c->head_dim;
+  void *data = (void *)(which ? c->v_cache : c->k_cache);
+  void *scale = (void *)(which ? c->v_scale : c->k_scale);
+  const float g = which ? c->v_global : c->k_global;
+  float *x = (float *)malloc(sizeof(float) * D);
+  for (int d = 0; d < D; ++d) x[d] = (float)oracle_bf16_value(src[d]);
+  switch (c->dtype) {
+    case OR_BF16:
+      for (int d = 0; d < D; ++d) ((uint16_t *)data)[row * D + d] = src[d];
+      break;
+    case OR_INT8: {
+      float amax = 0.0f;
+      for (int d = 0; d < D; ++d) if (fabsf(x[d]) > amax) amax = fabsf(x[d]);
+      float ratio = amax / 127.0f;
+      uint16_t s16 = (uint16_t)round_to_grid((double)ratio, fp16_grid, 0x7C01);
+      ((uint16_t *)scale)[row] = s16;
+      float s = (float)oracle_fp16_value(s16);
+      for (int d = 0; d < D; ++d) {
+        double code = 0.0;
+        if (s > 0.0f) {
+          float q = x[d] / s;
+          code = round_half_even((double)q);
+          if (code > 127.0) code = 127.0;
+          if (code < -127.0) code = -127.0;
+        }
+        ((int8_t *)data)[row * D + d] = (int8_t)code;
+      }
+      break;
+    }
+    case OR_FP8:
+      for (int d = 0; d < D; ++d) {
+        float y = g > 0.0f ? x[d] / g : 0.0f;
+        int mag = round_to_grid(fabs((double)y), e4m3_grid, 127);
+        ((uint8_t *)data)[row * D + d] = (uint8_t)(mag | ((y < 0.0f && mag != 0) ? 0x80 : 0));
+      }
+      break;
+    case OR_NVFP4:
+      for (int j = 0; j < D / 16; ++j) {
+        float amax = 0.0f;
+        for (int e = 0; e < 16; ++e) if (fabsf(x[16 * j + e]) > amax) amax = fabsf(x[16 * j + e]);
+        float denom = g * 6.0f;
+        float t = g > 0.0f ? amax / denom : 0.0f;
+        int sc = round_to_grid((double)t, e4m3_grid, 127);
+        ((uint8_t *)scale)[row * (D / 16) + j] = (uint8_t)sc;
+        float sval = (float)oracle_e4m3_value((uint8_t)sc);
+        float sg = sval * g;
+        for (int e = 0; e < 16; e += 2) {
+          uint8_t nib[2];
+          for (int k = 0; k < 2; ++k) {
+            float y = sg > 0.0f ? x[16 * j + e + k] / sg : 0.0f;
+            int mag = round_to_grid(fabs((double)y), e2m1_grid, 8);
+            nib[k] = (uint8_t)(mag | (signbit(y) ? 8 : 0));
+          }
+          ((uint8_t *)data)[row * (D / 2) + (16 * j + e) / 2] = (uint8_t)(nib[0] | (nib[1] << 4));
+        }
+      }
+      break;
+  }
+  free(x);
+}
+
+/* Append T new tokens: k_new / v_new bf16 bits [T, Hkv, D]; slot_mapping[t]
+ * = physical block * block_size + offset, or -1 for a padded row (nothing
+ * written).  A slot outside [-1, num_blocks * block_size) is skipped and
+ * counted; returns that count.  Slots are assumed distinct. */
+int oracle_append(const oracle_cache *c, const uint16_t *k_new, const uint16_t *v_new, int32_t T,
+                  const int64_t *slot_mapping) {
+  const int H = c->num_kv_heads, D = c->head_dim, bs = c->block_size;
+  const int64_t nslots = (int64_t)c->num_blocks * bs;
+  int bad = 0;
+  for (int t = 0; t < T; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot == -1) continue;
+    if (slot < -1 || slot >= nslots) {
+      ++bad;
+      continue;
+    }
+    int64_t blk = slot / bs, off = slot % bs;
+    for (int h = 0; h < H; ++h) {
+      int64_t row = (blk * H + h) * bs + off;
+      encode_row(c, 0, row, k_new + ((int64_t)t * H + h) * D);
+      encode_row(c, 1, row, v_new + ((int64_t)t * H + h) * D);
+    }
+  }
+  return bad;
 }

@@ -11,6 +11,7 @@ import subprocess
 import pytest
 
 import oracle
+import tests.test_oracle_append as apins
 import tests.test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
@@ -41,6 +42,18 @@ MUTANTS = {
                              "+= part_o[((int64_t)p * R + r) * D + d];"),
     "fp16_subnormal_exponent": ("v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
     "fp8_global_scale_dropped": ("return e * g;", "return e;"),
+    # quantise-on-write (KV append)
+    "grid_ties_away_from_zero": ("return (lo & 1) ? lo + 1 : lo;", "return lo + 1;"),
+    "int8_scale_divisor": ("float ratio = amax / 127.0f;", "float ratio = amax / 128.0f;"),
+    "nvfp4_scale_denominator": ("float denom = g * 6.0f;", "float denom = g * 4.0f;"),
+    "append_nibble_order": ("(uint8_t)(nib[0] | (nib[1] << 4))", "(uint8_t)(nib[1] | (nib[0] << 4))"),
+    "fp8_append_sign_dropped": ("(uint8_t)(mag | ((y < 0.0f && mag != 0) ? 0x80 : 0))",
+                                "(uint8_t)mag"),
+    # the pages' incident: a padded row's K/V lands in another request's slot
+    "padded_row_written": ("if (slot == -1) continue;", "if (slot == -1) slot = 0;"),
+    "append_offset_reversed": ("int64_t row = (blk * H + h) * bs + off;",
+                               "int64_t row = (blk * H + h) * bs + (bs - 1 - off);"),
+    "int8_round_half_up": ("return fmod(f, 2.0) == 0.0 ? f : f + 1.0;", "return f + 1.0;"),
 }
 
 
@@ -54,6 +67,15 @@ def _checks():
             yield pins.test_attention_matches_dense_brute_force, (dt, Q)
     yield pins.test_merge_ignores_empty_partials_and_handles_all_empty, ()
     yield pins.test_golden_closed_form_examples, ()
+    yield apins.test_fp8_encoder_matches_torch_float8_over_all_bf16_in_range, ()
+    yield apins.test_int8_scale_matches_numpy_float16_over_all_bf16_maxima, ()
+    yield apins.test_e2m1_ties_saturation_and_signed_zero, ()
+    yield apins.test_e4m3_ties_subnormals_saturation_and_sign, ()
+    yield apins.test_int8_ties_round_half_even, ()
+    for dt in ("bf16", "int8", "fp8", "nvfp4"):
+        yield apins.test_append_matches_generator_encoders, (dt,)
+        yield apins.test_padded_rows_write_nothing_bad_slots_counted, (dt,)
+    yield apins.test_on_grid_values_round_trip, ()
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
