@@ -80,7 +80,7 @@ def profiled_traffic(workload: str):
     """dram bytes per launch of the attention kernel from the committed ncu
     summary for this workload, or None if absent or taken on other source."""
     lines = None
-    for kind in ("decode", "verify"):
+    for kind in ("decode", "verify", "append"):
         try:
             lines = open(os.path.join(ROOT, "profiles", f"{kind}_{workload}.md")).read().splitlines()
             break
@@ -417,6 +417,157 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------- KV append
+
+APPEND_METRIC = "paged KV append (quantise-on-write): achieved HBM GB/s and rows/s, 1×GB300"
+
+
+def append_bytes(aw) -> int:
+    """Algorithmic bytes of one append: bf16 K and V of every valid row in,
+    their codes and scales out, and the slot mapping."""
+    rows = aw.valid_rows * aw.Hkv
+    return rows * (2 * aw.D * 2 + kv_bytes_per_token_head(aw.dtype, aw.D)) + aw.T * 8
+
+
+def oracle_append_sample(aw, tokens: int):
+    """Times the oracle's append of the first `tokens` tokens of the workload."""
+    import oracle
+    from paged_kv_decode_07_gb300 import workloads as W
+    h = W.append_host_arrays(aw)
+    cache = oracle.HostCache(aw.dtype, h["k_cache"], h["v_cache"], h["k_scale"], h["v_scale"],
+                             aw.k_global, aw.v_global)
+    n = min(tokens, aw.T)
+    sm = h["slot_mapping"][:n]
+    t0 = time.perf_counter()
+    oracle.append(cache, h["k_new"][:n], h["v_new"][:n], sm)
+    dt = time.perf_counter() - t0
+    rows = int((sm >= 0).sum()) * aw.Hkv
+    byts = rows * (2 * aw.D * 2 + kv_bytes_per_token_head(aw.dtype, aw.D)) + n * 8
+    return dt, rows, byts, n
+
+
+def run_append(args, world, rank):
+    import torch
+
+    from paged_kv_decode_07_gb300 import workloads as W
+    name = args.workload if args.workload.startswith("append_") else "append_int8_t64k_d256"
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        aw = W.make_append_workload(name, device="cpu")
+        times = []
+        for i in range(args.warmup + args.steps):
+            dt, rows, byts, n = oracle_append_sample(aw, args.ref_tokens // 8)
+            if i >= args.warmup:
+                times.append(dt)
+        sec = sum(times) / len(times)
+        value = byts / sec / 1e9
+        nthreads = 1
+        print(json.dumps({
+            "metric": APPEND_METRIC, "value": value, "unit": "GB/s", "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": name, "sample_tokens": n},
+            "rows_per_s": rows / sec,
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+                             "sample": f"first {n} of {aw.T} tokens of {name}"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}), flush=True)
+        return
+
+    from paged_kv_decode_07_gb300 import pa
+    dev = torch.device("cuda", torch.cuda.current_device())
+    spec = W.APPEND_WORKLOADS[name]
+    aw = W.make_append_workload(name, device=dev, seed=1000 + spec["id"] + 7919 * rank,
+                                T=args.append_tokens or None)
+    kv = pa.KvCache(aw.dtype, aw.k_cache, aw.v_cache, aw.k_scale, aw.v_scale, aw.k_global,
+                    aw.v_global)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    nbytes = append_bytes(aw)
+
+    def step(k=None, v=None, sm=None, w=None):
+        pa.append_kv(kv, aw.k_new if k is None else k, aw.v_new if v is None else v,
+                     aw.slot_mapping if sm is None else sm, workspace=w)
+
+    for _ in range(max(args.warmup, 3)):
+        step(w=ws)
+    torch.cuda.synchronize()
+    flags = pa.read_error(ws)
+    if flags:
+        raise RuntimeError(f"device error flags {flags:#x}")
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()                      # one kernel launch per step, no flag reset
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, world)
+
+    e2e = None
+    if not args.no_e2e:
+        hk = aw.k_new.cpu().pin_memory()
+        hv = aw.v_new.cpu().pin_memory()
+        hs = aw.slot_mapping.cpu().pin_memory()
+        dk, dv, ds = torch.empty_like(aw.k_new), torch.empty_like(aw.v_new), torch.empty_like(aw.slot_mapping)
+        hflag = torch.empty(1, dtype=torch.int32).pin_memory()
+        h2d = 2 * hk.numel() * 2 + hs.numel() * 8
+
+        def e2e_step():
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            ds.copy_(hs, non_blocking=True)
+            step(dk, dv, ds, ws)
+            hflag.copy_(ws[:4].view(torch.int32), non_blocking=True)
+            torch.cuda.current_stream().synchronize()   # the host reads the flags each step
+        for _ in range(2):
+            e2e_step()
+        barrier(world)
+        s0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        e2e_s = max_over_ranks((time.perf_counter() - s0) / args.steps, world)
+        e2e = {"value": world * nbytes / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": 4, "ms_per_step": e2e_s * 1e3,
+               "resident": "KV pool (written in place)"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, rows, byts, n = oracle_append_sample(aw, args.ref_tokens // 8)
+        cpu = {"value": byts / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {n} of {aw.T} tokens of {name}, {dt:.1f} s"}
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": APPEND_METRIC, "value": world * achieved, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16-in/" + aw.dtype + "-kv", "data": "synthetic",
+            "config": {"workload": name, "tokens": aw.T, "valid_rows": aw.valid_rows * aw.Hkv,
+                       "kv_heads": aw.Hkv, "head_dim": aw.D, "algorithmic_bytes": nbytes,
+                       "l2": "inputs larger than L2 (new K/V %.2f GB > 129 MB)"
+                             % (4 * aw.T * aw.Hkv * aw.D / 1e9),
+                       "parallelism": f"replicas x{world}, no collective"},
+            "rows_per_s": world * aw.valid_rows * aw.Hkv / (ms * 1e-3),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": profiled_traffic(name),
+                         "kernel_ms": ms, "kernel": "pa_append_kv kernel (one launch per step)",
+                         "peak_kind": peak_kind},
+            "gpu_launches": args.steps, "clocks": clk, "e2e": e2e, "cpu_baseline": cpu}),
+              flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -431,9 +582,15 @@ def main():
                     help="keys in the oracle's bounded sample")
     ap.add_argument("--cpu-tokens", type=int, default=1 << 40,
                     help="keys in the cpu_baseline sample (default: the whole workload)")
+    ap.add_argument("--op", default="decode", choices=["decode", "append"],
+                    help="decode: the attention step (default); append: the KV append")
+    ap.add_argument("--append-tokens", type=int, default=0,
+                    help="tokens per append call (default: the workload's)")
     args = ap.parse_args()
     world, rank, local = dist_setup(args)
-    if args.impl == "reference":
+    if args.op == "append":
+        run_append(args, world, rank)
+    elif args.impl == "reference":
         run_reference(args, world, rank)
     else:
         run_ours(args, world, rank, local)

@@ -91,6 +91,7 @@ typedef enum { PA_KV_BF16 = 0, PA_KV_INT8 = 1, PA_KV_NVFP4 = 2, PA_KV_FP8 = 3 } 
 #define PA_ERRF_LEN_LT_QLEN       0x8u  /* verify: 0 < seq_len < q_len: rows with no key get 0 */
 #define PA_ERRF_WAIT_TIMEOUT      0x10u /* an in-kernel wait hit its iteration cap: outputs invalid */
 #define PA_ERRF_PLAN_OVERFLOW     0x20u /* the split plan did not fit the workspace: nothing computed */
+#define PA_ERRF_BAD_SLOT          0x40u /* pa_append_kv: slot outside [-1, 16 * num_blocks): row skipped */
 
 /* The paged KV pool.  block_size must be 16; head_dim 128 or 256. */
 typedef struct pa_kv_cache {
@@ -197,6 +198,39 @@ int pa_dequant_gather(const pa_kv_cache *kv, const int32_t *block_tables,
                       int32_t block_table_stride, const int32_t *seq_lens, int32_t batch,
                       int32_t max_seq_len, float *k_out, float *v_out, void *ws,
                       pa_stream_t stream);
+
+/* KV append: quantise-on-write of the new tokens' K and V into the pool --
+ * the write side of the paged cache (PagedAttention, "vLLM Fork with focus
+ * on GB10 Homelabs", "About"): row (t, h) goes to block slot_mapping[t] / 16,
+ * offset slot_mapping[t] % 16, kv head h.  A padded row carries slot -1 and
+ * writes nothing ("vLLM-SM70", "Known limitations": padded drafter rows
+ * once wrote K/V into other requests' slots).
+ *   kv            the pool; its code and scale arrays are WRITTEN (the const
+ *                 of pa_kv_cache's pointers is cast away).  NVFP4 / FP8 use
+ *                 k_global_scale / v_global_scale as the pool's fixed
+ *                 per-tensor scales (a scale <= 0 writes zero codes).
+ *   k_new, v_new  bf16 [num_tokens, num_kv_heads, head_dim], 16-byte aligned.
+ *   slot_mapping  int64 [num_tokens], 8-byte aligned: block * 16 + offset,
+ *                 or -1.  Slots must be distinct within one call (two rows
+ *                 for one slot leave that slot's bytes unspecified).  A slot
+ *                 outside [-1, 16 * num_blocks) is skipped and sets
+ *                 PA_ERRF_BAD_SLOT.
+ *   ws            NULL, or >= 256 bytes whose header receives the flags.
+ * Encoding (every rounding decision in fp32, round to nearest even):
+ *   bf16  : copied.
+ *   int8  : s = fp16(amax / 127) over the (token, kv head) row; code =
+ *           clamp(rint(x / s), -127, 127); s = 0 gives 0.
+ *   FP8   : code = E4M3 nearest to |x / g| (saturating at 448) with the
+ *           sign of x / g, except that a zero magnitude is written +0.
+ *   NVFP4 : per 16 elements, scale = E4M3 nearest to amax16 / (g * 6);
+ *           code = E2M1 nearest to |x / (e4m3(scale) * g)| (saturating at 6)
+ *           with the sign bit of that quotient; element 2i in the low
+ *           nibble.
+ * num_tokens = 0 launches nothing but the flag reset.  Returns PA_OK,
+ * PA_ERR_INVALID_ARG (null pointer, misalignment, num_tokens < 0),
+ * PA_ERR_UNSUPPORTED (head_dim, block_size) or PA_ERR_CUDA. */
+int pa_append_kv(const pa_kv_cache *kv, const void *k_new, const void *v_new, int32_t num_tokens,
+                 const int64_t *slot_mapping, void *ws, pa_stream_t stream);
 
 /* Copies the device error flags (PA_ERRF_*) of the last call that used ws
  * to *host_flags (host).  Synchronises `stream`. */

@@ -350,6 +350,28 @@ int pa_dequant_gather(const pa_kv_cache *kv, const int32_t *block_tables, int32_
   return PA_OK;
 }
 
+int pa_append_kv(const pa_kv_cache *kv, const void *k_new, const void *v_new, int32_t num_tokens,
+                 const int64_t *slot_mapping, void *ws, pa_stream_t stream) {
+  int st = check_kv(kv);
+  if (st) return st;
+  if (num_tokens < 0) return PA_ERR_INVALID_ARG;
+  if ((long long)num_tokens * kv->num_kv_heads > (1LL << 30)) return PA_ERR_UNSUPPORTED;
+  if (ws && !aligned16(ws)) return PA_ERR_INVALID_ARG;
+  if (num_tokens > 0) {
+    if (!k_new || !v_new || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) ||
+        reinterpret_cast<uintptr_t>(slot_mapping) % 8 != 0)
+      return PA_ERR_INVALID_ARG;
+  }
+  uint32_t *hdr = static_cast<uint32_t *>(ws);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (hdr && cudaMemsetAsync(hdr, 0, 4, s) != cudaSuccess) return PA_ERR_CUDA;
+  if (num_tokens == 0) return PA_OK;
+  if (launch_append(view_of(kv), k_new, v_new, num_tokens, slot_mapping, hdr, s) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
+
 int pa_read_error(const void *ws, uint32_t *host_flags, pa_stream_t stream) {
   if (!ws || !host_flags) return PA_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

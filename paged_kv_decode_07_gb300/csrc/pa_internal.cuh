@@ -277,6 +277,8 @@ int simt_supported(int dtype, int D, int R);
 cudaError_t launch_merge_plan(const AttnParams &p, cudaStream_t s);
 cudaError_t launch_merge_dense(const float *po, const float *pl, int S, int R, int D, void *out,
                                int out_fp32, float *lse_out, cudaStream_t s);
+cudaError_t launch_append(const KvView &kv, const void *k_new, const void *v_new, int T,
+                          const int64_t *slots, uint32_t *hdr, cudaStream_t s);
 cudaError_t launch_gather(const KvView &kv, const int *tables, int stride, const int *seq_lens,
                           int B, int max_len, float *k_out, float *v_out, uint32_t *hdr,
                           cudaStream_t s);

@@ -33,9 +33,10 @@ PA_ERRF_NEG_LEN = 0x4
 PA_ERRF_LEN_LT_QLEN = 0x8
 PA_ERRF_WAIT_TIMEOUT = 0x10
 PA_ERRF_PLAN_OVERFLOW = 0x20
+PA_ERRF_BAD_SLOT = 0x40
 
 EXPORTED = ("pa_workspace_bytes", "pa_decode", "pa_verify", "pa_merge", "pa_dequant_gather",
-            "pa_read_error", "pa_status_string", "pa_version")
+            "pa_append_kv", "pa_read_error", "pa_status_string", "pa_version")
 
 
 class PaError(RuntimeError):
@@ -94,6 +95,8 @@ def lib():
         L.pa_merge.argtypes = [P, P, i32, i32, i32, P, i32, P, P]
         L.pa_dequant_gather.restype = ctypes.c_int
         L.pa_dequant_gather.argtypes = [P, P, i32, P, i32, i32, P, P, P, P]
+        L.pa_append_kv.restype = ctypes.c_int
+        L.pa_append_kv.argtypes = [P, P, P, i32, P, P, P]
         L.pa_read_error.restype = ctypes.c_int
         L.pa_read_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
         L.pa_status_string.restype = ctypes.c_char_p
@@ -232,6 +235,21 @@ def dequant_gather(kv: KvCache, block_tables, seq_lens, max_len: int, workspace=
     if st != PA_OK:
         raise PaError("pa_dequant_gather", st)
     return k, v
+
+
+def append_kv(kv: KvCache, k_new, v_new, slot_mapping, workspace=None, stream=None):
+    """Quantise-on-write of new tokens into the pool (in place).  k_new /
+    v_new bf16 [T, Hkv, D]; slot_mapping int64 [T] (-1 = padded row)."""
+    T = int(slot_mapping.shape[0])
+    if T:
+        assert k_new.dtype == torch.bfloat16 and v_new.dtype == torch.bfloat16
+        assert slot_mapping.dtype == torch.int64
+        assert tuple(k_new.shape) == (T, kv.num_kv_heads, kv.head_dim) == tuple(v_new.shape)
+        assert k_new.is_contiguous() and v_new.is_contiguous() and slot_mapping.is_contiguous()
+    st = lib().pa_append_kv(ctypes.byref(kv.struct()), _ptr(k_new), _ptr(v_new), T,
+                            _ptr(slot_mapping), _ptr(workspace), _stream(stream))
+    if st != PA_OK:
+        raise PaError("pa_append_kv", st)
 
 
 def read_error(workspace: torch.Tensor, stream=None) -> int:

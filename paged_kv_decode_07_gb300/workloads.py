@@ -493,3 +493,136 @@ def host_arrays(wl: Workload) -> dict:
         q=np_bits(wl.q), k_cache=np_bits(wl.k_cache), v_cache=np_bits(wl.v_cache),
         k_scale=np_bits(wl.k_scale), v_scale=np_bits(wl.v_scale),
         block_tables=wl.block_tables.cpu().numpy(), seq_lens=wl.seq_lens.cpu().numpy())
+
+
+# --------------------------------------------------------------------------
+# KV append (quantise-on-write) workloads
+# --------------------------------------------------------------------------
+
+# T new tokens of `seq` tokens per sequence (a prefill chunk per sequence),
+# Hkv 4 / D 256 like the decode workloads; every `pad_every`-th row is a
+# padded row (slot -1).  Seeds 1000 + id.
+APPEND_WORKLOADS = {
+    f"append_{dt}_t64k_d256": dict(id=8 + i, dtype=dt, T=65536, seq=4096, Hkv=4, D=256,
+                                   pad_every=61)
+    for i, dt in enumerate(("bf16", "int8", "fp8", "nvfp4"))
+}
+
+
+@dataclass
+class AppendWorkload:
+    name: str
+    dtype: str
+    T: int
+    Hkv: int
+    D: int
+    seed: int
+    k_new: torch.Tensor            # bf16 [T, Hkv, D]
+    v_new: torch.Tensor
+    slot_mapping: torch.Tensor     # int64 [T], -1 = padded row
+    k_cache: torch.Tensor          # the pool before the append (random bytes)
+    v_cache: torch.Tensor
+    k_scale: Optional[torch.Tensor] = None
+    v_scale: Optional[torch.Tensor] = None
+    k_global: float = 1.0
+    v_global: float = 1.0
+
+    @property
+    def num_blocks(self) -> int:
+        return int(self.k_cache.shape[0])
+
+    @property
+    def valid_rows(self) -> int:
+        return int((self.slot_mapping >= 0).sum().item())
+
+
+def make_append_workload(name: str, device="cpu", *, T: Optional[int] = None,
+                         seed: Optional[int] = None, D: Optional[int] = None,
+                         Hkv: Optional[int] = None, dtype: Optional[str] = None) -> AppendWorkload:
+    """New K / V rows N(0, 1) (rows of magnitude 1e-3 and 1e3 mixed in, one in
+    eight each), bf16; sequences of `seq` tokens whose blocks come from a
+    shuffled pool, each token at its block and offset; padded rows -1.  The
+    pool starts as random bytes so that untouched bytes can be checked.
+    NVFP4 / FP8 per-tensor scales: amax / (6 * 448) and amax / 448 of the new
+    rows, in fp32."""
+    sp = APPEND_WORKLOADS[name]
+    dt = dtype or sp["dtype"]
+    T = sp["T"] if T is None else T
+    D = D or sp["D"]
+    Hkv = Hkv or sp["Hkv"]
+    seed = 1000 + sp["id"] if seed is None else seed
+    g = _cpu_gen(seed)
+    seq = sp["seq"]
+    lens = [min(seq, T - s) for s in range(0, T, seq)]
+    nblk = [(L + BLOCK_SIZE - 1) // BLOCK_SIZE for L in lens]
+    NB = max(sum(nblk) + 8, 1)
+    perm = torch.randperm(NB, generator=g)
+    slots = []
+    pos = 0
+    for L, n in zip(lens, nblk):
+        blocks = perm[pos: pos + n]
+        pos += n
+        t = torch.arange(L)
+        slots.append(blocks[t // BLOCK_SIZE] * BLOCK_SIZE + t % BLOCK_SIZE)
+    slot_mapping = torch.cat(slots) if slots else torch.zeros(0, dtype=torch.int64)
+    if T:
+        slot_mapping[sp["pad_every"] - 1:: sp["pad_every"]] = -1
+    slot_mapping = slot_mapping.to(torch.int64)
+
+    def rows(tag):
+        x = torch.randn((T, Hkv, D), generator=_cpu_gen(seed * 31 + tag), dtype=torch.float32)
+        mag = torch.ones(T)
+        mag[3::8] = 1e-3
+        mag[5::8] = 1e3
+        return (x * mag.view(T, 1, 1)).to(torch.bfloat16)
+
+    k_new, v_new = rows(1), rows(2)
+    gl = []
+    for x in (k_new, v_new):
+        amax = float(x.float().abs().max()) if T else 0.0
+        den = E4M3_MAX * (E2M1_MAX if dt == "nvfp4" else 1.0)
+        gl.append(float(torch.tensor(amax / den, dtype=torch.float32)))
+
+    def pool(shape, dtype, tag):
+        b = torch.randint(0, 256, shape + (torch.empty(0, dtype=dtype).element_size(),),
+                          generator=_cpu_gen(seed * 131 + tag), dtype=torch.int64)
+        return b.to(torch.uint8).view(dtype).reshape(shape)
+
+    base = (NB, Hkv, BLOCK_SIZE)
+    ks = vs = None
+    if dt == "bf16":
+        kc, vc = pool(base + (D,), torch.bfloat16, 1), pool(base + (D,), torch.bfloat16, 2)
+    elif dt == "int8":
+        kc, vc = pool(base + (D,), torch.int8, 1), pool(base + (D,), torch.int8, 2)
+        ks, vs = pool(base, torch.float16, 3), pool(base, torch.float16, 4)
+    elif dt == "fp8":
+        kc, vc = pool(base + (D,), torch.uint8, 1), pool(base + (D,), torch.uint8, 2)
+    elif dt == "nvfp4":
+        kc, vc = pool(base + (D // 2,), torch.uint8, 1), pool(base + (D // 2,), torch.uint8, 2)
+        ks, vs = pool(base + (D // 16,), torch.uint8, 3), pool(base + (D // 16,), torch.uint8, 4)
+    else:
+        raise ValueError(dt)
+
+    def dev(t):
+        return None if t is None else t.to(device)
+
+    return AppendWorkload(
+        name=name, dtype=dt, T=T, Hkv=Hkv, D=D, seed=seed, k_new=dev(k_new), v_new=dev(v_new),
+        slot_mapping=dev(slot_mapping), k_cache=dev(kc), v_cache=dev(vc), k_scale=dev(ks),
+        v_scale=dev(vs), k_global=gl[0] if dt in ("fp8", "nvfp4") else 1.0,
+        v_global=gl[1] if dt in ("fp8", "nvfp4") else 1.0)
+
+
+def append_host_arrays(aw: AppendWorkload) -> dict:
+    """numpy copies (raw bits) of the pool and the new rows, as the oracle reads them."""
+    def np_bits(t):
+        if t is None:
+            return None
+        t = t.detach().cpu().contiguous().clone()
+        if t.dtype in (torch.bfloat16, torch.float16):
+            return t.view(torch.int16).numpy().view("uint16")
+        return t.numpy()
+    return dict(k_cache=np_bits(aw.k_cache), v_cache=np_bits(aw.v_cache),
+                k_scale=np_bits(aw.k_scale), v_scale=np_bits(aw.v_scale),
+                k_new=np_bits(aw.k_new), v_new=np_bits(aw.v_new),
+                slot_mapping=aw.slot_mapping.cpu().numpy())

@@ -28,7 +28,7 @@ def declared_functions():
 def test_header_declares_the_api():
     fns = declared_functions()
     for name in ("pa_decode", "pa_verify", "pa_merge", "pa_workspace_bytes",
-                 "pa_dequant_gather", "pa_read_error", "pa_status_string"):
+                 "pa_dequant_gather", "pa_append_kv", "pa_read_error", "pa_status_string"):
         assert name in fns
 
 
@@ -114,3 +114,22 @@ def test_merge_and_gather_argument_checks(L):
                                ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), None,
                                None) == pa.PA_ERR_INVALID_ARG
     assert L.pa_read_error(None, None, None) == pa.PA_ERR_INVALID_ARG
+
+
+def test_append_argument_checks(L):
+    F = ctypes.c_void_p(FAKE)
+    kv = kv_struct(dtype=1)
+    ap = L.pa_append_kv
+    assert ap(ctypes.byref(kv), F, F, -1, F, None, None) == pa.PA_ERR_INVALID_ARG
+    assert ap(ctypes.byref(kv), None, F, 4, F, None, None) == pa.PA_ERR_INVALID_ARG
+    assert ap(ctypes.byref(kv), F, F, 4, None, None, None) == pa.PA_ERR_INVALID_ARG
+    assert ap(ctypes.byref(kv), F, ctypes.c_void_p(FAKE + 8), 4, F, None,
+              None) == pa.PA_ERR_INVALID_ARG                           # v_new misaligned
+    assert ap(ctypes.byref(kv), F, F, 4, ctypes.c_void_p(FAKE + 4), None,
+              None) == pa.PA_ERR_INVALID_ARG                           # slot_mapping misaligned
+    assert ap(ctypes.byref(kv_struct(dtype=1, D=96)), F, F, 4, F, None,
+              None) == pa.PA_ERR_UNSUPPORTED
+    assert ap(ctypes.byref(kv_struct(dtype=2, scales=False)), F, F, 4, F, None,
+              None) == pa.PA_ERR_INVALID_ARG                           # NVFP4 without scales
+    assert ap(None, F, F, 4, F, None, None) == pa.PA_ERR_INVALID_ARG
+    assert ap(ctypes.byref(kv), None, None, 0, None, None, None) == pa.PA_OK   # nothing to do
