@@ -67,10 +67,11 @@ def measured_peaks():
         return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(files=None) -> str:
+    """sha256 prefix over the named files of csrc/ (default: all of them)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_07_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(files or os.listdir(csrc)):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -93,7 +94,8 @@ def profiled_traffic(workload: str):
         if ":" in ln and ln.startswith("- "):
             k, v = ln[2:].split(":", 1)
             vals[k.strip()] = v.strip().strip("`")
-    if vals.get("kernel_source_hash") != kernel_source_hash():
+    files = vals.get("kernel_sources", "").split() or None   # the files the kernel is built from
+    if vals.get("kernel_source_hash") != kernel_source_hash(files):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])

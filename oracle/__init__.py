@@ -69,6 +69,13 @@ def _load(path):
     L.oracle_merge.argtypes = [P, P, i32, i32, i32, P, P]
     L.oracle_append.restype = ctypes.c_int
     L.oracle_append.argtypes = [P, P, P, i32, P]
+    L.oracle_block_means.restype = None
+    L.oracle_block_means.argtypes = [P, P, i32, P, i32, i32, i32, P]
+    L.oracle_sparse_select.restype = None
+    L.oracle_sparse_select.argtypes = [P, i32, i32, i32, i32, P, P, i32, i32, P, P]
+    L.oracle_attend_sparse.restype = None
+    L.oracle_attend_sparse.argtypes = [P, P, i32, i32, P, i32, P, P, i32, i32, ctypes.c_double,
+                                       P, P]
     return L
 
 
@@ -198,6 +205,53 @@ def append(cache: HostCache, k_bits, v_bits, slot_mapping) -> int:
     for a in cache.arrays:
         assert a is None or a.flags.writeable
     return lib().oracle_append(ctypes.byref(cache.struct), _ptr(k), _ptr(v), T, _ptr(sm))
+
+
+def block_means(cache: HostCache, block_tables, seq_lens, sparse_block: int, max_nsb: int):
+    """Mean dequantised key of every sparse block: fp64 [B, max_nsb, Hkv, D]."""
+    t = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B = t.shape[0]
+    means = np.zeros((B, max_nsb, cache.num_kv_heads, cache.head_dim))
+    lib().oracle_block_means(ctypes.byref(cache.struct), _ptr(t), t.shape[1], _ptr(sl), B,
+                             int(sparse_block), int(max_nsb), _ptr(means))
+    return means
+
+
+def sparse_select(q_bits, num_kv_heads: int, means, nsb, top_k: int):
+    """q_bits uint16 bf16 [B, 1, Hq, D]; means fp64 [B, max_nsb, Hkv, D];
+    nsb int [B].  Returns (scores fp64 [B, Hkv, max_nsb], sel int32
+    [B, Hkv, top_k] ascending, -1 padded)."""
+    q = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    B, Q, Hq, D = q.shape
+    assert Q == 1
+    m = np.ascontiguousarray(means, dtype=np.float64)
+    n = np.ascontiguousarray(nsb, dtype=np.int32)
+    max_nsb = m.shape[1]
+    scores = np.zeros((B, num_kv_heads, max_nsb))
+    sel = np.zeros((B, num_kv_heads, top_k), np.int32)
+    lib().oracle_sparse_select(_ptr(q), B, Hq, int(num_kv_heads), D, _ptr(m), _ptr(n), max_nsb,
+                               int(top_k), _ptr(scores), _ptr(sel))
+    return scores, sel
+
+
+def attend_sparse(cache: HostCache, q_bits, block_tables, seq_lens, sel, sparse_block: int,
+                  scale: float):
+    """Exact decode attention over the selected sparse blocks of each kv
+    head.  Returns (out fp64 [B, 1, Hq, D], lse fp64 [B, 1, Hq])."""
+    q = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    B, Q, Hq, D = q.shape
+    assert Q == 1
+    t = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    s = np.ascontiguousarray(sel, dtype=np.int32)
+    k = s.shape[2]
+    out = np.zeros((B, 1, Hq, D))
+    lse = np.zeros((B, 1, Hq))
+    lib().oracle_attend_sparse(ctypes.byref(cache.struct), _ptr(q), B, Hq, _ptr(t), t.shape[1],
+                               _ptr(sl), _ptr(s), k, int(sparse_block), float(scale), _ptr(out),
+                               _ptr(lse))
+    return out, lse
 
 
 def attend_workload(wl, *, items=None, nthreads=None, key_begin=None, key_end=None):

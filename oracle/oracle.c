@@ -49,6 +49,14 @@
  *           Homelabs", "Acknowledgments").
  *   The fp32 dequantised value is widened to double for the attention.
  *
+ *   Block-sparse decode ("vLLM-SM70", "Known limitations" and the
+ *   production fixes: sparse-decode selection over per-block mean keys,
+ *   blocks of 64 tokens, at most 4096 of them): the mean key of sparse
+ *   block j is the mean of the dequantised keys of its valid tokens; block
+ *   j of kv head h scores max over the query heads of h of q . mean_j;
+ *   the top_k blocks (ties to the lower index) are attended exactly
+ *   (oracle_block_means, oracle_sparse_select, oracle_attend_sparse).
+ *
  *   KV append (quantise-on-write): new K / V rows of a step go to the
  *   slots that a slot mapping names, slot = block * block_size + offset;
  *   a padded row carries slot -1 and writes nothing ("vLLM-SM70", "Known
@@ -496,4 +504,132 @@ int oracle_append(const oracle_cache *c, const uint16_t *k_new, const uint16_t *
     }
   }
   return bad;
+}
+
+/* ------------------------------------------------- block-sparse decode */
+
+/* means [B, max_nsb, Hkv, D]: sparse block j of sequence b covers logical
+ * tokens [j * sb, min((j + 1) * sb, L)); its mean key is the mean of their
+ * dequantised keys.  Blocks past the sequence are 0. */
+void oracle_block_means(const oracle_cache *c, const int32_t *tables, int32_t stride,
+                        const int32_t *seq_lens, int32_t B, int32_t sb, int32_t max_nsb,
+                        double *means) {
+  const int H = c->num_kv_heads, D = c->head_dim;
+  float *row = (float *)malloc(sizeof(float) * D);
+  for (int b = 0; b < B; ++b)
+    for (int j = 0; j < max_nsb; ++j)
+      for (int h = 0; h < H; ++h) {
+        double *m = means + (((int64_t)b * max_nsb + j) * H + h) * D;
+        for (int d = 0; d < D; ++d) m[d] = 0.0;
+        int lo = j * sb, hi = (j + 1) * sb;
+        if (hi > seq_lens[b]) hi = seq_lens[b];
+        if (lo >= hi) continue;
+        for (int t = lo; t < hi; ++t) {
+          token_row(c, 0, tables, stride, b, t, h, row);
+          for (int d = 0; d < D; ++d) m[d] += (double)row[d];
+        }
+        for (int d = 0; d < D; ++d) m[d] /= (double)(hi - lo);
+      }
+  free(row);
+}
+
+/* scores [B, Hkv, max_nsb]: score of block j for kv head h = max over the
+ * query heads of h of q . mean_j (q bf16 [B, 1, Hq, D]); blocks j >= nsb[b]
+ * score -inf.  sel [B, Hkv, k]: the min(k, nsb[b]) blocks of largest score,
+ * ties to the lower index, in ascending block order, then -1. */
+void oracle_sparse_select(const uint16_t *q, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                          const double *means, const int32_t *nsb, int32_t max_nsb, int32_t k,
+                          double *scores, int32_t *sel) {
+  const int G = Hq / Hkv;
+  char *taken = (char *)malloc(max_nsb > 0 ? max_nsb : 1);
+  for (int b = 0; b < B; ++b)
+    for (int h = 0; h < Hkv; ++h) {
+      double *sc = scores + ((int64_t)b * Hkv + h) * max_nsb;
+      for (int j = 0; j < max_nsb; ++j) {
+        sc[j] = -INFINITY;
+        if (j >= nsb[b]) continue;
+        const double *m = means + (((int64_t)b * max_nsb + j) * Hkv + h) * D;
+        for (int g = 0; g < G; ++g) {
+          const uint16_t *qh = q + ((int64_t)b * Hq + h * G + g) * D;
+          double dot = 0.0;
+          for (int d = 0; d < D; ++d) dot += oracle_bf16_value(qh[d]) * m[d];
+          if (dot > sc[j]) sc[j] = dot;
+        }
+      }
+      /* k rounds of "largest remaining score, lowest index on ties" */
+      int n = nsb[b] < k ? nsb[b] : k;
+      memset(taken, 0, max_nsb > 0 ? max_nsb : 1);
+      for (int r = 0; r < n; ++r) {
+        int best = -1;
+        for (int j = 0; j < nsb[b]; ++j)
+          if (!taken[j] && (best < 0 || sc[j] > sc[best])) best = j;
+        taken[best] = 1;
+      }
+      int32_t *out = sel + ((int64_t)b * Hkv + h) * k;
+      int pos = 0;
+      for (int j = 0; j < nsb[b]; ++j)
+        if (taken[j]) out[pos++] = j;
+      for (; pos < k; ++pos) out[pos] = -1;
+    }
+  free(taken);
+}
+
+/* Exact decode attention (Q = 1) of every query head over the keys of the
+ * sparse blocks its kv head selected (sel as above, sparse block size sb).
+ * out [B, 1, Hq, D], lse [B, 1, Hq]; a head with no key gets 0 and -inf. */
+void oracle_attend_sparse(const oracle_cache *c, const uint16_t *q, int32_t B, int32_t Hq,
+                          const int32_t *tables, int32_t stride, const int32_t *seq_lens,
+                          const int32_t *sel, int32_t k, int32_t sb, double scale, double *out,
+                          double *lse) {
+  const int H = c->num_kv_heads, D = c->head_dim, G = Hq / H;
+  float *row = (float *)malloc(sizeof(float) * D);
+  int lmax = 1;
+  for (int b = 0; b < B; ++b) if (seq_lens[b] > lmax) lmax = seq_lens[b];
+  double *s = (double *)malloc(sizeof(double) * lmax);
+  char *keep = (char *)malloc(lmax);
+  double *acc = (double *)malloc(sizeof(double) * D);
+  for (int b = 0; b < B; ++b)
+    for (int h = 0; h < H; ++h) {
+      const int L = seq_lens[b];
+      memset(keep, 0, lmax);
+      for (int r = 0; r < k; ++r) {
+        int j = sel[((int64_t)b * H + h) * k + r];
+        if (j < 0) continue;
+        for (int t = j * sb; t < (j + 1) * sb && t < L; ++t) keep[t] = 1;
+      }
+      for (int g = 0; g < G; ++g) {
+        const int qh = h * G + g;
+        const uint16_t *qv = q + ((int64_t)b * Hq + qh) * D;
+        double m = -INFINITY;
+        for (int t = 0; t < L; ++t) {
+          if (!keep[t]) continue;
+          token_row(c, 0, tables, stride, b, t, h, row);
+          double dot = 0.0;
+          for (int d = 0; d < D; ++d) dot += oracle_bf16_value(qv[d]) * (double)row[d];
+          s[t] = scale * dot;
+          if (s[t] > m) m = s[t];
+        }
+        double sum = 0.0;
+        for (int d = 0; d < D; ++d) acc[d] = 0.0;
+        for (int t = 0; t < L; ++t) {
+          if (!keep[t]) continue;
+          double w = exp(s[t] - m);
+          sum += w;
+          token_row(c, 1, tables, stride, b, t, h, row);
+          for (int d = 0; d < D; ++d) acc[d] += w * (double)row[d];
+        }
+        double *o = out + ((int64_t)b * Hq + qh) * D;
+        if (sum == 0.0) {
+          for (int d = 0; d < D; ++d) o[d] = 0.0;
+          lse[(int64_t)b * Hq + qh] = -INFINITY;
+        } else {
+          for (int d = 0; d < D; ++d) o[d] = acc[d] / sum;
+          lse[(int64_t)b * Hq + qh] = m + log(sum);
+        }
+      }
+    }
+  free(row);
+  free(s);
+  free(keep);
+  free(acc);
 }

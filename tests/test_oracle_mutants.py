@@ -13,6 +13,7 @@ import pytest
 import oracle
 import tests.test_oracle_append as apins
 import tests.test_oracle_pins as pins
+import tests.test_oracle_sparse as spins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -54,6 +55,14 @@ MUTANTS = {
     "append_offset_reversed": ("int64_t row = (blk * H + h) * bs + off;",
                                "int64_t row = (blk * H + h) * bs + (bs - 1 - off);"),
     "int8_round_half_up": ("return fmod(f, 2.0) == 0.0 ? f : f + 1.0;", "return f + 1.0;"),
+    # block-sparse decode
+    "sparse_score_summed_over_heads": ("if (dot > sc[j]) sc[j] = dot;",
+                                       "sc[j] = (sc[j] == -INFINITY ? 0.0 : sc[j]) + dot;"),
+    "sparse_ties_to_higher_index": ("(best < 0 || sc[j] > sc[best])",
+                                    "(best < 0 || sc[j] >= sc[best])"),
+    "block_mean_over_full_block": ("m[d] /= (double)(hi - lo);", "m[d] /= (double)sb;"),
+    "sparse_token_range_shifted": ("for (int t = j * sb; t < (j + 1) * sb && t < L; ++t) keep[t] = 1;",
+                                   "for (int t = j * sb + 1; t <= (j + 1) * sb && t < L; ++t) keep[t] = 1;"),
 }
 
 
@@ -76,6 +85,13 @@ def _checks():
         yield apins.test_append_matches_generator_encoders, (dt,)
         yield apins.test_padded_rows_write_nothing_bad_slots_counted, (dt,)
     yield apins.test_on_grid_values_round_trip, ()
+    for dt in ("int8", "nvfp4"):
+        yield spins.test_block_means_match_numpy_mean_of_gathered_keys, (dt,)
+        yield spins.test_sparse_attention_matches_numpy_softmax_over_selected_tokens, (dt,)
+    yield spins.test_select_matches_numpy_brute_force, ()
+    yield spins.test_select_ties_go_to_the_lower_index, ()
+    yield spins.test_block_aligned_with_the_query_is_selected, ()
+    yield spins.test_sparse_attention_with_every_block_equals_dense, ("int8",)
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
