@@ -223,6 +223,39 @@ def oracle_sample(wl, bs, nthreads):
     return time.perf_counter() - t0, lens.tolist()
 
 
+def oracle_sparse_sample(wl, b, sb, top_k):
+    """Times the oracle's block-sparse decode of sequence b (selection and the
+    exact attention over the selected blocks; its mean keys are cache state,
+    computed beforehand)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    L = int(wl.seq_lens[b])
+    n = (L + 15) // 16
+    ids = wl.block_tables.cpu()[b, :n].long().to(wl.k_cache.device)
+
+    def take(t):
+        if t is None:
+            return None
+        a = t[ids].contiguous().cpu()
+        if a.dtype in (torch.bfloat16, torch.float16):
+            return a.view(torch.int16).numpy().view(np.uint16)
+        return a.numpy()
+
+    cache = oracle.HostCache(wl.dtype, take(wl.k_cache), take(wl.v_cache), take(wl.k_scale),
+                             take(wl.v_scale), wl.k_global, wl.v_global)
+    tab = np.arange(n, dtype=np.int32)[None]
+    lens = np.array([L], np.int32)
+    nsb = (L + sb - 1) // sb
+    means = oracle.block_means(cache, tab, lens, sb, nsb)
+    qb = wl.q[b:b + 1].contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    _, sel = oracle.sparse_select(qb, wl.Hkv, means, np.array([nsb], np.int32), top_k)
+    oracle.attend_sparse(cache, qb, tab, lens, sel, sb, wl.softmax_scale)
+    return time.perf_counter() - t0
+
+
 def pick_sample(seq_lens, budget_tokens):
     """Deterministic sample: sequences in index order until the token budget."""
     bs, tot = [], 0
@@ -303,6 +336,55 @@ def run_ours(args, world, rank, local):
              wl.seq_lens if seq_lens is None else seq_lens, wl.softmax_scale, out=out,
              max_seq_len=maxlen, workspace=ws, kernel=args.kernel, events=events)
 
+    launches_per_step = 3          # planner, attention kernel, merge
+    sparse = spec.get("top_k")
+    if sparse:
+        # block-sparse decode step: refresh the mean key of each sequence's last
+        # sparse block, score + select, then the decode over the selection
+        SB, K = spec["sparse_block"], spec["top_k"]
+        M = (maxlen + SB - 1) // SB
+        means = pa.block_means(kv, wl.block_tables, wl.seq_lens, SB, M)   # prefill-time state
+        last = torch.tensor([max((L + SB - 1) // SB - 1, 0) for L in lens], dtype=torch.int32,
+                            device=dev)
+        ws = torch.empty(pa.sparse_workspace_bytes(kv, wl.B, wl.Hq, maxlen, means, SB, K,
+                                                   kernel=args.kernel), dtype=torch.uint8,
+                         device=dev)
+        sel = torch.empty((wl.B, wl.Hkv, K), dtype=torch.int32, device=dev)
+
+        def step(events=None, q=None, tables=None, seq_lens=None):
+            t = wl.block_tables if tables is None else tables
+            sl = wl.seq_lens if seq_lens is None else seq_lens
+            pa.block_means(kv, t, sl, SB, M, first=last, count=1, means=means)
+            pa.decode_sparse(kv, wl.q if q is None else q, t, sl, wl.softmax_scale, means, SB, K,
+                             out=out, max_seq_len=maxlen, workspace=ws, kernel=args.kernel,
+                             events=events)
+        launches_per_step = 6      # means refresh, score, select, planner, attention, merge
+        fn = "pa_decode_sparse"
+        # algorithmic bytes: all mean keys scored, the refreshed blocks' keys
+        # read and means written, the selected keys / values, tables, q, out
+        step()
+        torch.cuda.synchronize()
+        _, _, selt, _ = pa.decode_sparse(kv, wl.q, wl.block_tables, wl.seq_lens,
+                                         wl.softmax_scale, means, SB, K, return_lse=True,
+                                         return_selected=True)
+        selt = selt.cpu()
+        toks = 0
+        for b, L in enumerate(lens):
+            for j in selt[b].flatten().tolist():
+                if j >= 0:
+                    toks += min((j + 1) * SB, L) - j * SB
+        per_tok = kv_bytes_per_token_head(wl.dtype, wl.D)
+        nsb_tot = sum((L + SB - 1) // SB for L in lens)
+        refresh = sum(L - ((L + SB - 1) // SB - 1) * SB for L in lens if L > 0)
+        total = (toks * per_tok                                   # selected K and V
+                 + nsb_tot * wl.Hkv * wl.D * 4                    # mean keys scored
+                 + refresh * wl.Hkv * per_tok // 2 + wl.B * wl.Hkv * wl.D * 4   # refresh
+                 + (toks // 16) * 4 + wl.B * wl.Hq * wl.D * 4)    # tables, q, out
+        # the attention kernel's own share: selected K / V, virtual tables, q, out
+        ab = dict(total=total, kv=toks * per_tok, tokens=toks // wl.Hkv,
+                  kernel=toks * per_tok + (toks // 16) * 4 + 2 * wl.B * wl.Hq * wl.D * 2,
+                  pool=sum((L + 15) // 16 for L in lens) * 16 * wl.Hkv * per_tok)
+
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
@@ -340,7 +422,7 @@ def run_ours(args, world, rank, local):
     kern_ms = [a.elapsed_time(b) for a, b in kev]
     ms_step = max_over_ranks(total_ms / args.steps, world)
     kern_avg = max_over_ranks(sum(kern_ms) / len(kern_ms), world)
-    launches = 3 * args.steps    # planner, attention kernel, merge per step
+    launches = launches_per_step * args.steps
 
     # ---- end-to-end: pinned host inputs copied in, output copied out, every step
     e2e = None
@@ -377,20 +459,27 @@ def run_ours(args, world, rank, local):
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     value = world * ab["total"] / (ms_step * 1e-3) / 1e9
-    achieved = ab["total"] / (kern_avg * 1e-3) / 1e9
+    achieved = ab.get("kernel", ab["total"]) / (kern_avg * 1e-3) / 1e9
     traffic = profiled_traffic(args.workload) if args.kernel in (0,) else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import numpy as np  # noqa: F401
         nthreads = os.cpu_count() or 1
-        bs = pick_sample(lens, args.cpu_tokens)
-        dt, slens = oracle_sample(wl, bs, nthreads)
-        cab = algorithmic_bytes(dict(spec, B_eff=len(bs)), slens)
-        cpu = {"value": cab["total"] / dt / 1e9, "unit": "GB/s", "cores": nthreads,
-               "kind": "oracle",
-               "sample": f"{len(bs)} of {wl.B} sequences ({cab['tokens']} keys) of "
-                         f"{args.workload}, fp64 two-pass softmax, {dt:.1f} s"}
+        if sparse:
+            dt = oracle_sparse_sample(wl, 0, spec["sparse_block"], spec["top_k"])
+            cpu = {"value": ab["total"] / wl.B / dt / 1e9, "unit": "GB/s", "cores": 1,
+                   "kind": "oracle",
+                   "sample": f"sequence 0 of {wl.B} of {args.workload}: selection + exact "
+                             f"attention over the selected blocks (mean keys given), {dt:.1f} s"}
+        else:
+            bs = pick_sample(lens, args.cpu_tokens)
+            dt, slens = oracle_sample(wl, bs, nthreads)
+            cab = algorithmic_bytes(dict(spec, B_eff=len(bs)), slens)
+            cpu = {"value": cab["total"] / dt / 1e9, "unit": "GB/s", "cores": nthreads,
+                   "kind": "oracle",
+                   "sample": f"{len(bs)} of {wl.B} sequences ({cab['tokens']} keys) of "
+                             f"{args.workload}, fp64 two-pass softmax, {dt:.1f} s"}
 
     if rank == 0:
         line = {
@@ -402,7 +491,8 @@ def run_ours(args, world, rank, local):
             "config": {"workload": args.workload, "batch": wl.B, "q_len": wl.Q,
                        "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": wl.D,
                        "kv_tokens": ab["tokens"], "algorithmic_bytes": ab["total"],
-                       "l2": "inputs larger than L2 (KV pool %.2f GB > 129 MB)" % (ab["kv"] / 1e9),
+                       "l2": "inputs larger than L2 (KV pool %.2f GB > 129 MB)"
+                             % (ab.get("pool", ab["kv"]) / 1e9),
                        "parallelism": f"replicas x{world}, no collective"},
             "kv_tokens_per_s": world * ab["tokens"] / (ms_step * 1e-3),
             "pct_of_peak": 100.0 * value / world / peak,

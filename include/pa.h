@@ -199,6 +199,52 @@ int pa_dequant_gather(const pa_kv_cache *kv, const int32_t *block_tables,
                       int32_t max_seq_len, float *k_out, float *v_out, void *ws,
                       pa_stream_t stream);
 
+/* Block-sparse decode by per-block mean keys ("vLLM-SM70", "Known
+ * limitations" and its production fixes: sparse-decode selection over
+ * per-block mean keys, 64-token blocks, at most 4096 of them, mean keys
+ * refreshed for every request of a decode batch).  Sparse block j of a
+ * sequence holds logical tokens [j * sparse_block, (j + 1) * sparse_block).
+ * Its mean key is the mean of the dequantised keys of its valid tokens; for
+ * kv head h it scores max over the query heads of h of q . mean_j; the
+ * top_k blocks of largest score (ties to the lower index) are attended
+ * exactly, each kv head over its own selection. */
+typedef struct pa_sparse {
+  int32_t sparse_block;       /* tokens per sparse block: a multiple of 16, 16..256 */
+  int32_t top_k;              /* sparse blocks attended per (sequence, kv head), >= 1 */
+  int32_t max_sparse_blocks;  /* second axis of means, 1..4096, and at least
+                                 ceil(max_seq_len / sparse_block) */
+  const float *means;         /* fp32 [batch, max_sparse_blocks, num_kv_heads, head_dim] */
+  int32_t *selected;          /* optional out: int32 [batch, num_kv_heads, top_k], the
+                                 selected sparse blocks in ascending order, -1 padded */
+} pa_sparse;
+
+/* Mean keys of sparse blocks first_sparse_block[b] .. first_sparse_block[b]
+ * + count - 1 of every sequence (those that hold keys) into means (layout
+ * as in pa_sparse; other entries are not written).  first_sparse_block
+ * (int32 [batch]) may be NULL (= 0); count = 0 means max_sparse_blocks.  A
+ * decode step refreshes each sequence's last sparse block (count 1),
+ * prefill all of them.  ws: NULL, or >= 256 bytes whose header receives the
+ * flags. */
+int pa_block_means(const pa_kv_cache *kv, const int32_t *block_tables,
+                   int32_t block_table_stride, const int32_t *seq_lens,
+                   const int32_t *first_sparse_block, int32_t count, int32_t batch,
+                   int32_t sparse_block, int32_t max_sparse_blocks, float *means, void *ws,
+                   pa_stream_t stream);
+
+/* Workspace of pa_decode_sparse (0 on invalid arguments). */
+size_t pa_sparse_workspace_bytes(const pa_kv_cache *kv, const pa_problem *prob,
+                                 const pa_sparse *sp, const pa_options *opt);
+
+/* Block-sparse decode (q_len 1): scores and selects the sparse blocks on the
+ * device, then runs pa_decode over the selected blocks of each kv head
+ * (the pool viewed as [num_blocks * num_kv_heads, 1, 16, head_dim], one
+ * virtual sequence per (sequence, kv head)).  Outputs as pa_decode; the
+ * workspace header (pa_read_error) also collects the selection's flags
+ * (PA_ERRF_PLAN_OVERFLOW: a sequence longer than max_sparse_blocks sparse
+ * blocks, attended over its first max_sparse_blocks only). */
+int pa_decode_sparse(const pa_kv_cache *kv, const pa_problem *prob, const pa_sparse *sp,
+                     const pa_options *opt, void *ws, size_t ws_bytes, pa_stream_t stream);
+
 /* KV append: quantise-on-write of the new tokens' K and V into the pool --
  * the write side of the paged cache (PagedAttention, "vLLM Fork with focus
  * on GB10 Homelabs", "About"): row (t, h) goes to block slot_mapping[t] / 16,

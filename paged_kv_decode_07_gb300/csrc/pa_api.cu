@@ -192,7 +192,8 @@ KvView view_of(const pa_kv_cache *kv) {
 }
 
 int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *o, void *ws,
-                  size_t ws_bytes, cudaStream_t stream, bool verify) {
+                  size_t ws_bytes, cudaStream_t stream, bool verify,
+                  const uint32_t *extra_err = nullptr) {
   int st = check_kv(kv);
   if (st) return st;
   st = check_problem(kv, p, verify ? kMaxQLen : 1);
@@ -248,6 +249,7 @@ int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *
   pp.units = reinterpret_cast<UnitInfo *>(w + L.units);
   pp.prefix_a = reinterpret_cast<int *>(w + L.prefix_a);
   pp.prefix_b = reinterpret_cast<int *>(w + L.prefix_b);
+  pp.extra_err = extra_err;
 
   AttnParams ap;
   std::memset(&ap, 0, sizeof ap);
@@ -290,9 +292,122 @@ int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *
   return PA_OK;
 }
 
+// ---- block-sparse decode: the selection writes a block table per (sequence,
+// kv head) into the pool viewed with one kv head per tile; the attention is
+// the ordinary decode over that view.
+constexpr int kMaxSparseBlocks = 4096;
+
+int check_sparse(const pa_kv_cache *kv, const pa_problem *p, const pa_sparse *sp) {
+  if (!sp) return PA_ERR_INVALID_ARG;
+  if (sp->sparse_block < kBlock || sp->sparse_block > 256 || sp->sparse_block % kBlock)
+    return PA_ERR_UNSUPPORTED;
+  if (sp->top_k < 1 || sp->max_sparse_blocks < 1) return PA_ERR_INVALID_ARG;
+  if (sp->max_sparse_blocks > kMaxSparseBlocks) return PA_ERR_UNSUPPORTED;
+  if ((long long)p->max_seq_len > (long long)sp->max_sparse_blocks * sp->sparse_block)
+    return PA_ERR_INVALID_ARG;
+  if ((long long)kv->num_blocks * kv->num_kv_heads > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+  if (p->batch > 0 && (!sp->means || !aligned16(sp->means))) return PA_ERR_INVALID_ARG;
+  if (sp->selected && !aligned4(sp->selected)) return PA_ERR_INVALID_ARG;
+  return PA_OK;
+}
+
+struct SparseLayout {
+  pa_kv_cache kv;        // the view: num_blocks * Hkv tiles of one kv head
+  pa_problem prob;       // batch * Hkv virtual sequences of G query heads
+  int k_eff, vstride;
+  size_t decode_ws, scores, vtables, vlens, err, total;
+};
+
+SparseLayout sparse_layout(const pa_kv_cache *kv, const pa_problem *p, const pa_sparse *sp,
+                           const pa_options *o) {
+  SparseLayout S;
+  const int H = kv->num_kv_heads, B = p->batch;
+  S.kv = *kv;
+  S.kv.num_blocks = kv->num_blocks * H;
+  S.kv.num_kv_heads = 1;
+  S.k_eff = std::min(sp->top_k, sp->max_sparse_blocks);
+  S.vstride = S.k_eff * (sp->sparse_block / kBlock);
+  S.prob = *p;
+  S.prob.batch = B * H;
+  S.prob.num_q_heads = p->num_q_heads / H;
+  S.prob.block_table_stride = S.vstride;
+  S.prob.max_seq_len = S.k_eff * sp->sparse_block;
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  S.decode_ws = up(pa_workspace_bytes(&S.kv, &S.prob, o));
+  S.scores = S.decode_ws;
+  S.vtables = S.scores + up((size_t)B * H * sp->max_sparse_blocks * 4);
+  S.vlens = S.vtables + up((size_t)B * H * S.vstride * 4);
+  S.err = S.vlens + up((size_t)B * H * 4);
+  S.total = S.err + 256;
+  return S;
+}
+
 }  // namespace
 
 extern "C" {
+
+int pa_block_means(const pa_kv_cache *kv, const int32_t *block_tables, int32_t stride,
+                   const int32_t *seq_lens, const int32_t *first, int32_t count, int32_t batch,
+                   int32_t sb, int32_t max_nsb, float *means, void *ws, pa_stream_t stream) {
+  int st = check_kv(kv);
+  if (st) return st;
+  if (batch < 0 || max_nsb < 1 || count < 0) return PA_ERR_INVALID_ARG;
+  if (count == 0 || count > max_nsb) count = max_nsb;
+  if (sb < kBlock || sb > 256 || sb % kBlock) return PA_ERR_UNSUPPORTED;
+  if (batch == 0) return PA_OK;
+  if (!block_tables || !seq_lens || !means || stride < 1) return PA_ERR_INVALID_ARG;
+  if (!aligned16(means) || !aligned4(block_tables) || !aligned4(seq_lens) ||
+      (first && !aligned4(first)) || (ws && !aligned16(ws)))
+    return PA_ERR_INVALID_ARG;
+  uint32_t *hdr = static_cast<uint32_t *>(ws);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (hdr && cudaMemsetAsync(hdr, 0, 4, s) != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_means(view_of(kv), block_tables, stride, seq_lens, first, count, batch, sb, max_nsb,
+                   means, hdr, s) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+size_t pa_sparse_workspace_bytes(const pa_kv_cache *kv, const pa_problem *prob,
+                                 const pa_sparse *sp, const pa_options *opt) {
+  if (check_kv(kv) != PA_OK || !prob || prob->q_len != 1 || prob->batch < 0) return 0;
+  if (prob->num_q_heads < 1 || prob->num_q_heads % kv->num_kv_heads) return 0;
+  if (check_sparse(kv, prob, sp) != PA_OK) return 0;
+  const SparseLayout S = sparse_layout(kv, prob, sp, opt);
+  return S.decode_ws ? S.total : 0;
+}
+
+int pa_decode_sparse(const pa_kv_cache *kv, const pa_problem *prob, const pa_sparse *sp,
+                     const pa_options *opt, void *ws, size_t ws_bytes, pa_stream_t stream) {
+  int st = check_kv(kv);
+  if (st) return st;
+  st = check_problem(kv, prob, 1);
+  if (st) return st;
+  st = check_sparse(kv, prob, sp);
+  if (st) return st;
+  if (prob->batch == 0) return PA_OK;
+  if (!ws || !aligned16(ws)) return PA_ERR_INVALID_ARG;
+  const SparseLayout S = sparse_layout(kv, prob, sp, opt);
+  if (!S.decode_ws) return PA_ERR_INVALID_ARG;
+  if (ws_bytes < S.total) return PA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int *vtables = reinterpret_cast<int *>(w + S.vtables);
+  int *vlens = reinterpret_cast<int *>(w + S.vlens);
+  uint32_t *err = reinterpret_cast<uint32_t *>(w + S.err);
+  if (cudaMemsetAsync(err, 0, 4, s) != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_sparse_select(view_of(kv), static_cast<const __nv_bfloat16 *>(prob->q),
+                           prob->num_q_heads, prob->block_tables, prob->block_table_stride,
+                           prob->seq_lens, prob->batch, sp->sparse_block, sp->max_sparse_blocks,
+                           sp->top_k, sp->means, reinterpret_cast<float *>(w + S.scores),
+                           sp->selected, vtables, S.vstride, vlens, err, s) != cudaSuccess)
+    return PA_ERR_CUDA;
+  pa_problem vp = S.prob;
+  vp.block_tables = vtables;
+  vp.seq_lens = vlens;
+  return run_attention(&S.kv, &vp, opt, ws, S.decode_ws, s, false, err);
+}
+
 
 size_t pa_workspace_bytes(const pa_kv_cache *kv, const pa_problem *prob, const pa_options *opt) {
   if (check_kv(kv) != PA_OK || !prob) return 0;

@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
     p.items[j] = it;
   }
   if (tid == 0) {
-    p.hdr[HDR_ERR] = s_err;
+    p.hdr[HDR_ERR] = s_err | (p.extra_err ? *p.extra_err : 0u);
     p.hdr[HDR_NUM_ITEMS] = (uint32_t)num_items;
     p.hdr[HDR_SPLIT] = (uint32_t)W;
     p.hdr[HDR_NUM_SLOTS] = (uint32_t)slots;

@@ -1,0 +1,341 @@
+// pa_sparse.cu -- block-sparse decode by per-block mean keys ("vLLM-SM70",
+// "Known limitations" and its production fixes: sparse-decode selection
+// over per-block mean keys, blocks of 64 tokens, at most 4096 of them; mean
+// keys refreshed for every request of a decode batch).
+//
+//   means_kernel   mean dequantised key of sparse blocks [first[b], nsb(b))
+//                  of every sequence: one CTA per (sequence, block, kv head)
+//   score_kernel   score[b, h, j] = max over the query heads g of kv head h
+//                  of q_g . mean_j: one lane per (sequence, kv head, block)
+//   select_kernel  one CTA per (sequence, kv head): the top_k scores (ties to
+//                  the lower index) by a bitwise search for the n-th largest
+//                  (score, index) key, then the selected blocks in ascending
+//                  order written as a block table of a per-kv-head virtual
+//                  sequence: logical block lb of the sequence becomes entry
+//                  table[b][lb] * Hkv + h, which is the id of that (block,
+//                  kv head) tile in the pool viewed as [NB * Hkv, 1, 16, D].
+// The attention itself is the ordinary decode over that view (B * Hkv
+// sequences of one kv head and G query heads each): only the work list
+// changes.  Only the sequence's last sparse block can be partial, and it
+// sorts last, so every virtual sequence is whole 16-token blocks but its
+// last.
+#include "pa_internal.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kSelThreads = 256;
+
+// dequantised key elements d0 .. d0 + 7 of pool row `row` (fp32, exactly the
+// values the attention kernels use)
+__device__ __forceinline__ void key8(const KvView &kv, size_t row, int d0, float (&f)[8]) {
+  const int D = kv.D;
+  if (kv.dtype == PA_KV_BF16) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(
+        reinterpret_cast<const __nv_bfloat16 *>(kv.k) + row * D + d0);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 x = bf16x2_to_f2(w[j]);
+      f[2 * j] = x.x;
+      f[2 * j + 1] = x.y;
+    }
+  } else if (kv.dtype == PA_KV_INT8) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(reinterpret_cast<const int8_t *>(kv.k) +
+                                                     row * D + d0);
+    s8x4_to_f4(u.x, f);
+    s8x4_to_f4(u.y, f + 4);
+    const float s = fp16_bits_to_f(reinterpret_cast<const uint16_t *>(kv.ks)[row]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) f[j] = f[j] * s;
+  } else if (kv.dtype == PA_KV_FP8) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(reinterpret_cast<const uint8_t *>(kv.k) +
+                                                     row * D + d0);
+    const uint32_t w[2] = {u.x, u.y};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 x = h2u_to_f2(e4m3x2_u16_to_h2(w[j >> 1] >> (16 * (j & 1))));
+      f[2 * j] = x.x * kv.kg;
+      f[2 * j + 1] = x.y * kv.kg;
+    }
+  } else {
+    const uint32_t u = *reinterpret_cast<const uint32_t *>(
+        reinterpret_cast<const uint8_t *>(kv.k) + row * (D / 2) + d0 / 2);
+    const uint32_t s2 =
+        e4m3_to_h2_dup(reinterpret_cast<const uint8_t *>(kv.ks)[row * (D / 16) + d0 / 16]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 x = h2u_to_f2(hmul2_u32(e2m1x2_to_h2((u >> (8 * j)) & 0xffu), s2));
+      f[2 * j] = x.x * kv.kg;
+      f[2 * j + 1] = x.y * kv.kg;
+    }
+  }
+}
+
+__device__ __forceinline__ int seq_len_of(const int *seq_lens, int b, int capacity) {
+  const int L = seq_lens[b];
+  return L < 0 ? 0 : (L > capacity ? capacity : L);
+}
+
+// one CTA per (b, j, h); warp w sums the 16-token block j * sb / 16 + w with
+// its 16 row loads in flight, then the warps' sums are added in fixed order
+__global__ void __launch_bounds__(512) means_kernel(const KvView kv, const int *tables, int stride,
+                                                    const int *seq_lens, const int *first, int count,
+                                                    int B, int sb, int max_nsb, float *means,
+                                                    uint32_t *hdr) {
+  __shared__ float part[16][256];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;   // sb / 16
+  const int H = kv.hkv, D = kv.D;
+  const int h = (int)(blockIdx.x % H);
+  const int b = (int)(blockIdx.x / ((unsigned)H * count));
+  const int j = (first ? max(first[b], 0) : 0) + (int)((blockIdx.x / H) % count);
+  const int L = seq_len_of(seq_lens, b, stride * kBlock);
+  const int lo = j * sb, hi = min(L, lo + sb);
+  if (lo >= hi || j >= max_nsb) return;   // uniform over the CTA
+  const int d0 = lane * 8;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  const int t0 = lo + warp * kBlock;
+  if (t0 < hi) {
+    const int phys = tables[(size_t)b * stride + t0 / kBlock];
+    if (phys < 0 || phys >= kv.num_blocks) {   // skipped like the attention kernels do
+      if (lane == 0) set_err(hdr, PA_ERRF_BAD_BLOCK_ID);
+    } else if (d0 < D) {
+      const int n = min(kBlock, hi - t0);
+      const size_t row0 = ((size_t)phys * H + h) * kBlock;
+#pragma unroll
+      for (int t = 0; t < kBlock; ++t) {
+        if (t < n) {
+          float f[8];
+          key8(kv, row0 + t, d0, f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] += f[i];
+        }
+      }
+    }
+  }
+  if (d0 < D) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) part[warp][d0 + i] = acc[i];
+  }
+  __syncthreads();
+  const float inv = __frcp_rn((float)(hi - lo));
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float sum = 0.f;
+    for (int w = 0; w < nw; ++w) sum += part[w][d];
+    means[(((size_t)b * max_nsb + j) * H + h) * D + d] = sum * inv;
+  }
+}
+
+// One lane per sparse block: a CTA of 128 threads scores 128 consecutive
+// blocks of one (b, h), walking each block's mean row (contiguous, L1-cached
+// across the float4 steps, eight loads in flight) against the G query rows
+// broadcast from shared memory -- no cross-lane reduction.
+constexpr int kScoreThreads = 128;
+constexpr int kScoreCta = kScoreThreads;   // blocks per CTA
+
+template <int G>
+__global__ void __launch_bounds__(kScoreThreads) score_kernel(
+    const __nv_bfloat16 *q, int Hq, const int *seq_lens, int capacity, int B, int H, int D,
+    int sb, int max_nsb, const float *means, float *scores) {
+  __shared__ float4 sq[G][256 / 4];
+  const int chunks = (max_nsb + kScoreCta - 1) / kScoreCta;
+  const int c = blockIdx.x % chunks;
+  const int h = (blockIdx.x / chunks) % H;
+  const int b = blockIdx.x / (chunks * H);
+  for (int i = threadIdx.x; i < G * D / 4; i += kScoreThreads) {
+    const int g = i / (D / 4), d4 = i % (D / 4);
+    const uint2 u = *reinterpret_cast<const uint2 *>(q + ((size_t)b * Hq + h * G + g) * D + 4 * d4);
+    const float2 lo = bf16x2_to_f2(u.x), hi = bf16x2_to_f2(u.y);
+    sq[g][d4] = make_float4(lo.x, lo.y, hi.x, hi.y);
+  }
+  __syncthreads();
+  const int L = seq_len_of(seq_lens, b, capacity);
+  const int nsb = (L + sb - 1) / sb;
+  const int j = c * kScoreCta + threadIdx.x;
+  if (j >= max_nsb) return;
+  float sc = kNegInf;
+  if (j < nsb) {
+    const float4 *m = reinterpret_cast<const float4 *>(means + (((size_t)b * max_nsb + j) * H + h) * D);
+    float acc[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) acc[g] = 0.f;
+    for (int d0 = 0; d0 < D / 4; d0 += 8) {
+      float4 x[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = m[d0 + i];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float4 y = sq[g][d0 + i];
+          acc[g] = fmaf(x[i].x, y.x, fmaf(x[i].y, y.y, fmaf(x[i].z, y.z, fmaf(x[i].w, y.w, acc[g]))));
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) sc = fmaxf(sc, acc[g]);
+  }
+  scores[((size_t)b * H + h) * max_nsb + j] = sc;
+}
+
+// (score, index) -> key ordered like (score descending, index ascending)
+__device__ __forceinline__ unsigned long long sel_key(float s, int j) {
+  uint32_t u = __float_as_uint(s);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);   // order-preserving for finite and -inf
+  return ((unsigned long long)u << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)j);
+}
+
+// One CTA of 256 threads per (b, h), each thread holding up to 16
+// (score, index) keys in registers.  The keys are unique, so the top n are
+// exactly the keys >= the n-th largest, which is found bit by bit from the
+// top: keep a bit when at least n keys are >= the prefix with it set (warp
+// ballots, per-warp counts in shared memory, one barrier per bit).  Bits
+// 31..12 are 1 in every key (index < 4096) and are not searched.  A bitmap
+// of the winners gives each one its rank in ascending block order.
+__global__ void __launch_bounds__(kSelThreads) select_kernel(
+    const int *tables, int stride, const int *seq_lens, int B, int H, int sb, int max_nsb,
+    int top_k, const float *scores, int *selected, int *vtables, int vstride, int *vlens,
+    int num_blocks, uint32_t *err) {
+  constexpr int kPer = 4096 / kSelThreads;   // keys per thread
+  constexpr int kWarpsSel = kSelThreads / 32;
+  __shared__ uint32_t s_flag[4096 / 32], s_wpre[4096 / 32];
+  __shared__ int s_cnt[2][kWarpsSel];
+  const int b = blockIdx.x / H, h = blockIdx.x % H;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int L = seq_len_of(seq_lens, b, stride * kBlock);
+  if (tid == 0) {
+    const int raw = seq_lens[b];
+    if (raw < 0) atomicOr(err, PA_ERRF_NEG_LEN);
+    if (raw > stride * kBlock) atomicOr(err, PA_ERRF_LEN_OVER_CAPACITY);
+  }
+  int nsb = (L + sb - 1) / sb;
+  if (nsb > max_nsb) {   // beyond the means' capacity: attended over its first blocks only
+    if (tid == 0) atomicOr(err, PA_ERRF_PLAN_OVERFLOW);
+    nsb = max_nsb;
+    L = nsb * sb;
+  }
+  const int n = min(top_k, nsb);
+  const float *sc = scores + ((size_t)b * H + h) * max_nsb;
+  unsigned long long key[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int j = tid + i * kSelThreads;
+    key[i] = j < nsb ? sel_key(sc[j], j) : 0ull;   // 0 is below every real key
+  }
+  for (int i = tid; i < 4096 / 32; i += kSelThreads) s_flag[i] = 0;
+  unsigned long long thr = 0;   // the n-th largest key (n < nsb), else 0 = take all
+  if (n < nsb) {
+    int buf = 0;
+    for (int bit = 63; bit >= 0; --bit) {
+      if (bit == 31) {            // index bits 31..12 are set in every key
+        thr |= 0xFFFFF000ull;
+        bit = 12;
+        continue;
+      }
+      const unsigned long long cand = thr | (1ull << bit);
+      int cnt = 0;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) cnt += __popc(__ballot_sync(0xffffffffu, key[i] >= cand));
+      if (lane == 0) s_cnt[buf][warp] = cnt;
+      __syncthreads();
+      int tot = 0;
+#pragma unroll
+      for (int w = 0; w < kWarpsSel; ++w) tot += s_cnt[buf][w];
+      if (tot >= n) thr = cand;
+      buf ^= 1;   // the next bit writes the other buffer: no second barrier
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int j = tid + i * kSelThreads;
+    if (j < nsb && key[i] >= thr) atomicOr(&s_flag[j >> 5], 1u << (j & 31));
+  }
+  __syncthreads();
+  if (warp == 0) {   // exclusive prefix of the bitmap's word counts
+    uint32_t run = 0;
+    for (int base = 0; base < 4096 / 32; base += 32) {
+      const uint32_t c = __popc(s_flag[base + lane]);
+      uint32_t incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      s_wpre[base + lane] = run + incl - c;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  __syncthreads();
+  const int bps = sb / kBlock;   // 16-token blocks per sparse block
+  const int nblk = (L + kBlock - 1) / kBlock;
+  const size_t vrow = (size_t)b * H + h;
+  for (int j = tid; j < nsb; j += kSelThreads) {
+    const uint32_t w = s_flag[j >> 5];
+    if (!((w >> (j & 31)) & 1u)) continue;
+    const int r = (int)(s_wpre[j >> 5] + __popc(w & ((1u << (j & 31)) - 1u)));
+    if (selected) selected[vrow * top_k + r] = j;
+    for (int i = 0; i < bps; ++i) {
+      const int lb = j * bps + i;
+      if (lb >= nblk) break;
+      const int phys = tables[(size_t)b * stride + lb];
+      vtables[vrow * vstride + r * bps + i] =
+          (phys >= 0 && phys < num_blocks) ? phys * H + h : -1;
+    }
+  }
+  if (selected)
+    for (int i = n + tid; i < top_k; i += kSelThreads) selected[vrow * top_k + i] = -1;
+  if (tid == 0) {
+    // keys of the selected blocks: whole sparse blocks, the sequence's last
+    // one (if chosen) only up to L
+    const int last = nsb - 1;
+    const bool last_in = nsb > 0 && ((s_flag[last >> 5] >> (last & 31)) & 1u);
+    vlens[vrow] = last_in ? (n - 1) * sb + (L - last * sb) : n * sb;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_means(const KvView &kv, const int *tables, int stride, const int *seq_lens,
+                         const int *first, int count, int B, int sb, int max_nsb, float *means,
+                         uint32_t *hdr, cudaStream_t s) {
+  const long long grid = (long long)B * count * kv.hkv;
+  if (grid == 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  means_kernel<<<(unsigned)grid, 32 * (sb / kBlock), 0, s>>>(kv, tables, stride, seq_lens, first,
+                                                             count, B, sb, max_nsb, means, hdr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sparse_select(const KvView &kv, const __nv_bfloat16 *q, int Hq,
+                                 const int *tables, int stride, const int *seq_lens, int B, int sb,
+                                 int max_nsb, int top_k, const float *means, float *scores,
+                                 int *selected, int *vtables, int vstride, int *vlens,
+                                 uint32_t *err, cudaStream_t s) {
+  const int H = kv.hkv, G = Hq / H;
+  const long long grid = (long long)B * H * ((max_nsb + kScoreCta - 1) / kScoreCta);
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const int cap = stride * kBlock;
+#define PA_SCORE_CASE(GG)                                                                    \
+  case GG:                                                                                   \
+    score_kernel<GG><<<(unsigned)grid, kScoreThreads, 0, s>>>(q, Hq, seq_lens, cap, B, H,    \
+                                                              kv.D, sb, max_nsb, means,      \
+                                                              scores);                       \
+    break;
+  switch (G) {
+    PA_SCORE_CASE(1) PA_SCORE_CASE(2) PA_SCORE_CASE(3) PA_SCORE_CASE(4)
+    PA_SCORE_CASE(5) PA_SCORE_CASE(6) PA_SCORE_CASE(7) PA_SCORE_CASE(8)
+    default: return cudaErrorInvalidValue;
+  }
+#undef PA_SCORE_CASE
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  select_kernel<<<B * H, kSelThreads, 0, s>>>(tables, stride, seq_lens, B, H, sb, max_nsb, top_k,
+                                                  scores, selected, vtables, vstride, vlens,
+                                                  kv.num_blocks, err);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -36,7 +36,8 @@ PA_ERRF_PLAN_OVERFLOW = 0x20
 PA_ERRF_BAD_SLOT = 0x40
 
 EXPORTED = ("pa_workspace_bytes", "pa_decode", "pa_verify", "pa_merge", "pa_dequant_gather",
-            "pa_append_kv", "pa_read_error", "pa_status_string", "pa_version")
+            "pa_append_kv", "pa_block_means", "pa_sparse_workspace_bytes", "pa_decode_sparse",
+            "pa_read_error", "pa_status_string", "pa_version")
 
 
 class PaError(RuntimeError):
@@ -61,6 +62,12 @@ class _Problem(ctypes.Structure):
                 ("seq_lens", ctypes.c_void_p), ("max_seq_len", ctypes.c_int32),
                 ("softmax_scale", ctypes.c_float), ("out", ctypes.c_void_p),
                 ("out_fp32", ctypes.c_int32), ("lse_out", ctypes.c_void_p)]
+
+
+class _Sparse(ctypes.Structure):
+    _fields_ = [("sparse_block", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("max_sparse_blocks", ctypes.c_int32), ("means", ctypes.c_void_p),
+                ("selected", ctypes.c_void_p)]
 
 
 class _Options(ctypes.Structure):
@@ -95,6 +102,12 @@ def lib():
         L.pa_merge.argtypes = [P, P, i32, i32, i32, P, i32, P, P]
         L.pa_dequant_gather.restype = ctypes.c_int
         L.pa_dequant_gather.argtypes = [P, P, i32, P, i32, i32, P, P, P, P]
+        L.pa_block_means.restype = ctypes.c_int
+        L.pa_block_means.argtypes = [P, P, i32, P, P, i32, i32, i32, i32, P, P, P]
+        L.pa_sparse_workspace_bytes.restype = ctypes.c_size_t
+        L.pa_sparse_workspace_bytes.argtypes = [P, P, P, P]
+        L.pa_decode_sparse.restype = ctypes.c_int
+        L.pa_decode_sparse.argtypes = [P, P, P, P, P, ctypes.c_size_t, P]
         L.pa_append_kv.restype = ctypes.c_int
         L.pa_append_kv.argtypes = [P, P, P, i32, P, P, P]
         L.pa_read_error.restype = ctypes.c_int
@@ -235,6 +248,75 @@ def dequant_gather(kv: KvCache, block_tables, seq_lens, max_len: int, workspace=
     if st != PA_OK:
         raise PaError("pa_dequant_gather", st)
     return k, v
+
+
+def block_means(kv: KvCache, block_tables, seq_lens, sparse_block: int, max_sparse_blocks: int,
+                first=None, count=0, means=None, workspace=None, stream=None):
+    """Mean keys of sparse blocks first[b] .. first[b] + count - 1 (count 0 =
+    all) of every sequence, fp32 [B, max_sparse_blocks, Hkv, D] (other
+    entries untouched; a new tensor starts at 0)."""
+    B = int(block_tables.shape[0])
+    if means is None:
+        means = torch.zeros((B, max_sparse_blocks, kv.num_kv_heads, kv.head_dim),
+                            dtype=torch.float32, device=kv.k_cache.device)
+    st = lib().pa_block_means(ctypes.byref(kv.struct()), _ptr(block_tables),
+                              int(block_tables.shape[1]), _ptr(seq_lens), _ptr(first),
+                              int(count), B, int(sparse_block), int(max_sparse_blocks), _ptr(means),
+                              _ptr(workspace), _stream(stream))
+    if st != PA_OK:
+        raise PaError("pa_block_means", st)
+    return means
+
+
+def _sparse(means, sparse_block, top_k, selected):
+    return _Sparse(int(sparse_block), int(top_k), int(means.shape[1]), _ptr(means), _ptr(selected))
+
+
+def sparse_workspace_bytes(kv: KvCache, batch: int, num_q_heads: int, max_seq_len: int, means,
+                           sparse_block: int, top_k: int, kernel=0) -> int:
+    p = _Problem(batch, num_q_heads, 1, None, None, 1, None, int(max_seq_len), 1.0, None, 0, None)
+    sp = _sparse(means, sparse_block, top_k, None)
+    o = _options(kernel)
+    return int(lib().pa_sparse_workspace_bytes(ctypes.byref(kv.struct()), ctypes.byref(p),
+                                               ctypes.byref(sp), ctypes.byref(o)))
+
+
+def decode_sparse(kv: KvCache, q, block_tables, seq_lens, softmax_scale, means, sparse_block: int,
+                  top_k: int, *, out=None, out_fp32=False, return_lse=False, return_selected=False,
+                  max_seq_len=None, workspace=None, kernel=0, split_blocks=0, target_items=0,
+                  events=None, stream=None):
+    """Block-sparse decode: q bf16 [B, 1, Hq, D]; means from block_means.
+    Returns (out, [lse,] [selected int32 [B, Hkv, top_k],] workspace)."""
+    B, Q, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Q, Hq, D), dtype=torch.float32 if out_fp32 else torch.bfloat16,
+                          device=q.device)
+    lse = torch.empty((B, Q, Hq), dtype=torch.float32, device=q.device) if return_lse else None
+    sel = (torch.empty((B, kv.num_kv_heads, top_k), dtype=torch.int32, device=q.device)
+           if return_selected else None)
+    if max_seq_len is None:
+        max_seq_len = min(int(block_tables.shape[1]) * kv.block_size,
+                          int(means.shape[1]) * int(sparse_block))
+    opts = _options(kernel, split_blocks, target_items, events)
+    kvs = kv.struct()
+    prob = _problem(kv, q, block_tables, seq_lens, softmax_scale, out, lse, max_seq_len)
+    sp = _sparse(means, sparse_block, top_k, sel)
+    need = int(lib().pa_sparse_workspace_bytes(ctypes.byref(kvs), ctypes.byref(prob),
+                                               ctypes.byref(sp), ctypes.byref(opts)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = lib().pa_decode_sparse(ctypes.byref(kvs), ctypes.byref(prob), ctypes.byref(sp),
+                                ctypes.byref(opts), _ptr(workspace), workspace.numel(),
+                                _stream(stream))
+    if st != PA_OK:
+        raise PaError("pa_decode_sparse", st)
+    res = [out]
+    if return_lse:
+        res.append(lse)
+    if return_selected:
+        res.append(sel)
+    res.append(workspace)
+    return tuple(res)
 
 
 def append_kv(kv: KvCache, k_new, v_new, slot_mapping, workspace=None, stream=None):

@@ -52,6 +52,11 @@ WORKLOADS = {
     "fp8_verify_q8_b4_ctx64k_d256": dict(
         id=7, dtype="fp8", B=4, Q=8, Hq=24, Hkv=4, D=256,
         lens=("fixed", 65536 + 8), pool=("shuffled",)),
+    # block-sparse decode: 64-token sparse blocks, 256 of them attended
+    # per (sequence, kv head) = 16,384 of 262,144 keys
+    "int8_sparse_b8_l262k_k256_d256": dict(
+        id=12, dtype="int8", B=8, Q=1, Hq=24, Hkv=4, D=256,
+        lens=("fixed", 262144), pool=("shuffled",), sparse_block=64, top_k=256),
     "bf16_skewed_b256_l16_128k_d256": dict(
         id=5, dtype="bf16", B=256, Q=1, Hq=24, Hkv=4, D=256,
         lens=("loguniform", 16, 131072), pool=("interleaved",)),

@@ -25,11 +25,9 @@ def run(wl, fn="decode", **kw):
              max_seq_len=max(wl.max_seq_len(), 1), **kw)
 
 
-def oracle_rows(wl, bs=None, nthreads=None):
-    """Oracle output for sequences `bs` (all when None) from a compact host
-    copy of just their blocks.  Returns (out [n, Q, Hq, D], lse [n, Q, Hq])."""
-    if bs is None:
-        bs = list(range(wl.B))
+def compact_host(wl, bs):
+    """Host copy of just the blocks of sequences `bs`: (oracle cache, table,
+    seq_lens, q bits) with the blocks renumbered in order."""
     lens = wl.seq_lens.cpu()[bs]
     nblk = [(int(L) + 15) // 16 for L in lens.tolist()]
     tabs = wl.block_tables.cpu()
@@ -58,8 +56,16 @@ def oracle_rows(wl, bs=None, nthreads=None):
             ks, vs = np.zeros((1,) + ks.shape[1:], ks.dtype), np.zeros((1,) + vs.shape[1:], vs.dtype)
     cache = oracle.HostCache(wl.dtype, k, v, ks, vs, wl.k_global, wl.v_global)
     qb = wl.q[bs].contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
-    return oracle.attend(cache, qb, new_tab, lens.numpy().astype(np.int32), wl.softmax_scale,
-                         nthreads=nthreads)
+    return cache, new_tab, lens.numpy().astype(np.int32), qb
+
+
+def oracle_rows(wl, bs=None, nthreads=None):
+    """Oracle output for sequences `bs` (all when None) from a compact host
+    copy of just their blocks.  Returns (out [n, Q, Hq, D], lse [n, Q, Hq])."""
+    if bs is None:
+        bs = list(range(wl.B))
+    cache, tab, lens, qb = compact_host(wl, bs)
+    return oracle.attend(cache, qb, tab, lens, wl.softmax_scale, nthreads=nthreads)
 
 
 def compare(gpu_out32, ref, what=""):

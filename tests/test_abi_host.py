@@ -133,3 +133,34 @@ def test_append_argument_checks(L):
               None) == pa.PA_ERR_INVALID_ARG                           # NVFP4 without scales
     assert ap(None, F, F, 4, F, None, None) == pa.PA_ERR_INVALID_ARG
     assert ap(ctypes.byref(kv), None, None, 0, None, None, None) == pa.PA_OK   # nothing to do
+
+
+def test_sparse_argument_checks(L):
+    F = ctypes.c_void_p(FAKE)
+    kv = kv_struct(dtype=1)
+    sp = pa._Sparse(64, 256, 4096, FAKE, None)
+    p = prob_struct(B=4, Hq=24, stride=16384, max_len=262144)
+    o = pa._Options(0, 0, 0, None, None)
+    ws = L.pa_sparse_workspace_bytes(ctypes.byref(kv), ctypes.byref(p), ctypes.byref(sp),
+                                     ctypes.byref(o))
+    assert ws > 0
+    for bad in (pa._Sparse(24, 256, 4096, FAKE, None),      # not a multiple of 16
+                pa._Sparse(64, 0, 4096, FAKE, None),        # top_k < 1
+                pa._Sparse(64, 256, 5000, FAKE, None),      # more than 4096 sparse blocks
+                pa._Sparse(64, 256, 100, FAKE, None)):      # max_seq_len beyond the means
+        assert L.pa_sparse_workspace_bytes(ctypes.byref(kv), ctypes.byref(p), ctypes.byref(bad),
+                                           ctypes.byref(o)) == 0
+    # verify-length queries are not supported by the sparse path
+    p2 = prob_struct(B=4, Hq=24, Q=2, stride=16384, max_len=262144)
+    assert L.pa_decode_sparse(ctypes.byref(kv), ctypes.byref(p2), ctypes.byref(sp), None, F,
+                              1 << 30, None) == pa.PA_ERR_UNSUPPORTED
+    assert L.pa_decode_sparse(ctypes.byref(kv), ctypes.byref(p), None, None, F, 1 << 30,
+                              None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_decode_sparse(ctypes.byref(kv), ctypes.byref(p), ctypes.byref(sp), None, F,
+                              16, None) == pa.PA_ERR_WORKSPACE_TOO_SMALL
+    bm = L.pa_block_means
+    assert bm(ctypes.byref(kv), F, 8, F, None, 0, 2, 64, 0, F, None, None) == pa.PA_ERR_INVALID_ARG
+    assert bm(ctypes.byref(kv), F, 8, F, None, -1, 2, 64, 8, F, None, None) == pa.PA_ERR_INVALID_ARG
+    assert bm(ctypes.byref(kv), F, 8, F, None, 0, 2, 40, 8, F, None, None) == pa.PA_ERR_UNSUPPORTED
+    assert bm(ctypes.byref(kv), None, 8, F, None, 0, 2, 64, 8, F, None, None) == pa.PA_ERR_INVALID_ARG
+    assert bm(ctypes.byref(kv), F, 8, F, None, 0, 0, 64, 8, F, None, None) == pa.PA_OK
