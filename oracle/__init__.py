@@ -254,6 +254,19 @@ def attend_sparse(cache: HostCache, q_bits, block_tables, seq_lens, sel, sparse_
     return out, lse
 
 
+def wo_project(out, w_bits):
+    """Output projection of decode attention ("vLLM Fork with focus on GB10
+    Homelabs", "Roadmap": fused attention + W_O GEMV):
+    y[b, n] = sum_k o[b, k] * W[k, n], o the attention output of all query
+    heads flattened (k = head * D + d), W bf16 bits [Hq * D, N].  fp64."""
+    o = np.asarray(out, dtype=np.float64)
+    B = o.shape[0]
+    o = o.reshape(B, -1)
+    w = (np.ascontiguousarray(w_bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+    assert w.shape[0] == o.shape[1]
+    return o @ w.astype(np.float64)
+
+
 def attend_workload(wl, *, items=None, nthreads=None, key_begin=None, key_end=None):
     """Convenience: run the oracle on a `workloads.Workload`."""
     from paged_kv_decode_07_gb300.workloads import host_arrays
