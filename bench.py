@@ -385,6 +385,31 @@ def run_ours(args, world, rank, local):
                   kernel=toks * per_tok + (toks // 16) * 4 + 2 * wl.B * wl.Hq * wl.D * 2,
                   pool=sum((L + 15) // 16 for L in lens) * 16 * wl.Hkv * per_tok)
 
+    result = out                   # what the host reads back in the e2e loop
+    wo_info = None
+    if args.op == "wo":
+        # attention + output projection y = o . W_O (random bf16 W_O, N(0, 1/K))
+        K, N = wl.Hq * wl.D, args.wo_hidden
+        gw = torch.Generator().manual_seed(77 + rank)
+        wmat = (torch.randn(K, N, generator=gw) / math.sqrt(K)).to(torch.bfloat16).to(dev)
+        y = torch.empty((wl.B * wl.Q, N), dtype=torch.bfloat16, device=dev)
+        _, ws = pa.decode_wo(kv, wl.q, wl.block_tables, wl.seq_lens, wl.softmax_scale, wmat, y=y,
+                             max_seq_len=maxlen, kernel=args.kernel)
+        torch.cuda.synchronize()
+
+        def step(events=None, q=None, tables=None, seq_lens=None):
+            pa.decode_wo(kv, wl.q if q is None else q,
+                         wl.block_tables if tables is None else tables,
+                         wl.seq_lens if seq_lens is None else seq_lens, wl.softmax_scale, wmat,
+                         y=y, max_seq_len=maxlen, workspace=ws, kernel=args.kernel,
+                         events=events)
+        launches_per_step = 5      # planner, attention, merge, W_O product, split reduce
+        fn = fn + "_wo"
+        result = y
+        wo_bytes = K * N * 2 + wl.B * wl.Q * N * 2
+        ab = dict(ab, total=ab["total"] + wo_bytes, kernel=ab["total"])   # the attention's own
+        wo_info = {"hidden": N, "w_bytes": K * N * 2}
+
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
@@ -431,7 +456,7 @@ def run_ours(args, world, rank, local):
         ht = wl.block_tables.cpu().pin_memory()
         hl = wl.seq_lens.cpu().pin_memory()
         dq, dt_, dl = torch.empty_like(wl.q), torch.empty_like(wl.block_tables), torch.empty_like(wl.seq_lens)
-        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hout = torch.empty(result.shape, dtype=result.dtype).pin_memory()
         h2d = hq.numel() * hq.element_size() + ht.numel() * 4 + hl.numel() * 4
         d2h = hout.numel() * hout.element_size()
         for _ in range(2):
@@ -439,7 +464,7 @@ def run_ours(args, world, rank, local):
             dt_.copy_(ht, non_blocking=True)
             dl.copy_(hl, non_blocking=True)
             step(q=dq, tables=dt_, seq_lens=dl)
-            hout.copy_(out, non_blocking=True)
+            hout.copy_(result, non_blocking=True)
         torch.cuda.synchronize()
         barrier(world)
         s0 = time.perf_counter()
@@ -448,7 +473,7 @@ def run_ours(args, world, rank, local):
             dt_.copy_(ht, non_blocking=True)
             dl.copy_(hl, non_blocking=True)
             step(q=dq, tables=dt_, seq_lens=dl)
-            hout.copy_(out, non_blocking=True)
+            hout.copy_(result, non_blocking=True)
             torch.cuda.current_stream().synchronize()   # the host reads the result each step
         e2e_s = max_over_ranks((time.perf_counter() - s0) / args.steps, world)
         e2e = {"value": world * ab["total"] / e2e_s / 1e9, "unit": "GB/s",
@@ -506,6 +531,8 @@ def run_ours(args, world, rank, local):
             "e2e": e2e,
             "cpu_baseline": cpu,
         }
+        if wo_info:
+            line["wo"] = wo_info
         print(json.dumps(line), flush=True)
 
 
@@ -674,8 +701,11 @@ def main():
                     help="keys in the oracle's bounded sample")
     ap.add_argument("--cpu-tokens", type=int, default=1 << 40,
                     help="keys in the cpu_baseline sample (default: the whole workload)")
-    ap.add_argument("--op", default="decode", choices=["decode", "append"],
-                    help="decode: the attention step (default); append: the KV append")
+    ap.add_argument("--op", default="decode", choices=["decode", "append", "wo"],
+                    help="decode: the attention step (default); append: the KV append; "
+                         "wo: attention + output projection")
+    ap.add_argument("--wo-hidden", type=int, default=5120,
+                    help="columns of W_O for --op wo")
     ap.add_argument("--append-tokens", type=int, default=0,
                     help="tokens per append call (default: the workload's)")
     args = ap.parse_args()

@@ -245,6 +245,28 @@ size_t pa_sparse_workspace_bytes(const pa_kv_cache *kv, const pa_problem *prob,
 int pa_decode_sparse(const pa_kv_cache *kv, const pa_problem *prob, const pa_sparse *sp,
                      const pa_options *opt, void *ws, size_t ws_bytes, pa_stream_t stream);
 
+/* Attention followed by the output projection in the same call: for every
+ * query token, y[token, :] = o[token, :] . W_O with o that token's output
+ * of all num_q_heads heads flattened (index head * head_dim + d) ("vLLM
+ * Fork with focus on GB10 Homelabs", "Roadmap": fused attention + W_O
+ * GEMV, K-parallel split).  W_O is bf16 [num_q_heads * head_dim, hidden]
+ * row-major; y is [batch * q_len, hidden], bf16 or fp32 (y_fp32).  hidden
+ * must be a multiple of 8.  prob->out may be NULL (o then stays in the
+ * workspace); if given it must be fp32 (out_fp32 = 1) and receives o.
+ * q_len > 1 runs the verify attention.  k_split: 0 = automatic. */
+typedef struct pa_wo {
+  const void *w;        /* bf16 [num_q_heads * head_dim, hidden], 16-byte aligned */
+  int32_t hidden;
+  void *y;
+  int32_t y_fp32;
+  int32_t k_split;
+} pa_wo;
+
+size_t pa_decode_wo_workspace_bytes(const pa_kv_cache *kv, const pa_problem *prob,
+                                    const pa_wo *wo, const pa_options *opt);
+int pa_decode_wo(const pa_kv_cache *kv, const pa_problem *prob, const pa_wo *wo,
+                 const pa_options *opt, void *ws, size_t ws_bytes, pa_stream_t stream);
+
 /* KV append: quantise-on-write of the new tokens' K and V into the pool --
  * the write side of the paged cache (PagedAttention, "vLLM Fork with focus
  * on GB10 Homelabs", "About"): row (t, h) goes to block slot_mapping[t] / 16,

@@ -342,9 +342,80 @@ SparseLayout sparse_layout(const pa_kv_cache *kv, const pa_problem *p, const pa_
   return S;
 }
 
+// ---- attention + output projection: o (fp32) in the workspace or the
+// caller's fp32 out, then the tensor-core W_O product.
+struct WoLayout {
+  pa_problem prob;   // with out pointing at o
+  int M, K, splits;
+  size_t attn_ws, o, part, total;
+};
+
+int check_wo(const pa_kv_cache *kv, const pa_problem *p, const pa_wo *wo) {
+  if (!wo || !p) return PA_ERR_INVALID_ARG;
+  if (wo->hidden < 8 || wo->hidden % 8 || wo->k_split < 0) return PA_ERR_INVALID_ARG;
+  if (p->out && !p->out_fp32) return PA_ERR_INVALID_ARG;
+  if (p->batch > 0 && (!wo->w || !wo->y || !aligned16(wo->w) || !aligned16(wo->y)))
+    return PA_ERR_INVALID_ARG;
+  if ((long long)p->num_q_heads * kv->head_dim > (1LL << 24)) return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+WoLayout wo_layout(const pa_kv_cache *kv, const pa_problem *p, const pa_wo *wo,
+                   const pa_options *o) {
+  WoLayout W;
+  W.prob = *p;
+  W.prob.out_fp32 = 1;
+  W.M = p->batch * p->q_len;
+  W.K = p->num_q_heads * kv->head_dim;
+  W.splits = wo_splits(std::max(W.M, 1), W.K, wo->hidden, wo->k_split);
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  pa_problem sizing = W.prob;
+  const Layout a = make_layout(kv, &sizing, o, 1);
+  size_t attn = a.total;
+  if (p->q_len > 1) attn = std::max(attn, make_layout(kv, &sizing, o, 2).total);
+  W.attn_ws = up(attn);
+  W.o = W.attn_ws;
+  W.part = W.o + up((size_t)W.M * W.K * 4);
+  W.total = W.part + up(W.splits > 1 ? (size_t)W.splits * W.M * wo->hidden * 4 : 0);
+  return W;
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t pa_decode_wo_workspace_bytes(const pa_kv_cache *kv, const pa_problem *prob,
+                                    const pa_wo *wo, const pa_options *opt) {
+  if (check_kv(kv) != PA_OK || !prob) return 0;
+  if (prob->batch < 0 || prob->q_len < 1 || prob->q_len > kMaxQLen || prob->max_seq_len < 0)
+    return 0;
+  if (prob->num_q_heads < 1 || prob->num_q_heads % kv->num_kv_heads) return 0;
+  if (check_wo(kv, prob, wo) != PA_OK) return 0;
+  return wo_layout(kv, prob, wo, opt).total;
+}
+
+int pa_decode_wo(const pa_kv_cache *kv, const pa_problem *prob, const pa_wo *wo,
+                 const pa_options *opt, void *ws, size_t ws_bytes, pa_stream_t stream) {
+  int st = check_kv(kv);
+  if (st) return st;
+  if (!prob) return PA_ERR_INVALID_ARG;
+  st = check_wo(kv, prob, wo);
+  if (st) return st;
+  if (prob->batch == 0) return PA_OK;
+  if (!ws || !aligned16(ws)) return PA_ERR_INVALID_ARG;
+  WoLayout W = wo_layout(kv, prob, wo, opt);
+  if (ws_bytes < W.total) return PA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  float *o = prob->out ? static_cast<float *>(prob->out) : reinterpret_cast<float *>(w + W.o);
+  W.prob.out = o;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  st = run_attention(kv, &W.prob, opt, ws, W.attn_ws, s, prob->q_len > 1);
+  if (st) return st;
+  if (launch_wo(o, W.M, W.K, wo->w, wo->hidden, W.splits, reinterpret_cast<float *>(w + W.part),
+                wo->y, wo->y_fp32 ? 1 : 0, static_cast<uint32_t *>(ws), s) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
 
 int pa_block_means(const pa_kv_cache *kv, const int32_t *block_tables, int32_t stride,
                    const int32_t *seq_lens, const int32_t *first, int32_t count, int32_t batch,

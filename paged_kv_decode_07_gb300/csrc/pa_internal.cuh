@@ -153,6 +153,12 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // Programmatic dependent launch: a kernel launched with the
 // programmatic-serialization attribute may start before its predecessor in
 // the stream finishes; griddep_wait() blocks until the predecessor has
@@ -286,6 +292,9 @@ cudaError_t launch_sparse_select(const KvView &kv, const __nv_bfloat16 *q, int H
                                  int max_nsb, int top_k, const float *means, float *scores,
                                  int *selected, int *vtables, int vstride, int *vlens,
                                  uint32_t *err, cudaStream_t s);
+int wo_splits(int M, int K, int N, int requested);
+cudaError_t launch_wo(const float *o, int M, int K, const void *w, int N, int splits, float *part,
+                      void *y, int y_fp32, uint32_t *hdr, cudaStream_t s);
 cudaError_t launch_append(const KvView &kv, const void *k_new, const void *v_new, int T,
                           const int64_t *slots, uint32_t *hdr, cudaStream_t s);
 cudaError_t launch_gather(const KvView &kv, const int *tables, int stride, const int *seq_lens,

@@ -37,6 +37,7 @@ PA_ERRF_BAD_SLOT = 0x40
 
 EXPORTED = ("pa_workspace_bytes", "pa_decode", "pa_verify", "pa_merge", "pa_dequant_gather",
             "pa_append_kv", "pa_block_means", "pa_sparse_workspace_bytes", "pa_decode_sparse",
+            "pa_decode_wo_workspace_bytes", "pa_decode_wo",
             "pa_read_error", "pa_status_string", "pa_version")
 
 
@@ -68,6 +69,11 @@ class _Sparse(ctypes.Structure):
     _fields_ = [("sparse_block", ctypes.c_int32), ("top_k", ctypes.c_int32),
                 ("max_sparse_blocks", ctypes.c_int32), ("means", ctypes.c_void_p),
                 ("selected", ctypes.c_void_p)]
+
+
+class _Wo(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("hidden", ctypes.c_int32), ("y", ctypes.c_void_p),
+                ("y_fp32", ctypes.c_int32), ("k_split", ctypes.c_int32)]
 
 
 class _Options(ctypes.Structure):
@@ -108,6 +114,10 @@ def lib():
         L.pa_sparse_workspace_bytes.argtypes = [P, P, P, P]
         L.pa_decode_sparse.restype = ctypes.c_int
         L.pa_decode_sparse.argtypes = [P, P, P, P, P, ctypes.c_size_t, P]
+        L.pa_decode_wo_workspace_bytes.restype = ctypes.c_size_t
+        L.pa_decode_wo_workspace_bytes.argtypes = [P, P, P, P]
+        L.pa_decode_wo.restype = ctypes.c_int
+        L.pa_decode_wo.argtypes = [P, P, P, P, P, ctypes.c_size_t, P]
         L.pa_append_kv.restype = ctypes.c_int
         L.pa_append_kv.argtypes = [P, P, P, i32, P, P, P]
         L.pa_read_error.restype = ctypes.c_int
@@ -317,6 +327,43 @@ def decode_sparse(kv: KvCache, q, block_tables, seq_lens, softmax_scale, means, 
         res.append(sel)
     res.append(workspace)
     return tuple(res)
+
+
+def decode_wo(kv: KvCache, q, block_tables, seq_lens, softmax_scale, w_o, *, y=None,
+              y_fp32=False, out=None, return_lse=False, k_split=0, max_seq_len=None,
+              workspace=None, kernel=0, split_blocks=0, target_items=0, events=None,
+              stream=None):
+    """Attention (q_len 1: decode, > 1: verify) and the output projection
+    y = o . W_O in one call.  w_o bf16 [Hq * D, hidden]; returns (y
+    [B * Q, hidden], [lse,] workspace); `out` (fp32 [B, Q, Hq, D]) receives o."""
+    B, Q, Hq, D = q.shape
+    hidden = int(w_o.shape[1])
+    assert w_o.dtype == torch.bfloat16 and w_o.is_contiguous() and int(w_o.shape[0]) == Hq * D
+    if y is None:
+        y = torch.empty((B * Q, hidden), dtype=torch.float32 if y_fp32 else torch.bfloat16,
+                        device=q.device)
+    y_fp32 = y.dtype == torch.float32
+    if out is not None:
+        assert out.dtype == torch.float32
+    lse = torch.empty((B, Q, Hq), dtype=torch.float32, device=q.device) if return_lse else None
+    if max_seq_len is None:
+        max_seq_len = int(block_tables.shape[1]) * kv.block_size
+    opts = _options(kernel, split_blocks, target_items, events)
+    kvs = kv.struct()
+    prob = _Problem(B, Hq, Q, _ptr(q), _ptr(block_tables), int(block_tables.shape[1]),
+                    _ptr(seq_lens), int(max_seq_len), float(softmax_scale), _ptr(out), 1,
+                    _ptr(lse))
+    wo = _Wo(_ptr(w_o), hidden, _ptr(y), 1 if y_fp32 else 0, int(k_split))
+    need = int(lib().pa_decode_wo_workspace_bytes(ctypes.byref(kvs), ctypes.byref(prob),
+                                                  ctypes.byref(wo), ctypes.byref(opts)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = lib().pa_decode_wo(ctypes.byref(kvs), ctypes.byref(prob), ctypes.byref(wo),
+                            ctypes.byref(opts), _ptr(workspace), workspace.numel(),
+                            _stream(stream))
+    if st != PA_OK:
+        raise PaError("pa_decode_wo", st)
+    return (y, lse, workspace) if return_lse else (y, workspace)
 
 
 def append_kv(kv: KvCache, k_new, v_new, slot_mapping, workspace=None, stream=None):

@@ -164,3 +164,27 @@ def test_sparse_argument_checks(L):
     assert bm(ctypes.byref(kv), F, 8, F, None, 0, 2, 40, 8, F, None, None) == pa.PA_ERR_UNSUPPORTED
     assert bm(ctypes.byref(kv), None, 8, F, None, 0, 2, 64, 8, F, None, None) == pa.PA_ERR_INVALID_ARG
     assert bm(ctypes.byref(kv), F, 8, F, None, 0, 0, 64, 8, F, None, None) == pa.PA_OK
+
+
+def test_wo_argument_checks(L):
+    F = ctypes.c_void_p(FAKE)
+    kv = kv_struct(dtype=1)
+    p = prob_struct(B=32, Hq=24, stride=2048, max_len=32768, out=None)
+    o = pa._Options(0, 0, 0, None, None)
+    wo = pa._Wo(FAKE, 5120, FAKE, 0, 0)
+    ws = L.pa_decode_wo_workspace_bytes(ctypes.byref(kv), ctypes.byref(p), ctypes.byref(wo),
+                                        ctypes.byref(o))
+    # at least o in fp32 (32 x 6144 x 4) on top of the attention workspace
+    assert ws >= 32 * 6144 * 4 + L.pa_workspace_bytes(ctypes.byref(kv), ctypes.byref(p),
+                                                      ctypes.byref(o))
+    for bad in (pa._Wo(FAKE, 100, FAKE, 0, 0),      # hidden not a multiple of 8
+                pa._Wo(FAKE, 5120, FAKE, 0, -1)):   # negative split
+        assert L.pa_decode_wo_workspace_bytes(ctypes.byref(kv), ctypes.byref(p), ctypes.byref(bad),
+                                              ctypes.byref(o)) == 0
+    assert L.pa_decode_wo(ctypes.byref(kv), ctypes.byref(p), None, None, F, 1 << 30,
+                          None) == pa.PA_ERR_INVALID_ARG
+    p_bf16_out = prob_struct(B=32, Hq=24, stride=2048, max_len=32768)   # out given, not fp32
+    assert L.pa_decode_wo(ctypes.byref(kv), ctypes.byref(p_bf16_out), ctypes.byref(wo), None, F,
+                          1 << 30, None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_decode_wo(ctypes.byref(kv), ctypes.byref(p), ctypes.byref(wo), None, F, 64,
+                          None) == pa.PA_ERR_WORKSPACE_TOO_SMALL
