@@ -4,7 +4,7 @@
 #include <cmath>
 #include <cstring>
 
-#include "pa_internal.cuh"
+#include "pa_launch.h"
 
 namespace pa {
 cudaError_t launch_decode_simt_bf16(const AttnParams &p, int grid, cudaStream_t s);

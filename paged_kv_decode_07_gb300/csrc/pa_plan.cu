@@ -24,6 +24,10 @@ namespace pa {
 namespace {
 
 constexpr int kThreads = 1024;
+// batches of up to this many sequences keep the planner's per-sequence
+// arrays in shared memory (the item sweep's binary searches then cost no
+// global-memory round trips); larger ones use the workspace scratch
+constexpr int kSmemGroups = 2048;
 
 // A group is one sequence: in virtual mode with q_len > 1 its q_len units
 // share partition boundaries (taken from the group's longest unit), and its
@@ -89,7 +93,8 @@ __device__ __forceinline__ int2 block_scan2(int2 v, int2 &tot) {
   return r;
 }
 
-__device__ __forceinline__ int upper_bound_minus1(const int *pre, int n, int j) {
+template <typename P>
+__device__ __forceinline__ int upper_bound_minus1(const P *pre, int n, int j) {
   int lo = 0, hi = n;  // first index with pre[idx] > j
   while (lo < hi) {
     int mid = (lo + hi) >> 1;
@@ -106,6 +111,8 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
   __shared__ uint32_t s_err;
   __shared__ int2 s_tot;
   __shared__ int s_W;
+  __shared__ int s_pa[kSmemGroups], s_pb[kSmemGroups];         // item prefix per group
+  __shared__ int s_parts[kSmemGroups], s_nblk[kSmemGroups], s_slot[kSmemGroups];
   griddep_launch();   // the attention kernel may launch now; it waits for this grid to finish
   const int tid = threadIdx.x;
   const int U = p.B * group_size(p);
@@ -117,6 +124,9 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
 
   const int GS = group_size(p);
   const int NG = p.B;                    // groups = sequences
+  const bool sm = NG <= kSmemGroups;
+  int *pa = sm ? s_pa : p.prefix_a;
+  int *pb = sm ? s_pb : p.prefix_b;
   // sweep 1: total key blocks over all units (the work the kernel streams)
   uint32_t err = 0;
   unsigned long long tot = 0;
@@ -159,7 +169,12 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
     int2 v = make_int2(multi ? parts * GS * p.hkv : 0, multi ? parts * GS : 0);
     int2 ex = block_scan2(v, s_tot);
     if (g < NG) {
-      p.prefix_a[g] = carry.x + ex.x;
+      pa[g] = carry.x + ex.x;
+      if (sm) {
+        s_parts[g] = parts;
+        s_nblk[g] = nblk;
+        s_slot[g] = multi ? carry.y + ex.y : -1;
+      }
       for (int i = 0; i < GS; ++i) {
         UnitInfo ui;
         ui.parts = parts;
@@ -179,10 +194,10 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
   for (int base = 0; base < NG; base += kThreads) {
     const int g = base + tid;
     int single = 0;
-    if (g < NG) single = p.units[g * GS].parts == 1;
+    if (g < NG) single = (sm ? s_parts[g] : p.units[g * GS].parts) == 1;
     int2 v = make_int2(single ? GS * p.hkv : 0, 0);
     int2 ex = block_scan2(v, s_tot);
-    if (g < NG) p.prefix_b[g] = carry_b.x + ex.x;
+    if (g < NG) pb[g] = carry_b.x + ex.x;
     __syncthreads();
     carry_b.x += s_tot.x;
     __syncthreads();
@@ -201,25 +216,35 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
   for (int j = tid; j < num_items; j += kThreads) {
     int g, local;
     if (j < items_a) {
-      g = upper_bound_minus1(p.prefix_a, NG, j);
-      local = j - p.prefix_a[g];
+      g = upper_bound_minus1(pa, NG, j);
+      local = j - pa[g];
     } else {
-      g = upper_bound_minus1(p.prefix_b, NG, j - items_a);
-      local = j - items_a - p.prefix_b[g];
+      g = upper_bound_minus1(pb, NG, j - items_a);
+      local = j - items_a - pb[g];
     }
     const int part = local / per_part, rem = local % per_part;
     const int i = rem / p.hkv, kvh = rem % p.hkv;
     const int u = g * GS + i;
-    const UnitInfo ui = p.units[u];
-    const int chunk = (ui.nblk + ui.parts - 1) / ui.parts;
+    int parts, nblk, slot_base;
+    if (sm) {   // every unit of a group shares its parts and blocks
+      parts = s_parts[g];
+      nblk = s_nblk[g];
+      slot_base = parts > 1 ? s_slot[g] + i * parts : -1;
+    } else {
+      const UnitInfo ui = p.units[u];
+      parts = ui.parts;
+      nblk = ui.nblk;
+      slot_base = ui.slot_base;
+    }
+    const int chunk = (nblk + parts - 1) / parts;
     WorkItem it;
     it.unit = u;
     it.kvh = kvh;
     it.blk_begin = part * chunk;
-    it.blk_end = min(ui.nblk, it.blk_begin + chunk);
+    it.blk_end = min(nblk, it.blk_begin + chunk);
     it.part = part;
-    it.parts = ui.parts;
-    it.slot = ui.parts > 1 ? ui.slot_base + part : -1;
+    it.parts = parts;
+    it.slot = parts > 1 ? slot_base + part : -1;
     it.pad = 0;
     p.items[j] = it;
   }
