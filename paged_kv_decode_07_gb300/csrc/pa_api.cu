@@ -35,6 +35,22 @@ cudaError_t launch_verify_int8(const AttnParams &p, int grid, cudaStream_t s);
 cudaError_t launch_verify_nvfp4(const AttnParams &p, int grid, cudaStream_t s);
 cudaError_t launch_verify_fp8(const AttnParams &p, int grid, cudaStream_t s);
 
+cudaError_t launch_verify_umma_nvfp4(const AttnParams &p, int max_items, cudaStream_t s);
+cudaError_t launch_verify_umma_fp8(const AttnParams &p, int max_items, cudaStream_t s);
+
+// tcgen05 verify (accumulators in tensor memory): NVFP4 / FP8, D = 256
+int umma_supported(int dtype, int D, int Q) {
+  return (dtype == PA_KV_NVFP4 || dtype == PA_KV_FP8) && D == 256 && Q > 1;
+}
+
+cudaError_t launch_verify_umma(const AttnParams &p, int max_items, cudaStream_t s) {
+  switch (p.kv.dtype) {
+    case PA_KV_NVFP4: return launch_verify_umma_nvfp4(p, max_items, s);
+    case PA_KV_FP8: return launch_verify_umma_fp8(p, max_items, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_verify_dense(const AttnParams &p, int grid, cudaStream_t s) {
   switch (p.kv.dtype) {
     case PA_KV_INT8: return launch_verify_int8(p, grid, s);
@@ -199,7 +215,7 @@ int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *
   st = check_problem(kv, p, verify ? kMaxQLen : 1);
   if (st) return st;
   const int kernel = o ? o->kernel : 0;
-  if (kernel < 0 || kernel > 3) return PA_ERR_INVALID_ARG;
+  if (kernel < 0 || kernel > 4) return PA_ERR_INVALID_ARG;
   if (o && (o->split_blocks < 0 || o->target_items < 0)) return PA_ERR_INVALID_ARG;
   if (p->batch == 0) return PA_OK;
   const int G = p->num_q_heads / kv->num_kv_heads;
@@ -209,8 +225,12 @@ int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *
   // runs as one dense tile of q_len * G rows when supported; otherwise every
   // kernel runs it as a virtual batch (one unit per query token).
   const int Q = p->q_len;
-  bool use_tc, dense = false;
-  if (kernel == 2 || kernel == 3) {
+  bool use_tc, dense = false, umma = false;
+  if (kernel == 4) {
+    if (!umma_supported(kv->dtype, kv->head_dim, Q) || !tc_supported(kv->dtype, kv->head_dim, G))
+      return PA_ERR_UNSUPPORTED;
+    use_tc = dense = umma = true;
+  } else if (kernel == 2 || kernel == 3) {
     if (!tc_supported(kv->dtype, kv->head_dim, G)) return PA_ERR_UNSUPPORTED;
     use_tc = true;
     dense = kernel == 2 && dense_supported(kv->dtype, kv->head_dim, Q, G);
@@ -239,7 +259,18 @@ int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *
   pp.RG = RG;
   pp.hkv = kv->num_kv_heads;
   pp.capacity = (int)std::min<long long>((long long)p->block_table_stride * kBlock, 1LL << 30);
-  pp.target_items = (o && o->target_items > 0) ? std::min(o->target_items, kMaxTargetItems) : 1184;
+  // auto target: about 8 items per SM for the one-CTA-per-item kernels; the
+  // persistent tcgen05 verify kernel pays a fixed cost per item (its q tile,
+  // epilogue and first-tile rescale), so it gets about 2 per SM
+  int auto_target = 1184;
+  if (umma) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
+      auto_target = std::min(2 * sms, kMaxTargetItems);
+  }
+  pp.target_items = (o && o->target_items > 0) ? std::min(o->target_items, kMaxTargetItems)
+                                               : auto_target;
   pp.split_blocks = o ? o->split_blocks : 0;
   pp.min_split_blocks = kMinSplitBlocks;
   pp.max_items = L.max_items;
@@ -281,7 +312,8 @@ int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *
   if (o && o->event_begin &&
       cudaEventRecord(static_cast<cudaEvent_t>(o->event_begin), stream) != cudaSuccess)
     return PA_ERR_CUDA;
-  if ((dense ? launch_verify_dense(ap, L.max_items, stream)
+  if ((umma    ? launch_verify_umma(ap, L.max_items, stream)
+       : dense ? launch_verify_dense(ap, L.max_items, stream)
              : use_tc ? launch_decode_tc(ap, L.max_items, stream)
                       : launch_decode_simt(ap, L.max_items, stream)) != cudaSuccess)
     return PA_ERR_CUDA;

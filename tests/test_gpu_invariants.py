@@ -144,25 +144,29 @@ def test_two_shards_merged_equal_single_call():
                                atol=2e-5, rtol=0)
 
 
+@pytest.mark.parametrize("kernel", [2, 4])
 @pytest.mark.parametrize("dt", ["nvfp4", "int8", "fp8"])
-def test_dense_verify_invariants(dt):
-    """Dense-tile verify: bitwise block-permutation invariance and
-    determinism; forced single / tiny partitions agree with the oracle; a bad
-    block id is skipped and flagged."""
+def test_dense_verify_invariants(dt, kernel):
+    """Dense-tile verify (mma.sync kernel 2, tcgen05 kernel 4): bitwise
+    block-permutation invariance and determinism; forced single / tiny
+    partitions agree with the oracle; a bad block id is skipped and
+    flagged."""
+    if kernel == 4 and dt == "int8":
+        pytest.skip("the tcgen05 verify kernel takes NVFP4 and FP8")
     wl = W.make_workload(VERIFY_NAMES[dt], device=DEV, seq_lens=[1500, 8, 300], Q=8)
-    a, la, ws = run(wl, "verify", out_fp32=True, return_lse=True, kernel=2)
-    b, lb, _ = run(wl, "verify", out_fp32=True, return_lse=True, kernel=2)
+    a, la, ws = run(wl, "verify", out_fp32=True, return_lse=True, kernel=kernel)
+    b, lb, _ = run(wl, "verify", out_fp32=True, return_lse=True, kernel=kernel)
     assert torch.equal(a, b) and torch.equal(la, lb)
-    c, _ = run(W.permute_pool(wl, seed=5), "verify", out_fp32=True, kernel=2)
+    c, _ = run(W.permute_pool(wl, seed=5), "verify", out_fp32=True, kernel=kernel)
     assert torch.equal(a, c)
     ref, _ = oracle_rows(wl)
     for kw in (dict(split_blocks=1 << 20), dict(split_blocks=1), dict(target_items=5)):
-        o, _ = run(wl, "verify", out_fp32=True, kernel=2, **kw)
+        o, _ = run(wl, "verify", out_fp32=True, kernel=kernel, **kw)
         compare(o, ref, f"dense verify {dt} {kw}")
     bad = wl.block_tables.clone()
     bad[0, 7] = -1
     o, ws = run(W.Workload(**{**wl.__dict__, "block_tables": bad}), "verify", out_fp32=True,
-                kernel=2)
+                kernel=kernel)
     torch.cuda.synchronize()
     assert pa.read_error(ws) & pa.PA_ERRF_BAD_BLOCK_ID
     assert torch.isfinite(o).all()

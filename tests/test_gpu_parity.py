@@ -36,13 +36,17 @@ def _fn(wl):
     return "verify" if wl.Q > 1 else "decode"
 
 
-def _kernels(dtype):
+def _kernels(dtype, q_len=1):
     """0 = auto; 1 = CUDA-core kernel; 2 = tensor-core kernel (verify: dense
-    tile); 3 = tensor-core kernel with verify as one unit per query token."""
+    tile); 3 = tensor-core kernel with verify as one unit per query token;
+    4 = tcgen05 verify (NVFP4 / FP8, q_len > 1)."""
+    if dtype in ("nvfp4", "fp8") and q_len > 1:
+        return [0, 1, 2, 3, 4]
     return [0, 1, 2, 3] if dtype in ("int8", "nvfp4", "fp8") else [0, 1]
 
 
-REDUCED_CASES = [(n, k) for n in REDUCED for k in _kernels(W.spec(n)["dtype"])]
+REDUCED_CASES = [(n, k) for n in REDUCED
+                 for k in _kernels(W.spec(n)["dtype"], W.spec(n).get("Q", 1))]
 
 
 @pytest.mark.parametrize("name,kernel", REDUCED_CASES)
@@ -128,9 +132,11 @@ def test_gqa_and_head_dim_variants(dt, kernel, shape):
 
 
 @pytest.mark.parametrize("Q", [2, 5, 8, 16])
-@pytest.mark.parametrize("kernel", [1, 2, 3])
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4])
 @pytest.mark.parametrize("dt", ["nvfp4", "int8", "fp8"])
 def test_verify_q_lens(Q, kernel, dt):
+    if kernel == 4 and dt == "int8":
+        pytest.skip("the tcgen05 verify kernel takes NVFP4 and FP8")
     wl = W.make_workload(VERIFY_NAMES[dt], device=DEV, seq_lens=[900, Q, 33, 3000], Q=Q)
     o32, lse, _ = run(wl, "verify", out_fp32=True, return_lse=True, kernel=kernel)
     ref_o, ref_l = oracle_rows(wl)
@@ -153,3 +159,34 @@ def test_merge_entry_point_matches_oracle():
     assert (lse.cpu().numpy()[~fin] == -np.inf).all()
     ob = pa.merge(po.to(DEV), pl.to(DEV))
     assert bf16_matches_fp32(ob, out)
+
+
+@pytest.mark.parametrize("split", [5, 13, 21, 1 << 20])
+@pytest.mark.parametrize("name", ["nvfp4_verify_q8_b4_ctx64k_d256", "fp8_verify_q8_b4_ctx64k_d256"])
+def test_umma_verify_many_items_per_cta(name, split):
+    """tcgen05 verify with partitions of `split` blocks: every CTA walks
+    several items whose last 128-token tile is partial (5, 13, 21 blocks) or
+    one long item per (sequence, kv head); each must match the oracle."""
+    wl = W.make_workload(name, device=DEV, seq_lens=[4104, 3001, 777, 9, 2048, 1500])
+    o32, lse, ws = run(wl, "verify", out_fp32=True, return_lse=True, kernel=4, split_blocks=split)
+    torch.cuda.synchronize()
+    assert pa.read_error(ws) == 0
+    ref_o, ref_l = oracle_rows(wl)
+    compare(o32, ref_o, f"{name} split {split}")
+    compare_lse(lse, ref_l, f"{name} split {split}")
+
+
+@pytest.mark.parametrize("name", ["nvfp4_verify_q8_b4_ctx64k_d256", "fp8_verify_q8_b4_ctx64k_d256"])
+def test_umma_verify_full_size_sampled(name):
+    """tcgen05 verify at the full workload size in the benchmark's launch
+    configuration, checked on sampled sequences against the oracle."""
+    wl = W.make_workload(name, device=DEV)
+    o32, lse, ws = run(wl, "verify", out_fp32=True, return_lse=True, kernel=4)
+    torch.cuda.synchronize()
+    assert pa.read_error(ws) == 0
+    bs = [0, wl.B - 1]
+    ref_o, ref_l = oracle_rows(wl, bs)
+    compare(o32[bs], ref_o, name)
+    compare_lse(lse[bs], ref_l, name)
+    del wl
+    torch.cuda.empty_cache()
