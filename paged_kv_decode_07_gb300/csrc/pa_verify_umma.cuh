@@ -366,9 +366,12 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
 constexpr uint32_t kSleepNs = 20000;        // one suspension: 20 us at most
 constexpr uint32_t kSleepCap = 1u << 16;    // => a wait gives up after ~1.3 s
 
-// capped wait that also gives up once another role has given up
+// capped wait that also gives up once another role has given up (the loop
+// stays rolled: every call site would otherwise carry unrolled copies, and
+// the kernel's code must fit the instruction caches of four roles at once)
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Ctl &c, uint32_t *hdr) {
   volatile int *ab = &c.abort;
+#pragma unroll 1
   for (uint32_t i = 0; i < kSleepCap; ++i) {
     if (mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
     if (*ab) return false;
@@ -376,6 +379,13 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Ctl &c,
   *ab = 1;
   set_err(hdr, PA_ERRF_WAIT_TIMEOUT);
   return false;
+}
+
+// capped wait without the abort check (draining before exit)
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+#pragma unroll 1
+  for (uint32_t i = 0; i < kSleepCap; ++i)
+    if (mbar_try_wait_sleep(bar, parity, kSleepNs)) return;
 }
 
 // ------------------------------------------------------------------ roles
@@ -431,9 +441,9 @@ __device__ void role_producer(const AttnParams &p, const CUtensorMap *tmK, const
   }
   // the last fill of every stage may still be in flight after a failure:
   // let the copies land before the CTA exits
-#pragma unroll
+#pragma unroll 1
   for (int s = 0; s < Gm::NR; ++s)
-    if (ruse[s] > 0) (void)mbar_wait(&c.rawfull[s], (ruse[s] - 1) & 1);
+    if (ruse[s] > 0) drain_wait(&c.rawfull[s], (ruse[s] - 1) & 1);
 }
 
 // warp 1, one thread: QK of tile g, then PV of tile g - 1 (so that the
@@ -464,7 +474,7 @@ __device__ void role_mma(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t tm
     tc_fence_after();
     const uint32_t dO = tmem + kColO + (t.oi & 1) * 128;
     const uint64_t dP = (t.g & 1) ? dP1 : dP0;
-#pragma unroll
+#pragma unroll 1
     for (int j = 0; j < kTileBlocks; ++j) {
       if (j < t.nb) {
         const uint64_t bd = dP + (uint64_t)(((j >> 2) * Gm::QCH + (j & 3) * 32) >> 4);
@@ -519,7 +529,7 @@ __device__ void role_mma(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t tm
   }
   if (ok && pend.on) (void)issue_pv(pend);
   tc_commit(&c.done);   // tensor memory is released only after every MMA completes
-  (void)mbar_wait(&c.done, 0);
+  drain_wait(&c.done, 0);
 }
 
 
@@ -533,8 +543,7 @@ __device__ __forceinline__ void deq_row(uint32_t st, int code_off, int scale_off
   const uint4 z = make_uint4(0, 0, 0, 0);
   if constexpr (DT == PA_KV_NVFP4) {
     const uint4 sc = valid ? lds_u4(st + scale_off + r * 16) : z;
-    const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
-#pragma unroll
+#pragma unroll 1
     for (int u = 0; u < 8; ++u) {
       const uint4 w = valid ? lds_u4(st + code_off + tc::sw_off(r, 16 * u)) : z;
       uint32_t h0[4], h1[4], h2[4], h3[4];
@@ -542,7 +551,8 @@ __device__ __forceinline__ void deq_row(uint32_t st, int code_off, int scale_off
       tc::e2m1x8_to_h2x4(w.y, h1);
       tc::e2m1x8_to_h2x4(w.z, h2);
       tc::e2m1x8_to_h2x4(w.w, h3);
-      const uint32_t sw = scw[u >> 1] >> (16 * (u & 1));   // scale bytes 2u, 2u + 1
+      const uint32_t w4 = (u >> 1) == 0 ? sc.x : (u >> 1) == 1 ? sc.y : (u >> 1) == 2 ? sc.z : sc.w;
+      const uint32_t sw = w4 >> (16 * (u & 1));   // scale bytes 2u, 2u + 1
       const uint32_t s0 = e4m3_to_h2_dup(sw & 0xffu), s1 = e4m3_to_h2_dup((sw >> 8) & 0xffu);
       uint32_t h[16];
 #pragma unroll
@@ -555,7 +565,7 @@ __device__ __forceinline__ void deq_row(uint32_t st, int code_off, int scale_off
       sink(u, h);
     }
   } else {   // FP8-E4M3: one byte per element, exact in f16
-#pragma unroll
+#pragma unroll 1
     for (int u = 0; u < 8; ++u) {
       const uint4 w0 = valid ? lds_u4(st + code_off + tc::sw_off(r, 32 * u)) : z;
       const uint4 w1 = valid ? lds_u4(st + code_off + tc::sw_off(r, 32 * u + 16)) : z;
@@ -794,18 +804,7 @@ __device__ void role_softmax(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_
         }
       }
     };
-    if (x.n_blk == 0) {   // nothing to attend: zeros, lse -inf
-      if (t < N) c.inv[t] = 0.f;
-      named_sync(kBarSoftmax, 128);
-      float zero[N];
-#pragma unroll
-      for (int n = 0; n < N; ++n) zero[n] = 0.f;
-      store_rows(zero, t);
-      store_rows(zero, 128 + t);
-      if (t < R && lo) lo[c.orow[t]] = kNegInf;
-      named_sync(kBarSoftmax, 128);
-      continue;
-    }
+    const bool empty = x.n_blk == 0;   // nothing to attend: zeros, lse -inf
     const int lim_min = x.L - p.Q + 1 + x.ro / p.G;   // the first live row's key limit
     float lp[N];                                      // this row's share of each l
 #pragma unroll
@@ -861,17 +860,23 @@ __device__ void role_softmax(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_
       };
       // One pass with the current max; the first tile of an item (no max yet)
       // and the rare tile that raises a row's max by more than the threshold
-      // are redone after the max update below.
+      // are redone after the max update (a second pass of the same code).
       float v[N];
-      bool need = tile == 0;
-      if (tile > 0) {
-        tmem_ldn<N>(sa, v);
-        scores(v);
-        emit(v, need);
-      }
-      if (named_sync_or(kBarSoftmax, 128, need || !ok)) {
+      bool redo = tile == 0;
+      bool stop = false;
+#pragma unroll 1
+      for (int pass = 0; pass < 2; ++pass) {
+        if (!redo || pass == 1) {   // probabilities with the current max
+          tmem_ldn<N>(sa, v);
+          scores(v);
+          bool need = false;
+          emit(v, need);
+          if (pass == 1) break;
+          redo = need;
+        }
+        if (!named_sync_or(kBarSoftmax, 128, redo || !ok)) break;
         if (named_sync_or(kBarSoftmax, 128, !ok)) {
-          failed = true;
+          stop = true;
           break;
         }
         // new running max of every row: max over this tile's 128 rows
@@ -891,31 +896,36 @@ __device__ void role_softmax(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_
         if (tile > 0) {   // O^T holds this item's earlier tiles: rescale once PV(g-1) is done
           const bool ok2 = wait_bar(&c.pdone[(g - 1) & 1], ((g - 1) >> 1) & 1, c, p.hdr);
           if (named_sync_or(kBarSoftmax, 128, !ok2)) {
-            failed = true;
+            stop = true;
             break;
           }
           tc_fence_after();
           const uint32_t oa = lb + kColO + (oi & 1) * 128;
+#pragma unroll 1
+          for (int hc = 0; hc < 2 * (N / 16); ++hc) {   // (half, 16-column chunk)
+            const int h = hc / (N / 16), cb = hc % (N / 16);
+            float o[16];
+            uint32_t w[16];
+            tmem_ld16(oa + h * 64 + cb * 16, o);
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int cb = 0; cb < N / 16; ++cb) {
-              float o[16];
-              uint32_t w[16];
-              tmem_ld16(oa + h * 64 + cb * 16, o);
-#pragma unroll
-              for (int k = 0; k < 16; ++k) w[k] = __float_as_uint(o[k] * c.alpha[cb * 16 + k]);
-              tmem_st16(oa + h * 64 + cb * 16, w);
+            for (int k4 = 0; k4 < 16; k4 += 4) {
+              const float4 a4 = lds_f4(smem_u32(c.alpha) + 4 * (cb * 16 + k4));
+              w[k4] = __float_as_uint(o[k4] * a4.x);
+              w[k4 + 1] = __float_as_uint(o[k4 + 1] * a4.y);
+              w[k4 + 2] = __float_as_uint(o[k4 + 2] * a4.z);
+              w[k4 + 3] = __float_as_uint(o[k4 + 3] * a4.w);
             }
+            tmem_st16(oa + h * 64 + cb * 16, w);
+          }
           tmem_st_wait();
         }
         if (t < N) c.m[t] = c.mnew[t];
         named_sync(kBarSoftmax, 128);
-        // the tile again with the new max
-        tmem_ldn<N>(sa, v);
-        scores(v);
-        bool unused = false;
-        emit(v, unused);
+        redo = true;
+      }
+      if (stop) {
+        failed = true;
+        break;
       }
 #pragma unroll
       for (int n = 0; n < N; ++n) lp[n] += v[n];   // this row's share of l
@@ -926,9 +936,9 @@ __device__ void role_softmax(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_
       ++g;
     }
     if (failed) break;
-    // ---- epilogue: l of every row, then O^T / l
+    // ---- epilogue: l of every row, then O^T / l (zeros for an empty item)
     colreduce<N, false>(lp, lane, c.red[q4]);
-    const bool ok = wait_bar(&c.odone[oi & 1], (oi >> 1) & 1, c, p.hdr);
+    const bool ok = empty || wait_bar(&c.odone[oi & 1], (oi >> 1) & 1, c, p.hdr);
     if (named_sync_or(kBarSoftmax, 128, !ok)) {
       failed = true;
       break;
@@ -941,20 +951,27 @@ __device__ void role_softmax(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_
     named_sync(kBarSoftmax, 128);
     tc_fence_after();
     const uint32_t oa = lb + kColO + (oi & 1) * 128;
-#pragma unroll
+#pragma unroll 1
     for (int h = 0; h < 2; ++h) {
       float o[N];
-      tmem_ldn<N>(oa + h * 64, o);
+      if (!empty) {
+        tmem_ldn<N>(oa + h * 64, o);
+      } else {
+#pragma unroll
+        for (int n = 0; n < N; ++n) o[n] = 0.f;
+      }
       store_rows(o, h * 128 + t);
     }
-    tc_fence_before();
-    mbar_arrive(&c.ofree[oi & 1]);
     if (t < R && lo) {
       const float l = c.mnew[t];
       lo[c.orow[t]] = l > 0.f ? (c.m[t] + __log2f(l)) * 0.69314718055994531f : kNegInf;
     }
+    if (!empty) {
+      tc_fence_before();
+      mbar_arrive(&c.ofree[oi & 1]);
+      ++oi;
+    }
     named_sync(kBarSoftmax, 128);   // tables and sums read before the next item rewrites them
-    ++oi;
   }
 }
 
