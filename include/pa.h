@@ -127,13 +127,16 @@ typedef struct pa_problem {
 
 /* Optional knobs; pass NULL for defaults. */
 typedef struct pa_options {
-  int32_t kernel;          /* 0 auto; 1 CUDA-core (SIMT) kernel; 2 tensor-core kernel
-                              (verify: dense tiles of 16 of the q_len * G rows when the
-                              format is int8/NVFP4 and head_dim 256); 3 tensor-core kernel
-                              with verify run as one unit per query token; 4 verify on
-                              the tcgen05 tensor cores (accumulators in tensor memory;
-                              NVFP4 / FP8, head_dim 256, q_len > 1; else
-                              PA_ERR_UNSUPPORTED) */
+  int32_t kernel;          /* 0 auto: bf16 -> 1; int8 / NVFP4 / FP8 decode -> 2;
+                              int8 / FP8 verify (head_dim 256) -> 2 (dense tiles);
+                              NVFP4 verify (head_dim 256) -> 4.
+                              1 CUDA-core (SIMT) kernel; 2 tensor-core kernel (mma.sync;
+                              verify: dense tiles of up to 48 of the q_len * G rows when
+                              the format is int8/NVFP4/FP8 and head_dim 256); 3
+                              tensor-core kernel with verify run as one unit per query
+                              token; 4 verify on the tcgen05 tensor cores (accumulators
+                              in tensor memory; NVFP4 / FP8, head_dim 256, q_len > 1;
+                              else PA_ERR_UNSUPPORTED) */
   int32_t split_blocks;    /* 0 auto; >0 = fixed number of 16-token blocks per partition
                               (a value >= the longest sequence's block count disables
                               split-K) */

@@ -246,15 +246,16 @@ constexpr int kTile = 128;                 // tokens per QK tile (the MMA's M)
 constexpr int kTileBlocks = kTile / kBlock;
 constexpr int kThreads = 512;              // 4 warpgroups
 // Registers per thread of each warpgroup after the split (launched with 128
-// each): producer/MMA 112, K dequant 112, softmax 192, V dequant 96.  Per
+// each): producer/MMA 88, K dequant 128, softmax 200, V dequant 96.  Per
 // SM sub-partition (one warp of each group) 512 = 4 x 128, so every
 // setmaxnreg.inc is satisfied by the decreases.
-constexpr int kRegCtl = 112, kRegK = 112, kRegSoftmax = 192, kRegV = 96;
+constexpr int kRegCtl = 88, kRegK = 128, kRegSoftmax = 200, kRegV = 96;
 static_assert(kRegCtl + kRegK + kRegSoftmax + kRegV <= 4 * 128, "register split");
 constexpr uint32_t kTmemCols = 512;
-// tensor-memory columns (32-bit each): K tile (128 tokens x 256 f16), two S
-// buffers, two O buffers of two 128-lane halves
-constexpr uint32_t kColK = 0, kColS = 128, kColO = 256;
+// tensor-memory columns (32-bit each): two K tiles (128 tokens x 256 f16,
+// 128 columns each), two S buffers (64 columns each, N used), one O^T of two
+// 128-lane halves (64 columns each, N used)
+constexpr uint32_t kColK = 0, kColS = 256, kColO = 384;
 // named barriers (0 is __syncthreads)
 constexpr uint32_t kBarSoftmax = 1, kBarK = 2;
 
@@ -310,14 +311,16 @@ constexpr int kMaxNR = 24;
 struct Ctl {
   uint64_t rawfull[kMaxNR], rawfree[kMaxNR];   // raw stages: TMA -> K and V dequant
   uint64_t vfull, vfree;                       // f16 V tile: V dequant <-> PV
-  uint64_t kfull, kfree;                       // K in tensor memory: K dequant <-> QK
+  uint64_t kfull[2], kfree[2];                 // K buffers in tensor memory: K dequant <-> QK
   uint64_t sfull[2], sfree[2];                 // S buffers: QK <-> softmax
   uint64_t pfull[2], pdone[2];                 // P buffers: softmax <-> PV
-  uint64_t odone[2], ofree[2];                 // O buffers: last PV of an item <-> epilogue
+  uint64_t odone, ofree;                       // O^T: last PV of an item <-> epilogue
   uint64_t done;                               // every MMA of the CTA complete
   uint32_t tmem;                               // tensor-memory base address
   int abort;                                   // a capped wait ran out somewhere
   int rvalid[kMaxNR];                          // raw stage holds a valid block
+  uint32_t ruse[kMaxNR];                       // producer: fills of each raw stage so far
+  int ids[2][kTileBlocks];                     // producer: block ids of this / the next tile
   alignas(16) float m[kMaxN];                  // running max of each row (log2 domain)
   alignas(16) float mnew[kMaxN], alpha[kMaxN], inv[kMaxN];
   alignas(16) float red[4][kMaxN];
@@ -398,52 +401,71 @@ __device__ void role_producer(const AttnParams &p, const CUtensorMap *tmK, const
                               uint8_t *smem, Ctl &c, int num_items) {
   using Gm = Geo<DT, N>;
   const uint64_t pol = policy_evict_first();
-  uint32_t ruse[Gm::NR];   // fills of each raw stage so far
-#pragma unroll
-  for (int s = 0; s < Gm::NR; ++s) ruse[s] = 0;
+  // fills of each raw stage and the block ids of the current and the next
+  // tile live in shared memory (a local-memory array would cost an L2 round
+  // trip per access: most of the SM's L1 is given to shared memory)
+#pragma unroll 1
+  for (int s = 0; s < Gm::NR; ++s) c.ruse[s] = 0;
   uint32_t g = 0;
   bool ok = true;
   for (int ii = blockIdx.x; ii < num_items && ok; ii += gridDim.x) {
     const Item x = load_item(p, ii);
-    for (int j = 0; j < x.n_blk && ok; ++j) {
-      const int jt = j % kTileBlocks;
-      const int s = (int)(g % Gm::NRT) * kTileBlocks + jt;
-      if (jt == kTileBlocks - 1 || j == x.n_blk - 1) ++g;   // last block of its tile
-      if (!wait_bar(&c.rawfree[s], (ruse[s] & 1) ^ 1, c, p.hdr)) {
-        ok = false;
-        break;
-      }
-      ++ruse[s];
-      const int phys = x.trow[x.it.blk_begin + j];
-      const bool v = phys >= 0 && phys < p.kv.num_blocks;
-      c.rvalid[s] = v;
-      if (!v) {
-        set_err(p.hdr, PA_ERRF_BAD_BLOCK_ID);
-        mbar_arrive(&c.rawfull[s]);
-        continue;
-      }
-      uint8_t *st = smem + (s / kTileBlocks) * Gm::RTILE;
-      const size_t tile = (size_t)phys * p.kv.hkv + x.kvh;
-      const int y = (int)(tile * kBlock);
-      mbar_arrive_expect_tx(&c.rawfull[s], Gm::PAYLOAD);
+    // block ids are read with independent loads one tile ahead, so that no
+    // table read sits between two blocks' copies
+    int nxt[kTileBlocks];
 #pragma unroll
-      for (int xo = 0; xo < Gm::ROW; xo += 128) {
-        tc::tma_rows(st + jt * Gm::CODE + xo * kBlock, tmK, xo, y, &c.rawfull[s], pol);
-        tc::tma_rows(st + Gm::R_V + jt * Gm::CODE + xo * kBlock, tmV, xo, y, &c.rawfull[s], pol);
+    for (int k = 0; k < kTileBlocks; ++k) nxt[k] = k < x.n_blk ? x.trow[x.it.blk_begin + k] : -1;
+#pragma unroll
+    for (int k = 0; k < kTileBlocks; ++k) c.ids[0][k] = nxt[k];
+    for (int tile = 0; tile < x.ntiles && ok; ++tile, ++g) {
+      const int nb = min(kTileBlocks, x.n_blk - tile * kTileBlocks);
+      const int nb2 = min(kTileBlocks, x.n_blk - (tile + 1) * kTileBlocks);   // <= 0 at the end
+#pragma unroll
+      for (int k = 0; k < kTileBlocks; ++k)
+        nxt[k] = k < nb2 ? x.trow[x.it.blk_begin + (tile + 1) * kTileBlocks + k] : -1;
+      const int stage = (int)(g % Gm::NRT);
+      uint8_t *st = smem + stage * Gm::RTILE;
+      const int *ids = c.ids[tile & 1];
+#pragma unroll 1
+      for (int jt = 0; jt < nb; ++jt) {
+        const int s = stage * kTileBlocks + jt;
+        const uint32_t use = c.ruse[s]++;
+        if (!wait_bar(&c.rawfree[s], (use & 1) ^ 1, c, p.hdr)) {
+          ok = false;
+          break;
+        }
+        const int phys = ids[jt];
+        const bool v = phys >= 0 && phys < p.kv.num_blocks;
+        c.rvalid[s] = v;
+        if (!v) {
+          set_err(p.hdr, PA_ERRF_BAD_BLOCK_ID);
+          mbar_arrive(&c.rawfull[s]);
+          continue;
+        }
+        const size_t tile_id = (size_t)phys * p.kv.hkv + x.kvh;
+        const int y = (int)(tile_id * kBlock);
+        mbar_arrive_expect_tx(&c.rawfull[s], Gm::PAYLOAD);
+#pragma unroll
+        for (int xo = 0; xo < Gm::ROW; xo += 128) {
+          tc::tma_rows(st + jt * Gm::CODE + xo * kBlock, tmK, xo, y, &c.rawfull[s], pol);
+          tc::tma_rows(st + Gm::R_V + jt * Gm::CODE + xo * kBlock, tmV, xo, y, &c.rawfull[s], pol);
+        }
+        if constexpr (Gm::SC > 0) {
+          bulk_g2s(st + Gm::R_KS + jt * Gm::SC, (const uint8_t *)p.kv.ks + tile_id * Gm::SC, Gm::SC,
+                   &c.rawfull[s], pol);
+          bulk_g2s(st + Gm::R_VS + jt * Gm::SC, (const uint8_t *)p.kv.vs + tile_id * Gm::SC, Gm::SC,
+                   &c.rawfull[s], pol);
+        }
       }
-      if constexpr (Gm::SC > 0) {
-        bulk_g2s(st + Gm::R_KS + jt * Gm::SC, (const uint8_t *)p.kv.ks + tile * Gm::SC, Gm::SC,
-                 &c.rawfull[s], pol);
-        bulk_g2s(st + Gm::R_VS + jt * Gm::SC, (const uint8_t *)p.kv.vs + tile * Gm::SC, Gm::SC,
-                 &c.rawfull[s], pol);
-      }
+#pragma unroll
+      for (int k = 0; k < kTileBlocks; ++k) c.ids[(tile + 1) & 1][k] = nxt[k];
     }
   }
   // the last fill of every stage may still be in flight after a failure:
   // let the copies land before the CTA exits
 #pragma unroll 1
   for (int s = 0; s < Gm::NR; ++s)
-    if (ruse[s] > 0) drain_wait(&c.rawfull[s], (ruse[s] - 1) & 1);
+    if (c.ruse[s] > 0) drain_wait(&c.rawfull[s], (c.ruse[s] - 1) & 1);
 }
 
 // warp 1, one thread: QK of tile g, then PV of tile g - 1 (so that the
@@ -469,10 +491,10 @@ __device__ void role_mma(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t tm
   Pend pend = {false, false, false, 0, 0, 0};
   auto issue_pv = [&](const Pend &t) -> bool {
     if (!wait_bar(&c.pfull[t.g & 1], (t.g >> 1) & 1, c, p.hdr)) return false;
-    if (t.first && !wait_bar(&c.ofree[t.oi & 1], ((t.oi >> 1) & 1) ^ 1, c, p.hdr)) return false;
+    if (t.first && !wait_bar(&c.ofree, (t.oi & 1) ^ 1, c, p.hdr)) return false;
     if (!wait_bar(&c.vfull, t.g & 1, c, p.hdr)) return false;
     tc_fence_after();
-    const uint32_t dO = tmem + kColO + (t.oi & 1) * 128;
+    const uint32_t dO = tmem + kColO;
     const uint64_t dP = (t.g & 1) ? dP1 : dP0;
 #pragma unroll 1
     for (int j = 0; j < kTileBlocks; ++j) {
@@ -486,7 +508,7 @@ __device__ void role_mma(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t tm
     }
     tc_commit(&c.vfree);
     tc_commit(&c.pdone[t.g & 1]);
-    if (t.last) tc_commit(&c.odone[t.oi & 1]);
+    if (t.last) tc_commit(&c.odone);
     return true;
   };
   uint32_t g = 0, oi = 0;
@@ -505,7 +527,7 @@ __device__ void role_mma(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t tm
         }
         pend.on = false;
       }
-      if (!wait_bar(&c.kfull, g & 1, c, p.hdr) ||
+      if (!wait_bar(&c.kfull[g & 1], (g >> 1) & 1, c, p.hdr) ||
           !wait_bar(&c.sfree[g & 1], ((g >> 1) & 1) ^ 1, c, p.hdr)) {
         ok = false;
         break;
@@ -514,10 +536,11 @@ __device__ void role_mma(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t tm
       const uint32_t dS = tmem + kColS + (g & 1) * 64;
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
-        mma_ts(dS, tmem + kColK + ks * 8, dQ + (uint64_t)(((ks >> 2) * Gm::QCH + (ks & 3) * 32) >> 4),
+        mma_ts(dS, tmem + kColK + (g & 1) * 128 + ks * 8,
+               dQ + (uint64_t)(((ks >> 2) * Gm::QCH + (ks & 3) * 32) >> 4),
                IQK, ks > 0 ? 1u : 0u);
       tc_commit(&c.sfull[g & 1]);
-      tc_commit(&c.kfree);
+      tc_commit(&c.kfree[g & 1]);
       if (pend.on && !issue_pv(pend)) {
         ok = false;
         break;
@@ -619,7 +642,7 @@ __device__ void role_kdeq(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t t
                           int num_items, int warp, int lane) {
   using Gm = Geo<DT, N>;
   const int q4 = warp & 3, t = q4 * 32 + lane, jb = t >> 4, r = t & 15;
-  const uint32_t ta = tmem + ((uint32_t)(q4 * 32) << 16) + kColK;
+  const uint32_t ta0 = tmem + ((uint32_t)(q4 * 32) << 16) + kColK;
   uint32_t g = 0, ru[Gm::NRT] = {};   // uses of this row's raw stages
   bool failed = false;
   for (int ii = blockIdx.x; ii < num_items && !failed; ii += gridDim.x) {
@@ -636,7 +659,12 @@ __device__ void role_kdeq(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t t
 #pragma unroll
       for (int i = 0; i < Gm::NRT; ++i)
         if (i == (int)tp) use = ru[i];
-      bool ok = g == 0 || wait_bar(&c.kfree, (g - 1) & 1, c, p.hdr);
+      // K buffer g % 2 is free once QK(g - 2) completed; the q tile of a new
+      // item may be written once QK(g - 1), the last of the previous item, is
+      const uint32_t kb = g & 1;
+      bool ok = wait_bar(&c.kfree[kb], ((g >> 1) & 1) ^ 1, c, p.hdr);
+      if (ok && tile == 0 && g > 0) ok = wait_bar(&c.kfree[kb ^ 1], ((g - 1) >> 1) & 1, c, p.hdr);
+      const uint32_t ta = ta0 + kb * 128;
       if (ok && have) ok = wait_bar(&c.rawfull[s], use & 1, c, p.hdr);
       if (named_sync_or(kBarK, 128, !ok)) {   // the whole group stops together
         failed = true;
@@ -651,7 +679,7 @@ __device__ void role_kdeq(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t t
       tmem_st_wait();
       if (tile == 0) fence_async_smem();   // Q, written by this thread, for the MMA
       tc_fence_before();
-      mbar_arrive(&c.kfull);
+      mbar_arrive(&c.kfull[kb]);
       if (have) {
         mbar_arrive(&c.rawfree[s]);
 #pragma unroll
@@ -900,7 +928,7 @@ __device__ void role_softmax(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_
             break;
           }
           tc_fence_after();
-          const uint32_t oa = lb + kColO + (oi & 1) * 128;
+          const uint32_t oa = lb + kColO;
 #pragma unroll 1
           for (int hc = 0; hc < 2 * (N / 16); ++hc) {   // (half, 16-column chunk)
             const int h = hc / (N / 16), cb = hc % (N / 16);
@@ -938,7 +966,7 @@ __device__ void role_softmax(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_
     if (failed) break;
     // ---- epilogue: l of every row, then O^T / l (zeros for an empty item)
     colreduce<N, false>(lp, lane, c.red[q4]);
-    const bool ok = empty || wait_bar(&c.odone[oi & 1], (oi >> 1) & 1, c, p.hdr);
+    const bool ok = empty || wait_bar(&c.odone, oi & 1, c, p.hdr);
     if (named_sync_or(kBarSoftmax, 128, !ok)) {
       failed = true;
       break;
@@ -950,7 +978,7 @@ __device__ void role_softmax(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_
     }
     named_sync(kBarSoftmax, 128);
     tc_fence_after();
-    const uint32_t oa = lb + kColO + (oi & 1) * 128;
+    const uint32_t oa = lb + kColO;
 #pragma unroll 1
     for (int h = 0; h < 2; ++h) {
       float o[N];
@@ -968,7 +996,7 @@ __device__ void role_softmax(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_
     }
     if (!empty) {
       tc_fence_before();
-      mbar_arrive(&c.ofree[oi & 1]);
+      mbar_arrive(&c.ofree);
       ++oi;
     }
     named_sync(kBarSoftmax, 128);   // tables and sums read before the next item rewrites them
@@ -998,16 +1026,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&c.vfull, 128);
     mbar_init(&c.vfree, 1);
-    mbar_init(&c.kfull, 128);
-    mbar_init(&c.kfree, 1);
+    mbar_init(&c.odone, 1);
+    mbar_init(&c.ofree, 128);
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c.sfull[i], 1);
       mbar_init(&c.sfree[i], 128);
       mbar_init(&c.pfull[i], 128);
       mbar_init(&c.pdone[i], 1);
-      mbar_init(&c.odone[i], 1);
-      mbar_init(&c.ofree[i], 128);
+      mbar_init(&c.kfull[i], 128);
+      mbar_init(&c.kfree[i], 1);
     }
     mbar_init(&c.done, 1);
     c.abort = 0;
