@@ -366,6 +366,18 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
   return ok != 0;
 }
 
+// non-blocking check of the same phase
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 constexpr uint32_t kSleepNs = 20000;        // one suspension: 20 us at most
 constexpr uint32_t kSleepCap = 1u << 16;    // => a wait gives up after ~1.3 s
 
@@ -373,6 +385,7 @@ constexpr uint32_t kSleepCap = 1u << 16;    // => a wait gives up after ~1.3 s
 // stays rolled: every call site would otherwise carry unrolled copies, and
 // the kernel's code must fit the instruction caches of four roles at once)
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Ctl &c, uint32_t *hdr) {
+  if (mbar_test(bar, parity)) return true;   // already complete: no suspension
   volatile int *ab = &c.abort;
 #pragma unroll 1
   for (uint32_t i = 0; i < kSleepCap; ++i) {
