@@ -319,8 +319,6 @@ struct Ctl {
   uint32_t tmem;                               // tensor-memory base address
   int abort;                                   // a capped wait ran out somewhere
   int rvalid[kMaxNR];                          // raw stage holds a valid block
-  uint32_t ruse[kMaxNR];                       // producer: fills of each raw stage so far
-  int ids[2][kTileBlocks];                     // producer: block ids of this / the next tile
   alignas(16) float m[kMaxN];                  // running max of each row (log2 domain)
   alignas(16) float mnew[kMaxN], alpha[kMaxN], inv[kMaxN];
   alignas(16) float red[4][kMaxN];
@@ -406,79 +404,70 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
 
 // ------------------------------------------------------------------ roles
 
-// warp 0, one thread: each 16-token block of each item in order into the
-// raw ring (K / V code tiles by 2-D TMA with 128-byte swizzle, NVFP4 block
-// scales by 1-D bulk copies)
+// warp 0, lanes 0-7: lane j copies block j of every tile into raw stage
+// (tile % NRT) * 8 + j (K / V code tiles by 2-D TMA with 128-byte swizzle,
+// NVFP4 block scales by 1-D bulk copies).  One lane per block position
+// issues a tile's copies in parallel and keeps its stage counters and the
+// next tile's block id in registers.
 template <int DT, int N>
 __device__ void role_producer(const AttnParams &p, const CUtensorMap *tmK, const CUtensorMap *tmV,
-                              uint8_t *smem, Ctl &c, int num_items) {
+                              uint8_t *smem, Ctl &c, int num_items, int jt) {
   using Gm = Geo<DT, N>;
   const uint64_t pol = policy_evict_first();
-  // fills of each raw stage and the block ids of the current and the next
-  // tile live in shared memory (a local-memory array would cost an L2 round
-  // trip per access: most of the SM's L1 is given to shared memory)
-#pragma unroll 1
-  for (int s = 0; s < Gm::NR; ++s) c.ruse[s] = 0;
+  uint32_t ruse[Gm::NRT];   // fills of this lane's raw stages so far
+#pragma unroll
+  for (int a = 0; a < Gm::NRT; ++a) ruse[a] = 0;
   uint32_t g = 0;
   bool ok = true;
   for (int ii = blockIdx.x; ii < num_items && ok; ii += gridDim.x) {
     const Item x = load_item(p, ii);
-    // block ids are read with independent loads one tile ahead, so that no
-    // table read sits between two blocks' copies
-    int nxt[kTileBlocks];
-#pragma unroll
-    for (int k = 0; k < kTileBlocks; ++k) nxt[k] = k < x.n_blk ? x.trow[x.it.blk_begin + k] : -1;
-#pragma unroll
-    for (int k = 0; k < kTileBlocks; ++k) c.ids[0][k] = nxt[k];
+    // this lane's block id of the next tile is read one tile ahead
+    int nxt = jt < x.n_blk ? x.trow[x.it.blk_begin + jt] : -1;
     for (int tile = 0; tile < x.ntiles && ok; ++tile, ++g) {
       const int nb = min(kTileBlocks, x.n_blk - tile * kTileBlocks);
-      const int nb2 = min(kTileBlocks, x.n_blk - (tile + 1) * kTileBlocks);   // <= 0 at the end
-#pragma unroll
-      for (int k = 0; k < kTileBlocks; ++k)
-        nxt[k] = k < nb2 ? x.trow[x.it.blk_begin + (tile + 1) * kTileBlocks + k] : -1;
+      const int phys = nxt;
+      const int j2 = (tile + 1) * kTileBlocks + jt;
+      nxt = j2 < x.n_blk ? x.trow[x.it.blk_begin + j2] : -1;
+      if (jt >= nb) continue;
       const int stage = (int)(g % Gm::NRT);
-      uint8_t *st = smem + stage * Gm::RTILE;
-      const int *ids = c.ids[tile & 1];
-#pragma unroll 1
-      for (int jt = 0; jt < nb; ++jt) {
-        const int s = stage * kTileBlocks + jt;
-        const uint32_t use = c.ruse[s]++;
-        if (!wait_bar(&c.rawfree[s], (use & 1) ^ 1, c, p.hdr)) {
-          ok = false;
-          break;
-        }
-        const int phys = ids[jt];
-        const bool v = phys >= 0 && phys < p.kv.num_blocks;
-        c.rvalid[s] = v;
-        if (!v) {
-          set_err(p.hdr, PA_ERRF_BAD_BLOCK_ID);
-          mbar_arrive(&c.rawfull[s]);
-          continue;
-        }
-        const size_t tile_id = (size_t)phys * p.kv.hkv + x.kvh;
-        const int y = (int)(tile_id * kBlock);
-        mbar_arrive_expect_tx(&c.rawfull[s], Gm::PAYLOAD);
+      const int s = stage * kTileBlocks + jt;
+      uint32_t use = 0;
 #pragma unroll
-        for (int xo = 0; xo < Gm::ROW; xo += 128) {
-          tc::tma_rows(st + jt * Gm::CODE + xo * kBlock, tmK, xo, y, &c.rawfull[s], pol);
-          tc::tma_rows(st + Gm::R_V + jt * Gm::CODE + xo * kBlock, tmV, xo, y, &c.rawfull[s], pol);
-        }
-        if constexpr (Gm::SC > 0) {
-          bulk_g2s(st + Gm::R_KS + jt * Gm::SC, (const uint8_t *)p.kv.ks + tile_id * Gm::SC, Gm::SC,
-                   &c.rawfull[s], pol);
-          bulk_g2s(st + Gm::R_VS + jt * Gm::SC, (const uint8_t *)p.kv.vs + tile_id * Gm::SC, Gm::SC,
-                   &c.rawfull[s], pol);
-        }
+      for (int a = 0; a < Gm::NRT; ++a)
+        if (a == stage) use = ruse[a]++;
+      if (!wait_bar(&c.rawfree[s], (use & 1) ^ 1, c, p.hdr)) {
+        ok = false;
+        break;
       }
+      const bool v = phys >= 0 && phys < p.kv.num_blocks;
+      c.rvalid[s] = v;
+      if (!v) {
+        set_err(p.hdr, PA_ERRF_BAD_BLOCK_ID);
+        mbar_arrive(&c.rawfull[s]);
+        continue;
+      }
+      uint8_t *st = smem + stage * Gm::RTILE;
+      const size_t tile_id = (size_t)phys * p.kv.hkv + x.kvh;
+      const int y = (int)(tile_id * kBlock);
+      mbar_arrive_expect_tx(&c.rawfull[s], Gm::PAYLOAD);
 #pragma unroll
-      for (int k = 0; k < kTileBlocks; ++k) c.ids[(tile + 1) & 1][k] = nxt[k];
+      for (int xo = 0; xo < Gm::ROW; xo += 128) {
+        tc::tma_rows(st + jt * Gm::CODE + xo * kBlock, tmK, xo, y, &c.rawfull[s], pol);
+        tc::tma_rows(st + Gm::R_V + jt * Gm::CODE + xo * kBlock, tmV, xo, y, &c.rawfull[s], pol);
+      }
+      if constexpr (Gm::SC > 0) {
+        bulk_g2s(st + Gm::R_KS + jt * Gm::SC, (const uint8_t *)p.kv.ks + tile_id * Gm::SC, Gm::SC,
+                 &c.rawfull[s], pol);
+        bulk_g2s(st + Gm::R_VS + jt * Gm::SC, (const uint8_t *)p.kv.vs + tile_id * Gm::SC, Gm::SC,
+                 &c.rawfull[s], pol);
+      }
     }
   }
-  // the last fill of every stage may still be in flight after a failure:
-  // let the copies land before the CTA exits
-#pragma unroll 1
-  for (int s = 0; s < Gm::NR; ++s)
-    if (c.ruse[s] > 0) drain_wait(&c.rawfull[s], (c.ruse[s] - 1) & 1);
+  // the last fill of each of this lane's stages may still be in flight after
+  // a failure: let the copies land before the CTA exits
+#pragma unroll
+  for (int a = 0; a < Gm::NRT; ++a)
+    if (ruse[a] > 0) drain_wait(&c.rawfull[a * kTileBlocks + jt], (ruse[a] - 1) & 1);
 }
 
 // warp 1, one thread: QK of tile g, then PV of tile g - 1 (so that the
@@ -1067,7 +1056,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (wg == 0) {
     setmaxnreg_dec<kRegCtl>();
     if (warp == 0) {
-      if (lane == 0) role_producer<DT, N>(p, &tmK, &tmV, smem, c, num_items);
+      if (lane < kTileBlocks) role_producer<DT, N>(p, &tmK, &tmV, smem, c, num_items, lane);
       __syncwarp();
     } else if (warp == 1) {
       if (lane == 0) role_mma<DT, N>(p, smem, c, tmem, num_items);
