@@ -128,8 +128,8 @@ typedef struct pa_problem {
 /* Optional knobs; pass NULL for defaults. */
 typedef struct pa_options {
   int32_t kernel;          /* 0 auto: bf16 -> 1; int8 / NVFP4 / FP8 decode -> 2;
-                              int8 / FP8 verify (head_dim 256) -> 2 (dense tiles);
-                              NVFP4 verify (head_dim 256) -> 4.
+                              int8 verify (head_dim 256) -> 2 (dense tiles);
+                              NVFP4 / FP8 verify (head_dim 256) -> 4.
                               1 CUDA-core (SIMT) kernel; 2 tensor-core kernel (mma.sync;
                               verify: dense tiles of up to 48 of the q_len * G rows when
                               the format is int8/NVFP4/FP8 and head_dim 256); 3

@@ -870,19 +870,25 @@ __device__ void role_softmax(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_
       tc_fence_after();
       const uint32_t sa = lb + kColS + (g & 1) * 64;
       const uint32_t pb = pcol + (g & 1) * Gm::PBUF;
-      // Scores in, probabilities out (written to P^T as f16) with the running
-      // max m; `need` is set where a score passes m by the threshold.  The
+      // Raw dot products in, probabilities out (written to P^T as f16) with
+      // the running max m: p = 2^(s * scale - m), one FMA for the exponent;
+      // `need` is set where a visible score passes m by the threshold.  The
       // exponent is capped so that a tile about to be redone stays finite.
       auto emit = [&](float (&v)[N], bool &need) {
 #pragma unroll
         for (int n4 = 0; n4 < N; n4 += 4) {
           const float4 m4 = lds_f4(s_m + 4 * n4);
           const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+          int4 lm = make_int4(0x7fffffff, 0x7fffffff, 0x7fffffff, 0x7fffffff);
+          if (causal) lm = lds_s4(s_lim + 4 * n4);
+          const int lv[4] = {lm.x, lm.y, lm.z, lm.w};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int n = n4 + k;
-            need |= v[n] > mv[k] + kRescale;
-            const float pr = v[n] == kNegInf ? 0.f : ex2_approx(fminf(v[n] - mv[k], 64.f));
+            const bool vis = row_ok && n < R && tok < lv[k];
+            const float d = fmaf(v[n], qscale, -mv[k]);
+            need |= vis && d > kRescale;
+            const float pr = vis ? ex2_approx(fminf(d, 64.f)) : 0.f;
             v[n] = pr;
             sts_u16(pb + n * 128 + ((tu ^ (n & 7)) << 4), __half_as_ushort(__float2half_rn(pr)));
           }
@@ -898,7 +904,6 @@ __device__ void role_softmax(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_
       for (int pass = 0; pass < 2; ++pass) {
         if (!redo || pass == 1) {   // probabilities with the current max
           tmem_ldn<N>(sa, v);
-          scores(v);
           bool need = false;
           emit(v, need);
           if (pass == 1) break;
