@@ -27,7 +27,8 @@
 // partitions) with warp-specialised roles:
 //   warp 0       producer: TMA copies of each 16-token block's K / V codes
 //                (and NVFP4 block scales) into a ring of raw stages
-//   warp 1       tensor-memory allocation; one thread issues every MMA
+//   warp 1       tensor-memory allocation; one thread issues the QK MMAs
+//   warp 2       one thread issues the PV MMAs
 //   warps 4-7    K dequant: token row t of the tile -> TMEM lane t (f16x2)
 //   warps 12-15  V dequant: token rows -> the f16 V tile in shared memory
 //                (MN-major A operand layout)
@@ -470,65 +471,23 @@ __device__ void role_producer(const AttnParams &p, const CUtensorMap *tmK, const
     if (ruse[a] > 0) drain_wait(&c.rawfull[a * kTileBlocks + jt], (ruse[a] - 1) & 1);
 }
 
-// warp 1, one thread: QK of tile g, then PV of tile g - 1 (so that the
-// softmax of tile g overlaps PV of tile g - 1)
+// Two MMA-issuing threads, each with its own accumulators and commit
+// barriers, so that neither stream waits behind the other: QK of tile g
+// needs only its K tile and a free S buffer, PV of tile g only its P and V.
+// warp 1, one thread: S^T(g) = K(g) . Q^T
 template <int DT, int N>
-__device__ void role_mma(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t tmem,
-                         int num_items) {
+__device__ void role_qk(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t tmem,
+                        int num_items) {
   using Gm = Geo<DT, N>;
   constexpr uint32_t IQK = idesc_f16(kTile, N, false);
-  constexpr uint32_t IPV = idesc_f16(kTile, N, true);
-  const uint32_t sQ = smem_u32(smem + Gm::OFF_Q), sP = smem_u32(smem + Gm::OFF_P);
-  const uint32_t sV = smem_u32(smem + Gm::OFF_V);
-  // Descriptors are built once; a k-step or block moves the start address,
-  // which is the low field (address >> 4), by a constant.
-  const uint64_t dQ = sdesc(sQ, 16, 1024);
-  const uint64_t dP0 = sdesc(sP, 16, 1024), dP1 = sdesc(sP + Gm::PBUF, 16, 1024);
-  const uint64_t dV = sdesc(sV, 2048, 1024);
-  struct Pend {
-    bool on, first, last;
-    uint32_t g, oi;
-    int nb;
-  };
-  Pend pend = {false, false, false, 0, 0, 0};
-  auto issue_pv = [&](const Pend &t) -> bool {
-    if (!wait_bar(&c.pfull[t.g & 1], (t.g >> 1) & 1, c, p.hdr)) return false;
-    if (t.first && !wait_bar(&c.ofree, (t.oi & 1) ^ 1, c, p.hdr)) return false;
-    if (!wait_bar(&c.vfull, t.g & 1, c, p.hdr)) return false;
-    tc_fence_after();
-    const uint32_t dO = tmem + kColO;
-    const uint64_t dP = (t.g & 1) ? dP1 : dP0;
-#pragma unroll 1
-    for (int j = 0; j < kTileBlocks; ++j) {
-      if (j < t.nb) {
-        const uint64_t bd = dP + (uint64_t)(((j >> 2) * Gm::QCH + (j & 3) * 32) >> 4);
-        const uint64_t ad = dV + (uint64_t)((j * Gm::VSLOT) >> 4);
-        const uint32_t acc = (t.first && j == 0) ? 0u : 1u;
-        mma_ss(dO, ad, bd, IPV, acc);
-        mma_ss(dO + 64, ad + (4096 >> 4), bd, IPV, acc);
-      }
-    }
-    tc_commit(&c.vfree);
-    tc_commit(&c.pdone[t.g & 1]);
-    if (t.last) tc_commit(&c.odone);
-    return true;
-  };
-  uint32_t g = 0, oi = 0;
+  // the descriptor is built once; a k-step moves the start address, which is
+  // the low field (address >> 4), by a constant
+  const uint64_t dQ = sdesc(smem_u32(smem + Gm::OFF_Q), 16, 1024);
+  uint32_t g = 0;
   bool ok = true;
   for (int ii = blockIdx.x; ii < num_items && ok; ii += gridDim.x) {
     const Item x = load_item(p, ii);
-    if (x.n_blk == 0) continue;
-    for (int tile = 0; tile < x.ntiles; ++tile) {
-      const int nb = min(kTileBlocks, x.n_blk - tile * kTileBlocks);
-      // the last PV of the previous item goes first: the epilogue waits for it
-      // and the next item's first QK waits for its q tile anyway
-      if (tile == 0 && pend.on) {
-        if (!issue_pv(pend)) {
-          ok = false;
-          break;
-        }
-        pend.on = false;
-      }
+    for (int tile = 0; tile < x.ntiles; ++tile, ++g) {
       if (!wait_bar(&c.kfull[g & 1], (g >> 1) & 1, c, p.hdr) ||
           !wait_bar(&c.sfree[g & 1], ((g >> 1) & 1) ^ 1, c, p.hdr)) {
         ok = false;
@@ -543,17 +502,53 @@ __device__ void role_mma(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t tm
                IQK, ks > 0 ? 1u : 0u);
       tc_commit(&c.sfull[g & 1]);
       tc_commit(&c.kfree[g & 1]);
-      if (pend.on && !issue_pv(pend)) {
+    }
+  }
+  tc_commit(&c.done);   // tensor memory is released only after every MMA completes
+  drain_wait(&c.done, 0);
+}
+
+// warp 2, one thread: O^T += V^T(g) . P^T(g), per 16-token block
+template <int DT, int N>
+__device__ void role_pv(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t tmem,
+                        int num_items) {
+  using Gm = Geo<DT, N>;
+  constexpr uint32_t IPV = idesc_f16(kTile, N, true);
+  const uint32_t sP = smem_u32(smem + Gm::OFF_P);
+  const uint64_t dP0 = sdesc(sP, 16, 1024), dP1 = sdesc(sP + Gm::PBUF, 16, 1024);
+  const uint64_t dV = sdesc(smem_u32(smem + Gm::OFF_V), 2048, 1024);
+  const uint32_t dO = tmem + kColO;
+  uint32_t g = 0, oi = 0;
+  bool ok = true;
+  for (int ii = blockIdx.x; ii < num_items && ok; ii += gridDim.x) {
+    const Item x = load_item(p, ii);
+    if (x.n_blk == 0) continue;
+    for (int tile = 0; tile < x.ntiles; ++tile, ++g) {
+      const int nb = min(kTileBlocks, x.n_blk - tile * kTileBlocks);
+      const bool first = tile == 0;
+      if (!wait_bar(&c.pfull[g & 1], (g >> 1) & 1, c, p.hdr) ||
+          (first && !wait_bar(&c.ofree, (oi & 1) ^ 1, c, p.hdr)) ||
+          !wait_bar(&c.vfull, g & 1, c, p.hdr)) {
         ok = false;
         break;
       }
-      pend = {true, tile == 0, tile == x.ntiles - 1, g, oi, nb};
-      ++g;
+      tc_fence_after();
+      const uint64_t dP = (g & 1) ? dP1 : dP0;
+#pragma unroll 1
+      for (int j = 0; j < nb; ++j) {
+        const uint64_t bd = dP + (uint64_t)(((j >> 2) * Gm::QCH + (j & 3) * 32) >> 4);
+        const uint64_t ad = dV + (uint64_t)((j * Gm::VSLOT) >> 4);
+        const uint32_t acc = (first && j == 0) ? 0u : 1u;
+        mma_ss(dO, ad, bd, IPV, acc);
+        mma_ss(dO + 64, ad + (4096 >> 4), bd, IPV, acc);
+      }
+      tc_commit(&c.vfree);
+      tc_commit(&c.pdone[g & 1]);
+      if (tile == x.ntiles - 1) tc_commit(&c.odone);
     }
     ++oi;
   }
-  if (ok && pend.on) (void)issue_pv(pend);
-  tc_commit(&c.done);   // tensor memory is released only after every MMA completes
+  tc_commit(&c.done);
   drain_wait(&c.done, 0);
 }
 
@@ -1044,7 +1039,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&c.kfull[i], 128);
       mbar_init(&c.kfree[i], 1);
     }
-    mbar_init(&c.done, 1);
+    mbar_init(&c.done, 2);   // one commit from each MMA-issuing thread
     c.abort = 0;
     fence_mbar_init();
   }
@@ -1064,7 +1059,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane < kTileBlocks) role_producer<DT, N>(p, &tmK, &tmV, smem, c, num_items, lane);
       __syncwarp();
     } else if (warp == 1) {
-      if (lane == 0) role_mma<DT, N>(p, smem, c, tmem, num_items);
+      if (lane == 0) role_qk<DT, N>(p, smem, c, tmem, num_items);
+      __syncwarp();
+    } else if (warp == 2) {
+      if (lane == 0) role_pv<DT, N>(p, smem, c, tmem, num_items);
       __syncwarp();
     }
   } else if (wg == 1) {
