@@ -28,7 +28,7 @@
 //   warp 0       producer: TMA copies of each 16-token block's K / V codes
 //                (and NVFP4 block scales) into a ring of raw stages
 //   warp 1       tensor-memory allocation; one thread issues the QK MMAs
-//   warp 2       one thread issues the PV MMAs
+//   warps 2, 3   one thread each issues the PV MMAs of one head-dim half
 //   warps 4-7    K dequant: token row t of the tile -> TMEM lane t (f16x2)
 //   warps 12-15  V dequant: token rows -> the f16 V tile in shared memory
 //                (MN-major A operand layout)
@@ -508,16 +508,19 @@ __device__ void role_qk(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t tme
   drain_wait(&c.done, 0);
 }
 
-// warp 2, one thread: O^T += V^T(g) . P^T(g), per 16-token block
+// warps 2 and 3, one thread each: O^T[half h] += V^T(g)[half h] . P^T(g) per
+// 16-token block (each issuing thread is limited to about one MMA per 100+
+// cycles whatever N, so the two head-dim halves of PV go to two threads;
+// V-free, P-done and O-done take one commit from each)
 template <int DT, int N>
 __device__ void role_pv(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t tmem,
-                        int num_items) {
+                        int num_items, int h) {
   using Gm = Geo<DT, N>;
   constexpr uint32_t IPV = idesc_f16(kTile, N, true);
   const uint32_t sP = smem_u32(smem + Gm::OFF_P);
   const uint64_t dP0 = sdesc(sP, 16, 1024), dP1 = sdesc(sP + Gm::PBUF, 16, 1024);
-  const uint64_t dV = sdesc(smem_u32(smem + Gm::OFF_V), 2048, 1024);
-  const uint32_t dO = tmem + kColO;
+  const uint64_t dV = sdesc(smem_u32(smem + Gm::OFF_V) + h * 4096, 2048, 1024);
+  const uint32_t dO = tmem + kColO + h * 64;
   uint32_t g = 0, oi = 0;
   bool ok = true;
   for (int ii = blockIdx.x; ii < num_items && ok; ii += gridDim.x) {
@@ -540,7 +543,6 @@ __device__ void role_pv(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t tme
         const uint64_t ad = dV + (uint64_t)((j * Gm::VSLOT) >> 4);
         const uint32_t acc = (first && j == 0) ? 0u : 1u;
         mma_ss(dO, ad, bd, IPV, acc);
-        mma_ss(dO + 64, ad + (4096 >> 4), bd, IPV, acc);
       }
       tc_commit(&c.vfree);
       tc_commit(&c.pdone[g & 1]);
@@ -1027,19 +1029,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&c.rawfree[s], 2 * kBlock);   // 16 K rows + 16 V rows
     }
     mbar_init(&c.vfull, 128);
-    mbar_init(&c.vfree, 1);
-    mbar_init(&c.odone, 1);
     mbar_init(&c.ofree, 128);
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c.sfull[i], 1);
       mbar_init(&c.sfree[i], 128);
       mbar_init(&c.pfull[i], 128);
-      mbar_init(&c.pdone[i], 1);
+      mbar_init(&c.pdone[i], 2);   // both PV threads
       mbar_init(&c.kfull[i], 128);
       mbar_init(&c.kfree[i], 1);
     }
-    mbar_init(&c.done, 2);   // one commit from each MMA-issuing thread
+    mbar_init(&c.done, 3);   // one commit from each MMA-issuing thread
+    mbar_init(&c.vfree, 2);  // one commit from each PV thread
+    mbar_init(&c.odone, 2);
     c.abort = 0;
     fence_mbar_init();
   }
@@ -1061,8 +1063,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
       if (lane == 0) role_qk<DT, N>(p, smem, c, tmem, num_items);
       __syncwarp();
-    } else if (warp == 2) {
-      if (lane == 0) role_pv<DT, N>(p, smem, c, tmem, num_items);
+    } else {
+      if (lane == 0) role_pv<DT, N>(p, smem, c, tmem, num_items, warp - 2);
       __syncwarp();
     }
   } else if (wg == 1) {
