@@ -200,6 +200,15 @@ template <int R>
 __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
 }
+// Moves this warpgroup from the launch count `From` to `To` registers per
+// thread: .inc only raises and .dec only lowers the current count (the other
+// direction is undefined), so the direction is chosen here, never by hand.
+template <int From, int To>
+__device__ __forceinline__ void setmaxnreg_to() {
+  static_assert(To % 8 == 0 && To >= 24 && To <= 256, "setmaxnreg count");
+  if constexpr (To > From) setmaxnreg_inc<To>();
+  else if constexpr (To < From) setmaxnreg_dec<To>();
+}
 
 // generic-proxy shared-memory writes -> visible to the tensor cores
 __device__ __forceinline__ void fence_async_smem() {
@@ -246,12 +255,14 @@ constexpr int D = 256;
 constexpr int kTile = 128;                 // tokens per QK tile (the MMA's M)
 constexpr int kTileBlocks = kTile / kBlock;
 constexpr int kThreads = 512;              // 4 warpgroups
+constexpr int kLaunchRegs = 128;           // per thread at launch: 65536 / 512
 // Registers per thread of each warpgroup after the split (launched with 128
 // each): producer/MMA 88, K dequant 128, softmax 200, V dequant 96.  Per
 // SM sub-partition (one warp of each group) 512 = 4 x 128, so every
 // setmaxnreg.inc is satisfied by the decreases.
 constexpr int kRegCtl = 88, kRegK = 128, kRegSoftmax = 200, kRegV = 96;
-static_assert(kRegCtl + kRegK + kRegSoftmax + kRegV <= 4 * 128, "register split");
+static_assert(kRegCtl + kRegK + kRegSoftmax + kRegV <= 4 * kLaunchRegs, "register split");
+static_assert(kLaunchRegs == 65536 / kThreads / 8 * 8, "launch register count");
 constexpr uint32_t kTmemCols = 512;
 // tensor-memory columns (32-bit each): two K tiles (128 tokens x 256 f16,
 // 128 columns each), two S buffers (64 columns each, N used), one O^T of two
@@ -690,7 +701,7 @@ __device__ void role_kdeq(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t t
   }
 }
 
-// warps 8-11: token row r of each block -> the block's f16 V slot, laid out
+// warps 12-15: token row r of each block -> the block's f16 V slot, laid out
 // [64-wide head-dim chunk][16 tokens][128 bytes, swizzled] (MN-major A of PV)
 template <int DT, int N>
 __device__ void role_vdeq(const AttnParams &p, uint8_t *smem, Ctl &c, int num_items, int warp,
@@ -1056,7 +1067,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int wg = warp >> 2;   // warpgroup
   if (wg == 0) {
-    setmaxnreg_dec<kRegCtl>();
+    setmaxnreg_to<kLaunchRegs, kRegCtl>();
     if (warp == 0) {
       if (lane < kTileBlocks) role_producer<DT, N>(p, &tmK, &tmV, smem, c, num_items, lane);
       __syncwarp();
@@ -1068,13 +1079,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     }
   } else if (wg == 1) {
-    setmaxnreg_dec<kRegK>();
+    setmaxnreg_to<kLaunchRegs, kRegK>();
     role_kdeq<DT, N>(p, smem, c, tmem, num_items, warp, lane);
   } else if (wg == 2) {
-    setmaxnreg_inc<kRegSoftmax>();
+    setmaxnreg_to<kLaunchRegs, kRegSoftmax>();
     role_softmax<DT, N>(p, smem, c, tmem, num_items, warp, lane);
   } else {
-    setmaxnreg_dec<kRegV>();
+    setmaxnreg_to<kLaunchRegs, kRegV>();
     role_vdeq<DT, N>(p, smem, c, num_items, warp, lane);
   }
   tc_fence_before();
@@ -1104,6 +1115,12 @@ cudaError_t launch_n(const AttnParams &p, int max_items, cudaStream_t s) {
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
   if (e != cudaSuccess) return e;
+  // the warpgroups' setmaxnreg steps start from kLaunchRegs: a build that
+  // gave the kernel another count is refused, never launched
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidDeviceFunction;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const int grid = max(1, min(sms, max_items));
