@@ -164,6 +164,21 @@ __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t lo, uint32_t hi) {
   return r;
 }
 
+// 2^x with the hardware approximation (relative error about 2^-22; results
+// below 2^-126 flush to zero, which the softmax weights can lose)
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// two E4M3 scale bytes (low 16 bits) -> (s0, s0) and (s1, s1) as f16x2
+__device__ __forceinline__ void e4m3x2_dup(uint32_t pair, uint32_t &d0, uint32_t &d1) {
+  const uint32_t h = e4m3x2_u16_to_h2(pair);
+  d0 = prmt(h, h, 0x1010);
+  d1 = prmt(h, h, 0x3232);
+}
+
 // byte offset of (row, byte) in a tile stored as 16-row x 128-byte boxes
 // with the 128-byte swizzle (boxes of 2 KB, one per 128 bytes of row)
 __device__ __forceinline__ int sw_off(int row, int byte) {
@@ -316,8 +331,10 @@ __global__ void __launch_bounds__(kThreads, 3)
       const int tok0 = t_begin + (warp + j * kWarps) * kBlock;
       const int nvalid = min(kBlock, t_end - tok0);
 
-      // ---- S^T = K . Q^T
-      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+      // ---- S^T = K . Q^T; int8 and NVFP4 alternate k-steps into two
+      // accumulators so that the MMAs form two independent dependency chains
+      // (FP8 keeps one: it is at its register bound for 3 CTAs per SM)
+      float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sacc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int g = 0; g < KG; ++g) {
         const int boff = g * 64 + c * 16;
@@ -329,8 +346,8 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
           for (int s2 = 0; s2 < KS; ++s2) {   // k-step s2 uses word s2 of each row
             const uint32_t x0 = w0[s2] ^ 0x80808080u, x1 = w1[s2] ^ 0x80808080u;
-            mma16816(sacc, s8pair_to_h2(x0, 0), s8pair_to_h2(x1, 0), s8pair_to_h2(x0, 1),
-                     s8pair_to_h2(x1, 1), qf[g][s2][0], qf[g][s2][1]);
+            mma16816((s2 & 1) ? sacc2 : sacc, s8pair_to_h2(x0, 0), s8pair_to_h2(x1, 0),
+                     s8pair_to_h2(x0, 1), s8pair_to_h2(x1, 1), qf[g][s2][0], qf[g][s2][1]);
           }
         } else if constexpr (DT == PA_KV_FP8) {
 #pragma unroll
@@ -339,11 +356,12 @@ __global__ void __launch_bounds__(kThreads, 3)
                      e4m3x2_u16_to_h2(w0[s2] >> 16), e4m3x2_u16_to_h2(w1[s2] >> 16),
                      qf[g][s2][0], qf[g][s2][1]);
         } else {
-          const int sb = (g * 4 * Gm::E + c * Gm::E) / 16;   // first 16-element scale block
-          const uint32_t sc00 = e4m3_to_h2_dup(sKs[r * SROW + sb]);
-          const uint32_t sc01 = e4m3_to_h2_dup(sKs[r * SROW + sb + 1]);
-          const uint32_t sc10 = e4m3_to_h2_dup(sKs[(r + 8) * SROW + sb]);
-          const uint32_t sc11 = e4m3_to_h2_dup(sKs[(r + 8) * SROW + sb + 1]);
+          // the lane's two 16-element scale blocks sb, sb + 1 (sb even): one
+          // 16-bit load per row
+          const int sb = (g * 4 * Gm::E + c * Gm::E) / 16;
+          uint32_t sc00, sc01, sc10, sc11;
+          e4m3x2_dup(*reinterpret_cast<const uint16_t *>(sKs + r * SROW + sb), sc00, sc01);
+          e4m3x2_dup(*reinterpret_cast<const uint16_t *>(sKs + (r + 8) * SROW + sb), sc10, sc11);
 #pragma unroll
           for (int wi = 0; wi < 4; ++wi) {   // word wi = k-steps 2 wi, 2 wi + 1
             uint32_t h0[4], h1[4];
@@ -352,11 +370,15 @@ __global__ void __launch_bounds__(kThreads, 3)
             const uint32_t a_s = wi < 2 ? sc00 : sc01, b_s = wi < 2 ? sc10 : sc11;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh)   // k-step 2 wi + hh = bytes 2 hh, 2 hh + 1
-              mma16816(sacc, hmul2_u32(h0[2 * hh], a_s), hmul2_u32(h1[2 * hh], b_s),
+              mma16816(hh ? sacc2 : sacc, hmul2_u32(h0[2 * hh], a_s), hmul2_u32(h1[2 * hh], b_s),
                        hmul2_u32(h0[2 * hh + 1], a_s), hmul2_u32(h1[2 * hh + 1], b_s),
                        qf[g][2 * wi + hh][0], qf[g][2 * wi + hh][1]);
           }
         }
+      }
+      if constexpr (DT != PA_KV_FP8) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sacc[k] += sacc2[k];
       }
       // scale, mask
       float f0 = qscale, f1 = qscale;
@@ -385,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const float mn = fmaxf(m_run[h], mx[h]);
-          al[h] = (mn == kNegInf) ? 1.f : exp2f(m_run[h] - mn);
+          al[h] = (mn == kNegInf) ? 1.f : ex2f(m_run[h] - mn);
           m_run[h] = mn;
           l_run[h] *= al[h];
         }
@@ -401,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       }
       float pr[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) pr[k] = (sc[k] == kNegInf) ? 0.f : exp2f(sc[k] - m_run[k & 1]);
+      for (int k = 0; k < 4; ++k) pr[k] = (sc[k] == kNegInf) ? 0.f : ex2f(sc[k] - m_run[k & 1]);
       l_run[0] += pr[0] + pr[2];
       l_run[1] += pr[1] + pr[3];
       if constexpr (DT == PA_KV_INT8) {
@@ -444,8 +466,13 @@ __global__ void __launch_bounds__(kThreads, 3)
           }
           if constexpr (DT == PA_KV_NVFP4) {
             const int sb = (g * 8 * VE + r * VE) / 16;
-            vsb[t][0] = ok ? sVs[tk[t] * SROW + sb] : 0u;
-            vsb[t][1] = (ok && VE > 16) ? sVs[tk[t] * SROW + sb + 1] : vsb[t][0];
+            if constexpr (VE > 16) {   // blocks sb, sb + 1 (sb even): one 16-bit load
+              vsb[t][0] = ok ? *reinterpret_cast<const uint16_t *>(sVs + tk[t] * SROW + sb) : 0u;
+            } else {
+              vsb[t][0] = ok ? sVs[tk[t] * SROW + sb] : 0u;
+              vsb[t][0] |= vsb[t][0] << 8;
+            }
+            vsb[t][1] = 0u;
           } else if constexpr (DT == PA_KV_INT8) {
 #pragma unroll
             for (int q = 0; q < VB / 4; ++q) vw[t][q] ^= 0x80808080u;   // offset-binary
@@ -459,11 +486,13 @@ __global__ void __launch_bounds__(kThreads, 3)
           // that byte e of X holds (token a, token b) at head-dim row r and
           // byte e of Y the same at row r + 8 -- each cvt then yields an A
           // register directly.
+          // scale pair (token a, token b) of block k: byte k of each token's pair
           uint32_t sp[2][2];
 #pragma unroll
           for (int pr2 = 0; pr2 < 2; ++pr2)
 #pragma unroll
-            for (int k = 0; k < 2; ++k) sp[pr2][k] = e4m3x2_to_h2(vsb[2 * pr2][k], vsb[2 * pr2 + 1][k]);
+            for (int k = 0; k < 2; ++k)
+              sp[pr2][k] = e4m3x2_u16_to_h2(prmt(vsb[2 * pr2][0], vsb[2 * pr2 + 1][0], k ? 0x51u : 0x40u));
 #pragma unroll
           for (int wq = 0; wq < VB / 4; ++wq) {
             uint32_t xa[4], ya[4], xb[4], yb[4];
