@@ -172,6 +172,14 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
+// transpose of an 8x8 matrix of 16-bit elements held by the warp (lane i:
+// row i / 4, elements 2 (i % 4), 2 (i % 4) + 1)
+__device__ __forceinline__ uint32_t movm_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
 // two E4M3 scale bytes (low 16 bits) -> (s0, s0) and (s1, s1) as f16x2
 __device__ __forceinline__ void e4m3x2_dup(uint32_t pair, uint32_t &d0, uint32_t &d1) {
   const uint32_t h = e4m3x2_u16_to_h2(pair);
@@ -308,10 +316,6 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
       for (int k = 0; k < 4; ++k) o[g][e][k] = 0.f;
 
-  // P^T fragment sources: token 2c lives in lane 8c + r/2, token 2c+1 four lanes up
-  const int srcA = 8 * c + (r >> 1), srcB = srcA + 4;
-  const bool odd = r & 1;
-
   const int prologue = min(NSTAGE, n_local);
   for (int j = 0; j < prologue; ++j) issue(j);
   int issued = prologue;
@@ -331,10 +335,11 @@ __global__ void __launch_bounds__(kThreads, 3)
       const int tok0 = t_begin + (warp + j * kWarps) * kBlock;
       const int nvalid = min(kBlock, t_end - tok0);
 
-      // ---- S^T = K . Q^T; int8 and NVFP4 alternate k-steps into two
-      // accumulators so that the MMAs form two independent dependency chains
+      // ---- S^T = K . Q^T; int8 alternates k-steps over two accumulators and
+      // NVFP4 over four, so that the MMAs form independent dependency chains
       // (FP8 keeps one: it is at its register bound for 3 CTAs per SM)
       float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sacc2[4] = {0.f, 0.f, 0.f, 0.f};
+      float sacc3[4] = {0.f, 0.f, 0.f, 0.f}, sacc4[4] = {0.f, 0.f, 0.f, 0.f};   // NVFP4: 4 chains
 #pragma unroll
       for (int g = 0; g < KG; ++g) {
         const int boff = g * 64 + c * 16;
@@ -370,13 +375,17 @@ __global__ void __launch_bounds__(kThreads, 3)
             const uint32_t a_s = wi < 2 ? sc00 : sc01, b_s = wi < 2 ? sc10 : sc11;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh)   // k-step 2 wi + hh = bytes 2 hh, 2 hh + 1
-              mma16816(hh ? sacc2 : sacc, hmul2_u32(h0[2 * hh], a_s), hmul2_u32(h1[2 * hh], b_s),
+              mma16816((wi & 1) ? (hh ? sacc4 : sacc3) : (hh ? sacc2 : sacc),
+                       hmul2_u32(h0[2 * hh], a_s), hmul2_u32(h1[2 * hh], b_s),
                        hmul2_u32(h0[2 * hh + 1], a_s), hmul2_u32(h1[2 * hh + 1], b_s),
                        qf[g][2 * wi + hh][0], qf[g][2 * wi + hh][1]);
           }
         }
       }
-      if constexpr (DT != PA_KV_FP8) {
+      if constexpr (DT == PA_KV_NVFP4) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sacc[k] = (sacc[k] + sacc2[k]) + (sacc3[k] + sacc4[k]);
+      } else if constexpr (DT == PA_KV_INT8) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) sacc[k] += sacc2[k];
       }
@@ -393,17 +402,20 @@ __global__ void __launch_bounds__(kThreads, 3)
       sc[2] = v1 ? sacc[2] * f1 : kNegInf;
       sc[3] = v1 ? sacc[3] * f1 : kNegInf;
 
-      // ---- online softmax over the block's tokens, per column
+      // ---- online softmax over the block's tokens, per column.  The lane's
+      // own scores decide whether the running max must move (some score above
+      // it by more than kRescale); only then is the column max reduced over
+      // the 8 lanes that hold the column.
       float mx[2] = {fmaxf(sc[0], sc[2]), fmaxf(sc[1], sc[3])};
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 4));
-        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 8));
-        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 16));
-      }
       const bool need = (mx[0] > m_run[0] + kRescale) || (mx[1] > m_run[1] + kRescale);
       if (__any_sync(0xffffffffu, need)) {
         float al[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 4));
+          mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 8));
+          mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 16));
+        }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const float mn = fmaxf(m_run[h], mx[h]);
@@ -434,13 +446,11 @@ __global__ void __launch_bounds__(kThreads, 3)
         pr[2] = v1 ? pr[2] * vs1 : 0.f;
         pr[3] = v1 ? pr[3] * vs1 : 0.f;
       }
-      // ---- P^T fragment (tokens 2c, 2c+1 | 2c+8, 2c+9; column r)
-      float pa0 = __shfl_sync(0xffffffffu, pr[0], srcA), pa1 = __shfl_sync(0xffffffffu, pr[1], srcA);
-      float pb0 = __shfl_sync(0xffffffffu, pr[0], srcB), pb1 = __shfl_sync(0xffffffffu, pr[1], srcB);
-      float pc0 = __shfl_sync(0xffffffffu, pr[2], srcA), pc1 = __shfl_sync(0xffffffffu, pr[3], srcA);
-      float pd0 = __shfl_sync(0xffffffffu, pr[2], srcB), pd1 = __shfl_sync(0xffffffffu, pr[3], srcB);
-      const uint32_t B0 = f2_to_h2(odd ? pa1 : pa0, odd ? pb1 : pb0);
-      const uint32_t B1 = f2_to_h2(odd ? pc1 : pc0, odd ? pd1 : pd0);
+      // ---- P^T fragment (tokens 2c, 2c+1 | 2c+8, 2c+9; column r): the lane
+      // holds P[token r | r + 8][heads 2c, 2c+1], which is the row layout of
+      // an 8x8 b16 matrix, so one warp transpose per 8 tokens gives it
+      const uint32_t B0 = movm_trans(f2_to_h2(pr[0], pr[1]));
+      const uint32_t B1 = movm_trans(f2_to_h2(pr[2], pr[3]));
 
       // ---- O^T += V^T . P^T ; this lane's tokens 2c, 2c+1, 2c+8, 2c+9
       const int tk[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
