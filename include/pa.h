@@ -127,12 +127,14 @@ typedef struct pa_problem {
 
 /* Optional knobs; pass NULL for defaults. */
 typedef struct pa_options {
-  int32_t kernel;          /* 0 auto: bf16 -> 1; int8 / NVFP4 / FP8 decode -> 2;
+  int32_t kernel;          /* 0 auto: decode (every format) -> 2;
                               int8 verify (head_dim 256) -> 2 (dense tiles);
+                              bf16 verify -> 2 (one unit per query token);
                               NVFP4 / FP8 verify (head_dim 256) -> 4.
                               1 CUDA-core (SIMT) kernel; 2 tensor-core kernel (mma.sync;
-                              verify: dense tiles of up to 48 of the q_len * G rows when
-                              the format is int8/NVFP4/FP8 and head_dim 256); 3
+                              bf16 fragments by ldmatrix; verify: dense tiles of up to
+                              48 of the q_len * G rows when the format is
+                              int8/NVFP4/FP8 and head_dim 256); 3
                               tensor-core kernel with verify run as one unit per query
                               token; 4 verify on the tcgen05 tensor cores (accumulators
                               in tensor memory; NVFP4 / FP8, head_dim 256, q_len > 1;

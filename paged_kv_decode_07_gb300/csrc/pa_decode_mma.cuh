@@ -93,16 +93,17 @@ constexpr int kThreads = kWarps * 32;
 
 template <int DT, int D>
 struct Geo {
-  static_assert(DT == PA_KV_INT8 || DT == PA_KV_NVFP4 || DT == PA_KV_FP8,
-                "quantised formats only");
-  static constexpr bool BYTE_CODES = DT != PA_KV_NVFP4;       // one byte per element
-  static constexpr int ROW = BYTE_CODES ? D : D / 2;          // code bytes per token row
-  static constexpr int E = BYTE_CODES ? 16 : 32;              // elements per 16 bytes
+  static constexpr bool BF16 = DT == PA_KV_BF16;              // ldmatrix fragments, no dequant
+  static constexpr bool BYTE_CODES = DT == PA_KV_INT8 || DT == PA_KV_FP8;   // one byte per element
+  static constexpr int ROW = BF16 ? 2 * D : (BYTE_CODES ? D : D / 2);   // bytes per token row
+  static constexpr int E = BF16 ? 8 : (BYTE_CODES ? 16 : 32);   // elements per 16 bytes
   static constexpr int KG = D / (4 * E);                      // K chunks per lane
   static constexpr int KS = E / 4;                            // k-steps per K chunk
-  static constexpr int VE = (8 * E <= D) ? E : D / 8;         // V elements per lane chunk
-  static constexpr int VB = BYTE_CODES ? VE : VE / 2;        // V chunk bytes
-  static constexpr int VG = D / (8 * VE);                     // V chunk groups
+  // V: the quantised formats read VE elements of 4 tokens per lane chunk; bf16
+  // reads 16 x 16 tiles by ldmatrix, one per 16 head-dim rows (VG = D / 16)
+  static constexpr int VE = BF16 ? 2 : ((8 * E <= D) ? E : D / 8);
+  static constexpr int VB = BYTE_CODES ? VE : VE / 2;        // V chunk bytes (quantised)
+  static constexpr int VG = BF16 ? D / 16 : D / (8 * VE);    // V chunk groups
   // scale bytes per token row (FP8 has only the per-tensor scale)
   static constexpr int SROW = DT == PA_KV_INT8 ? 2 : (DT == PA_KV_NVFP4 ? D / 16 : 0);
   static constexpr bool SW = ROW % 128 == 0;                  // TMA tensor copies + swizzle
@@ -110,8 +111,9 @@ struct Geo {
   static constexpr int SC = kBlock * SROW;
   static constexpr int PAYLOAD = 2 * (CODE + SC);
   static constexpr int STAGE = SW ? (PAYLOAD + 1023) / 1024 * 1024 : PAYLOAD;
-  // byte formats: 2 stages so that 3 CTAs (12 warps) fit per SM; NVFP4: 3
-  static constexpr int NSTAGE = BYTE_CODES ? 2 : 3;
+  // byte formats: 2 stages so that 3 CTAs (12 warps) fit per SM; NVFP4: 3;
+  // bf16 (16 KB per block at D = 256): 1, for 3 CTAs per SM
+  static constexpr int NSTAGE = BF16 ? 1 : (BYTE_CODES ? 2 : 3);
   static constexpr int WARP_BYTES = NSTAGE * STAGE;
   static constexpr int SMEM = kWarps * WARP_BYTES + (SW ? 1024 : 0);
   static_assert(KG >= 1 && VG >= 1 && CODE % 16 == 0 && SC % 16 == 0, "geometry");
@@ -125,6 +127,38 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// four 8x8 matrices of 16-bit elements from shared memory: lanes 8i..8i+7
+// give the row addresses of matrix i (16 contiguous bytes each); lane l gets
+// row l / 4, elements 2 (l % 4), 2 (l % 4) + 1 of each (.trans: of its transpose)
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &a0, uint32_t &a1, uint32_t &a2,
+                                        uint32_t &a3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &a0, uint32_t &a1,
+                                              uint32_t &a2, uint32_t &a3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+               : "r"(addr));
+}
+
+// (lo, hi) fp32 -> bf16x2, round to nearest even
+__device__ __forceinline__ uint32_t f2_to_bf2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -170,6 +204,12 @@ __device__ __forceinline__ float ex2f(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// this thread's generic-proxy shared-memory writes -> ordered before later
+// async-proxy (bulk copy) writes to the same bytes
+__device__ __forceinline__ void fence_async_smem_cta() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // transpose of an 8x8 matrix of 16-bit elements held by the warp (lane i:
@@ -232,16 +272,28 @@ __global__ void __launch_bounds__(kThreads, 3)
     const bool live = r < R;
     const __nv_bfloat16 *qrow =
         p.q + (((size_t)b * Q + qi) * p.Hq + (size_t)kvh * p.G + (live ? r : 0)) * D;
+    if constexpr (Gm::BF16) {
+      // bf16 keys come by ldmatrix in natural head-dim order: k-step t covers
+      // d = 16t .. 16t + 15, rows 2c, 2c+1 <-> d = 16t + 2c + {0,1}, rows
+      // 2c+8, 2c+9 <-> + 8; q stays bf16 (exact)
 #pragma unroll
-    for (int g = 0; g < KG; ++g)
-#pragma unroll
-      for (int s = 0; s < KS; ++s) {
-        const int d = g * 4 * Gm::E + c * Gm::E + 4 * s;
-        uint2 u = live ? *reinterpret_cast<const uint2 *>(qrow + d) : make_uint2(0, 0);
-        float2 x0 = bf16x2_to_f2(u.x), x1 = bf16x2_to_f2(u.y);
-        qf[g][s][0] = f2_to_h2(x0.x, x0.y);
-        qf[g][s][1] = f2_to_h2(x1.x, x1.y);
+      for (int t = 0; t < D / 16; ++t) {
+        const int d = 16 * t + 2 * c;
+        qf[t / KS][t % KS][0] = live ? *reinterpret_cast<const uint32_t *>(qrow + d) : 0u;
+        qf[t / KS][t % KS][1] = live ? *reinterpret_cast<const uint32_t *>(qrow + d + 8) : 0u;
       }
+    } else {
+#pragma unroll
+      for (int g = 0; g < KG; ++g)
+#pragma unroll
+        for (int s = 0; s < KS; ++s) {
+          const int d = g * 4 * Gm::E + c * Gm::E + 4 * s;
+          uint2 u = live ? *reinterpret_cast<const uint2 *>(qrow + d) : make_uint2(0, 0);
+          float2 x0 = bf16x2_to_f2(u.x), x1 = bf16x2_to_f2(u.y);
+          qf[g][s][0] = f2_to_h2(x0.x, x0.y);
+          qf[g][s][1] = f2_to_h2(x1.x, x1.y);
+        }
+    }
   }
   const float qscale = p.scale_log2 * (has_global_scale(DT) ? p.kv.kg : 1.0f);
 
@@ -339,7 +391,20 @@ __global__ void __launch_bounds__(kThreads, 3)
       // NVFP4 over four, so that the MMAs form independent dependency chains
       // (FP8 keeps one: it is at its register bound for 3 CTAs per SM)
       float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sacc2[4] = {0.f, 0.f, 0.f, 0.f};
-      float sacc3[4] = {0.f, 0.f, 0.f, 0.f}, sacc4[4] = {0.f, 0.f, 0.f, 0.f};   // NVFP4: 4 chains
+      float sacc3[4] = {0.f, 0.f, 0.f, 0.f}, sacc4[4] = {0.f, 0.f, 0.f, 0.f};   // NVFP4, bf16: 4 chains
+      if constexpr (Gm::BF16) {
+        // k-step t: matrices (tokens 0-7 | 8-15) x (d 16t .. +7 | 16t+8 .. +15);
+        // lane l addresses token row (l & 7) + 8 ((l >> 3) & 1), chunk l >> 4
+        const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8, lhalf = lane >> 4;
+        const uint32_t kbase = smem_u32(sK);
+#pragma unroll
+        for (int t = 0; t < D / 16; ++t) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(kbase + sw_off(lrow, 32 * t + 16 * lhalf), a0, a1, a2, a3);
+          float(&acc)[4] = (t & 3) == 0 ? sacc : (t & 3) == 1 ? sacc2 : (t & 3) == 2 ? sacc3 : sacc4;
+          mma16816_bf16(acc, a0, a1, a2, a3, qf[t / KS][t % KS][0], qf[t / KS][t % KS][1]);
+        }
+      } else {
 #pragma unroll
       for (int g = 0; g < KG; ++g) {
         const int boff = g * 64 + c * 16;
@@ -382,7 +447,8 @@ __global__ void __launch_bounds__(kThreads, 3)
           }
         }
       }
-      if constexpr (DT == PA_KV_NVFP4) {
+      }
+      if constexpr (DT == PA_KV_NVFP4 || Gm::BF16) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) sacc[k] = (sacc[k] + sacc2[k]) + (sacc3[k] + sacc4[k]);
       } else if constexpr (DT == PA_KV_INT8) {
@@ -449,6 +515,42 @@ __global__ void __launch_bounds__(kThreads, 3)
       // ---- P^T fragment (tokens 2c, 2c+1 | 2c+8, 2c+9; column r): the lane
       // holds P[token r | r + 8][heads 2c, 2c+1], which is the row layout of
       // an 8x8 b16 matrix, so one warp transpose per 8 tokens gives it
+      if constexpr (Gm::BF16) {
+        // bf16 P as hi + lo (hi = RN(p), lo = RN(p - hi)): about 16 significant
+        // bits of each probability reach the PV product
+        const uint32_t h0 = f2_to_bf2(pr[0], pr[1]), h1 = f2_to_bf2(pr[2], pr[3]);
+        const uint32_t l0 = f2_to_bf2(pr[0] - __uint_as_float(h0 << 16),
+                                      pr[1] - __uint_as_float(h0 & 0xffff0000u));
+        const uint32_t l1 = f2_to_bf2(pr[2] - __uint_as_float(h1 << 16),
+                                      pr[3] - __uint_as_float(h1 & 0xffff0000u));
+        const uint32_t B0h = movm_trans(h0), B1h = movm_trans(h1);
+        const uint32_t B0l = movm_trans(l0), B1l = movm_trans(l1);
+        // rows past the sequence end may hold anything (NaN included): zero
+        // them in this warp's own stage so that 0 * garbage never reaches O
+        if (nvalid < kBlock) {
+          uint8_t *vz = const_cast<uint8_t *>(sV);
+          constexpr int RC = ROW / 16;   // 16-byte chunks per row
+          for (int i = lane; i < (kBlock - nvalid) * RC; i += 32) {
+            const int t = nvalid + i / RC, j = i % RC;
+            *reinterpret_cast<uint4 *>(vz + (j >> 3) * (kBlock * 128) + t * 128 + (j & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_async_smem_cta();   // ordered before the next copy into this stage
+          __syncwarp();
+        }
+        // m-tile m: matrices (tokens 0-7 | 8-15) x (d 16m .. +7 | 16m+8 .. +15),
+        // transposed: lane l addresses token row (l & 7) + 8 ((l >> 4) & 1),
+        // chunk (l >> 3) & 1
+        const int vrow = (lane & 7) + ((lane >> 4) & 1) * 8, vhalf = (lane >> 3) & 1;
+        const uint32_t vbase = smem_u32(sV);
+#pragma unroll
+        for (int m = 0; m < VG; ++m) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_trans(vbase + sw_off(vrow, 32 * m + 16 * vhalf), a0, a1, a2, a3);
+          mma16816_bf16(o[m][0], a0, a1, a2, a3, B0h, B1h);
+          mma16816_bf16(o[m][0], a0, a1, a2, a3, B0l, B1l);
+        }
+      } else {
       const uint32_t B0 = movm_trans(f2_to_h2(pr[0], pr[1]));
       const uint32_t B1 = movm_trans(f2_to_h2(pr[2], pr[3]));
 
@@ -542,6 +644,7 @@ __global__ void __launch_bounds__(kThreads, 3)
           }
         }
       }
+      }
     }
     __syncwarp();
     if (issued < n_local) {
@@ -567,14 +670,25 @@ __global__ void __launch_bounds__(kThreads, 3)
     s_l[warp][2 * c + 1] = l_run[1];
   }
   float *ow = reinterpret_cast<float *>(wsm);   // [8 heads][D]
+  if constexpr (Gm::BF16) {   // m-tile g: rows d = 16 g + r and + 8 (natural order)
 #pragma unroll
-  for (int g = 0; g < VG; ++g)
-#pragma unroll
-    for (int e = 0; e < VE / 2; ++e) {
-      const int d = g * 8 * VE + r * VE + 2 * e;
-      *reinterpret_cast<float2 *>(ow + (2 * c) * D + d) = make_float2(o[g][e][0], o[g][e][2]);
-      *reinterpret_cast<float2 *>(ow + (2 * c + 1) * D + d) = make_float2(o[g][e][1], o[g][e][3]);
+    for (int g = 0; g < VG; ++g) {
+      const int d = 16 * g + r;
+      ow[(2 * c) * D + d] = o[g][0][0];
+      ow[(2 * c + 1) * D + d] = o[g][0][1];
+      ow[(2 * c) * D + d + 8] = o[g][0][2];
+      ow[(2 * c + 1) * D + d + 8] = o[g][0][3];
     }
+  } else {
+#pragma unroll
+    for (int g = 0; g < VG; ++g)
+#pragma unroll
+      for (int e = 0; e < VE / 2; ++e) {
+        const int d = g * 8 * VE + r * VE + 2 * e;
+        *reinterpret_cast<float2 *>(ow + (2 * c) * D + d) = make_float2(o[g][e][0], o[g][e][2]);
+        *reinterpret_cast<float2 *>(ow + (2 * c + 1) * D + d) = make_float2(o[g][e][1], o[g][e][3]);
+      }
+  }
   __syncthreads();
 
   // ---- merge the warps and write (rows h < R)

@@ -31,6 +31,7 @@ namespace vfy {
 
 using tc::e2m1x8_to_h2x4;
 using tc::e4m3x2_to_h2;
+using tc::ex2f;
 using tc::f2_to_h2;
 using tc::mma16816;
 using tc::prmt;
@@ -302,19 +303,21 @@ __global__ void __launch_bounds__(kThreads, NT == 2 ? 4 : 2)
       const bool ok1 = valid && r + 8 < nvalid && tok0 + r + 8 < olim[k];
       sc[k][0] = ok0 ? sc[k][0] * f0 : kNegInf;
       sc[k][1] = ok1 ? sc[k][1] * f1 : kNegInf;
-      float v = fmaxf(sc[k][0], sc[k][1]);
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-      mx[k] = v;
-      need |= v > m_run[k] + kRescale;
+      // the lane's own scores decide whether the running max must move; only
+      // then is the column max reduced over the 8 lanes holding the column
+      mx[k] = fmaxf(sc[k][0], sc[k][1]);
+      need |= mx[k] > m_run[k] + kRescale;
     }
     const bool any_need = __syncthreads_or(need);   // B2
     if (any_need) {
 #pragma unroll
       for (int k = 0; k < EPO; ++k) {
-        const float mn = fmaxf(m_run[k], mx[k]);
-        const float al = (mn == kNegInf) ? 1.f : exp2f(m_run[k] - mn);
+        float v = mx[k];
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+        const float mn = fmaxf(m_run[k], v);
+        const float al = (mn == kNegInf) ? 1.f : ex2f(m_run[k] - mn);
         m_run[k] = mn;
         l_run[k] *= al;
         if (r == 0) s_alpha[ocol[k]] = al;
@@ -332,8 +335,8 @@ __global__ void __launch_bounds__(kThreads, NT == 2 ? 4 : 2)
       }
 #pragma unroll
       for (int k = 0; k < EPO; ++k) {
-        const float p0 = sc[k][0] == kNegInf ? 0.f : exp2f(sc[k][0] - m_run[k]);
-        const float p1 = sc[k][1] == kNegInf ? 0.f : exp2f(sc[k][1] - m_run[k]);
+        const float p0 = sc[k][0] == kNegInf ? 0.f : ex2f(sc[k][0] - m_run[k]);
+        const float p1 = sc[k][1] == kNegInf ? 0.f : ex2f(sc[k][1] - m_run[k]);
         l_run[k] += p0 + p1;
         const __half h0 = __float2half_rn(p0 * vs0), h1 = __float2half_rn(p1 * vs1);
         pbuf[ocol[k] * kBlock + slot0] = __half_as_ushort(h0);

@@ -27,7 +27,8 @@ NAMES = {"bf16": "bf16_skewed_b256_l16_128k_d256", "int8": "int8_b32_l1k_32k_d25
 VERIFY_NAMES = {"nvfp4": "nvfp4_verify_q8_b4_ctx64k_d256", "int8": "int8_b32_l1k_32k_d256",
                 "fp8": "fp8_verify_q8_b4_ctx64k_d256"}
 # (dtype, kernel): 1 = CUDA-core kernel, 2 = tensor-core kernel
-DK = [("bf16", 1), ("int8", 1), ("int8", 2), ("nvfp4", 1), ("nvfp4", 2), ("fp8", 1), ("fp8", 2)]
+DK = [("bf16", 1), ("bf16", 2), ("int8", 1), ("int8", 2), ("nvfp4", 1), ("nvfp4", 2), ("fp8", 1),
+      ("fp8", 2)]
 LENS = [3000, 17, 1, 900, 0, 4099]
 
 

@@ -42,7 +42,7 @@ def _kernels(dtype, q_len=1):
     4 = tcgen05 verify (NVFP4 / FP8, q_len > 1)."""
     if dtype in ("nvfp4", "fp8") and q_len > 1:
         return [0, 1, 2, 3, 4]
-    return [0, 1, 2, 3] if dtype in ("int8", "nvfp4", "fp8") else [0, 1]
+    return [0, 1, 2, 3]
 
 
 REDUCED_CASES = [(n, k) for n in REDUCED
@@ -72,10 +72,15 @@ FULL_SAMPLES = {
 }
 
 
-@pytest.mark.parametrize("name", list(FULL_SAMPLES))
-def test_full_size_sampled_parity(name):
+# auto kernel for every workload; bf16 also on both of its kernels explicitly
+FULL_CASES = [(n, 0) for n in FULL_SAMPLES] + [("bf16_skewed_b256_l16_128k_d256", 1),
+                                                ("bf16_skewed_b256_l16_128k_d256", 2)]
+
+
+@pytest.mark.parametrize("name,kernel", FULL_CASES)
+def test_full_size_sampled_parity(name, kernel):
     wl = W.make_workload(name, device=DEV)
-    o32, lse, ws = run(wl, _fn(wl), out_fp32=True, return_lse=True)
+    o32, lse, ws = run(wl, _fn(wl), out_fp32=True, return_lse=True, kernel=kernel)
     torch.cuda.synchronize()
     assert pa.read_error(ws) == 0
     lens = wl.seq_lens.cpu()
@@ -117,8 +122,8 @@ def test_dequant_gather_bit_exact(dt):
     assert np.array_equal(vg.view(np.uint32), rv.view(np.uint32))
 
 
-@pytest.mark.parametrize("dt,kernel", [("bf16", 1), ("int8", 1), ("int8", 2), ("nvfp4", 1),
-                                       ("nvfp4", 2), ("fp8", 1), ("fp8", 2)])
+@pytest.mark.parametrize("dt,kernel", [("bf16", 1), ("bf16", 2), ("int8", 1), ("int8", 2),
+                                       ("nvfp4", 1), ("nvfp4", 2), ("fp8", 1), ("fp8", 2)])
 @pytest.mark.parametrize("shape", [(8, 8, 128), (16, 8, 128), (12, 2, 256), (4, 4, 256),
                                    (32, 4, 256), (2, 1, 128)])
 def test_gqa_and_head_dim_variants(dt, kernel, shape):
