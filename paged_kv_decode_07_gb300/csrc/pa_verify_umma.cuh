@@ -30,12 +30,13 @@
 //   warp 1       tensor-memory allocation; one thread issues the QK MMAs
 //   warps 2, 3   one thread each issues the PV MMAs of one head-dim half
 //   warps 4-7    K dequant: token row t of the tile -> TMEM lane t (f16x2)
-//   warps 12-15  V dequant: token rows -> the f16 V tile in shared memory
-//                (MN-major A operand layout)
-//   warps 8-11   softmax: S^T from tensor memory, masks, online softmax in
+//   warps 8-15   softmax, two groups of 4 warps, each with half of the N
+//                columns: S^T from tensor memory, masks, online softmax in
 //                the log2 domain with a lazy rescale (threshold 8), P^T to
 //                shared memory; at the end of an item O^T / l to the output
 //                or to the split-K partials (merged afterwards)
+//   warps 16-19  V dequant: token rows -> the f16 V tile in shared memory
+//                (MN-major A operand layout)
 // A warp reaches the tensor-memory lanes 32 (warp % 4) .. + 31, so each
 // group of 4 consecutive warps covers all 128 lanes.
 // Hand-offs are mbarriers (tcgen05.commit for the MMA side); every wait is
@@ -132,12 +133,42 @@ __device__ __forceinline__ void tmem_ld48(uint32_t taddr, float (&v)[48]) {
       : "r"(taddr), "r"(taddr + 16), "r"(taddr + 32)
       : "memory");
 }
-// N columns (16, 32 or 48) of this thread's lane
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+      " tcgen05.wait::ld.sync.aligned;"
+      : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]),
+        "=f"(v[7])
+      : "r"(taddr)
+      : "memory");
+}
+// 24 columns as three 8-column loads: every load starts at a multiple of its
+// own width (the second softmax group's columns start at 24)
+__device__ __forceinline__ void tmem_ld24(uint32_t taddr, float (&v)[24]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%24];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%25];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16,%17,%18,%19,%20,%21,%22,%23}, [%26];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]), "=f"(v[14]), "=f"(v[15]), "=f"(v[16]), "=f"(v[17]), "=f"(v[18]), "=f"(v[19]), "=f"(v[20]), "=f"(v[21]), "=f"(v[22]), "=f"(v[23])
+      : "r"(taddr), "r"(taddr + 8), "r"(taddr + 16)
+      : "memory");
+}
+// N columns (8, 16, 24, 32 or 48) of this thread's lane
 template <int N>
 __device__ __forceinline__ void tmem_ldn(uint32_t taddr, float (&v)[N]) {
-  if constexpr (N == 16) tmem_ld16(taddr, v);
+  static_assert(N == 8 || N == 16 || N == 24 || N == 32 || N == 48, "column count");
+  if constexpr (N == 8) tmem_ld8(taddr, v);
+  else if constexpr (N == 16) tmem_ld16(taddr, v);
+  else if constexpr (N == 24) tmem_ld24(taddr, v);
   else if constexpr (N == 32) tmem_ld32(taddr, v);
   else tmem_ld48(taddr, v);
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
 }
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
@@ -254,14 +285,14 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn) {
 constexpr int D = 256;
 constexpr int kTile = 128;                 // tokens per QK tile (the MMA's M)
 constexpr int kTileBlocks = kTile / kBlock;
-constexpr int kThreads = 512;              // 4 warpgroups
-constexpr int kLaunchRegs = 128;           // per thread at launch: 65536 / 512
-// Registers per thread of each warpgroup after the split (launched with 128
-// each): producer/MMA 88, K dequant 128, softmax 200, V dequant 96.  Per
-// SM sub-partition (one warp of each group) 512 = 4 x 128, so every
+constexpr int kThreads = 640;              // 5 warpgroups
+constexpr int kLaunchRegs = 96;            // per thread at launch: 65536 / 640, to a multiple of 8
+// Registers per thread of each warpgroup after the split: producer/MMA 64,
+// K dequant 104, each of the two softmax groups 120, V dequant 64.  Per SM
+// sub-partition (one warp of each group) 472 <= 5 x 96, so every
 // setmaxnreg.inc is satisfied by the decreases.
-constexpr int kRegCtl = 88, kRegK = 128, kRegSoftmax = 200, kRegV = 96;
-static_assert(kRegCtl + kRegK + kRegSoftmax + kRegV <= 4 * kLaunchRegs, "register split");
+constexpr int kRegCtl = 64, kRegK = 104, kRegSoftmax = 120, kRegV = 64;
+static_assert(kRegCtl + kRegK + 2 * kRegSoftmax + kRegV <= 5 * kLaunchRegs, "register split");
 static_assert(kLaunchRegs == 65536 / kThreads / 8 * 8, "launch register count");
 constexpr uint32_t kTmemCols = 512;
 // tensor-memory columns (32-bit each): two K tiles (128 tokens x 256 f16,
@@ -269,7 +300,7 @@ constexpr uint32_t kTmemCols = 512;
 // 128-lane halves (64 columns each, N used)
 constexpr uint32_t kColK = 0, kColS = 256, kColO = 384;
 // named barriers (0 is __syncthreads)
-constexpr uint32_t kBarSoftmax = 1, kBarK = 2;
+constexpr uint32_t kBarSoftmax = 1, kBarK = 2, kBarSoftmax1 = 3;
 
 template <int DT, int N>
 struct Geo {
@@ -701,7 +732,7 @@ __device__ void role_kdeq(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t t
   }
 }
 
-// warps 12-15: token row r of each block -> the block's f16 V slot, laid out
+// warps 16-19: token row r of each block -> the block's f16 V slot, laid out
 // [64-wide head-dim chunk][16 tokens][128 bytes, swizzled] (MN-major A of PV)
 template <int DT, int N>
 __device__ void role_vdeq(const AttnParams &p, uint8_t *smem, Ctl &c, int num_items, int warp,
@@ -784,14 +815,40 @@ __device__ __forceinline__ void colreduce(const float (&v)[N], int lane, float *
   }
 }
 
+// the same for any multiple of 8 columns: the reduce-scatter when the count
+// is a multiple of 16, else a butterfly per column (lane 0 writes)
+template <int N, bool MAX>
+__device__ __forceinline__ void colreduce_any(const float (&v)[N], int lane, float *dst) {
+  if constexpr (N % 16 == 0) {
+    colreduce<N, MAX>(v, lane, dst);
+  } else {
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+      float x = v[n];
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        const float y = __shfl_xor_sync(0xffffffffu, x, o);
+        x = MAX ? fmaxf(x, y) : x + y;
+      }
+      if (lane == 0) dst[n] = x;
+    }
+  }
+}
 
-// warps 12-15: token row t of each tile's S^T; per item an epilogue that
-// writes O^T / l (thread t owns head-dim elements t and 128 + t of every row)
+
+// warps 8-11 (half 0) and 12-15 (half 1): token row t of each tile's S^T,
+// columns (rows of the group) half * N/2 .. + N/2 - 1; per item an epilogue
+// that writes O^T / l (thread t owns head-dim elements t and 128 + t of its
+// rows)
 template <int DT, int N>
 __device__ void role_softmax(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t tmem,
-                             int num_items, int warp, int lane) {
+                             int num_items, int warp, int lane, int half) {
   using Gm = Geo<DT, N>;
   constexpr float kRescale = 8.0f;
+  // this warpgroup's columns (rows of the group): c0 .. c0 + NS - 1
+  constexpr int NS = N / 2;
+  const int c0 = half * NS;
+  const uint32_t bar = half ? kBarSoftmax1 : kBarSoftmax;
   const int q4 = warp & 3, t = q4 * 32 + lane, jb = t >> 4;
   const uint32_t lb = tmem + ((uint32_t)(q4 * 32) << 16);
   const float qscale = p.scale_log2 * p.kv.kg;
@@ -808,32 +865,34 @@ __device__ void role_softmax(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_
   for (int ii = blockIdx.x; ii < num_items && !failed; ii += gridDim.x) {
     const Item x = load_item(p, ii);
     const bool split = x.it.parts > 1;
-    if (t < N) {
-      const bool live = t < x.R;
-      const int qi = live ? (x.ro + t) / p.G : 0, gg = live ? (x.ro + t) % p.G : 0;
-      c.lim[t] = live ? x.L - p.Q + 1 + qi : 0;
-      c.orow[t] = split ? (x.it.slot * Hkv + x.kvh) * p.R + t
+    if (t < NS) {
+      const int n = c0 + t;
+      const bool live = n < x.R;
+      const int qi = live ? (x.ro + n) / p.G : 0, gg = live ? (x.ro + n) % p.G : 0;
+      c.lim[n] = live ? x.L - p.Q + 1 + qi : 0;
+      c.orow[n] = split ? (x.it.slot * Hkv + x.kvh) * p.R + n
                         : (x.b * p.Q + qi) * p.Hq + x.kvh * p.G + gg;
-      c.m[t] = kNegInf;
+      c.m[n] = kNegInf;
     }
-    named_sync(kBarSoftmax, 128);
+    named_sync(bar, 128);
     // rows are written as fp32 (split-K partials or an fp32 output) or bf16
     const bool f32 = split || p.out_fp32;
     float *const of = split ? p.part_o : reinterpret_cast<float *>(p.out);
     __nv_bfloat16 *const ob = reinterpret_cast<__nv_bfloat16 *>(p.out);
     float *const lo = split ? p.part_lse : p.lse_out;
     const int R = x.R;
-    // O^T columns (or zeros) of the 48 rows for head-dim element d; inv = 1 / l
-    auto store_rows = [&](const float (&o)[N], int d) {
+    // O^T columns (or zeros) of this group's rows for head-dim element d;
+    // inv = 1 / l
+    auto store_rows = [&](const float (&o)[NS], int d) {
 #pragma unroll
-      for (int n4 = 0; n4 < N; n4 += 4) {
-        const float4 iv = lds_f4(s_inv + 4 * n4);
-        const int4 rw = lds_s4(s_orow + 4 * n4);
+      for (int n4 = 0; n4 < NS; n4 += 4) {
+        const float4 iv = lds_f4(s_inv + 4 * (c0 + n4));
+        const int4 rw = lds_s4(s_orow + 4 * (c0 + n4));
         const float ivs[4] = {iv.x, iv.y, iv.z, iv.w};
         const int rws[4] = {rw.x, rw.y, rw.z, rw.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          if (n4 + k < R) {
+          if (c0 + n4 + k < R) {
             const size_t off = (size_t)rws[k] * D + d;
             const float val = o[n4 + k] * ivs[k];
             if (f32) of[off] = val;
@@ -844,9 +903,9 @@ __device__ void role_softmax(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_
     };
     const bool empty = x.n_blk == 0;   // nothing to attend: zeros, lse -inf
     const int lim_min = x.L - p.Q + 1 + x.ro / p.G;   // the first live row's key limit
-    float lp[N];                                      // this row's share of each l
+    float lp[NS];                                     // this row's share of each l
 #pragma unroll
-    for (int n = 0; n < N; ++n) lp[n] = 0.f;
+    for (int n = 0; n < NS; ++n) lp[n] = 0.f;
     for (int tile = 0; tile < x.ntiles; ++tile) {
       const int nb = min(kTileBlocks, x.n_blk - tile * kTileBlocks);
       const int tok0 = x.t_begin + tile * kTile, tok = tok0 + t;
@@ -859,16 +918,16 @@ __device__ void role_softmax(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_
       const int R = x.R;
       // log2-domain scores of one tile row (this thread's token), -inf where
       // masked; the causal limits are read only in the tiles that reach them
-      auto scores = [&](float (&v)[N]) {
+      auto scores = [&](float (&v)[NS]) {
 #pragma unroll
-        for (int n4 = 0; n4 < N; n4 += 4) {
+        for (int n4 = 0; n4 < NS; n4 += 4) {
           int4 lm = make_int4(0x7fffffff, 0x7fffffff, 0x7fffffff, 0x7fffffff);
-          if (causal) lm = lds_s4(s_lim + 4 * n4);
+          if (causal) lm = lds_s4(s_lim + 4 * (c0 + n4));
           const int lv[4] = {lm.x, lm.y, lm.z, lm.w};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int n = n4 + k;
-            const bool vis = row_ok && n < R && tok < lv[k];
+            const bool vis = row_ok && c0 + n < R && tok < lv[k];
             v[n] = vis ? v[n] * qscale : kNegInf;
           }
         }
@@ -876,94 +935,95 @@ __device__ void role_softmax(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_
       const bool ok = wait_bar(&c.sfull[g & 1], (g >> 1) & 1, c, p.hdr) &&
                       wait_bar(&c.pdone[g & 1], ((g >> 1) & 1) ^ 1, c, p.hdr);
       tc_fence_after();
-      const uint32_t sa = lb + kColS + (g & 1) * 64;
+      const uint32_t sa = lb + kColS + (g & 1) * 64 + c0;
       const uint32_t pb = pcol + (g & 1) * Gm::PBUF;
       // Raw dot products in, probabilities out (written to P^T as f16) with
       // the running max m: p = 2^(s * scale - m), one FMA for the exponent;
       // `need` is set where a visible score passes m by the threshold.  The
       // exponent is capped so that a tile about to be redone stays finite.
-      auto emit = [&](float (&v)[N], bool &need) {
+      auto emit = [&](float (&v)[NS], bool &need) {
 #pragma unroll
-        for (int n4 = 0; n4 < N; n4 += 4) {
-          const float4 m4 = lds_f4(s_m + 4 * n4);
+        for (int n4 = 0; n4 < NS; n4 += 4) {
+          const float4 m4 = lds_f4(s_m + 4 * (c0 + n4));
           const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
           int4 lm = make_int4(0x7fffffff, 0x7fffffff, 0x7fffffff, 0x7fffffff);
-          if (causal) lm = lds_s4(s_lim + 4 * n4);
+          if (causal) lm = lds_s4(s_lim + 4 * (c0 + n4));
           const int lv[4] = {lm.x, lm.y, lm.z, lm.w};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const int n = n4 + k;
-            const bool vis = row_ok && n < R && tok < lv[k];
+            const int n = n4 + k, col = c0 + n;
+            const bool vis = row_ok && col < R && tok < lv[k];
             const float d = fmaf(v[n], qscale, -mv[k]);
             need |= vis && d > kRescale;
             const float pr = vis ? ex2_approx(fminf(d, 64.f)) : 0.f;
             v[n] = pr;
-            sts_u16(pb + n * 128 + ((tu ^ (n & 7)) << 4), __half_as_ushort(__float2half_rn(pr)));
+            sts_u16(pb + col * 128 + ((tu ^ (col & 7)) << 4), __half_as_ushort(__float2half_rn(pr)));
           }
         }
       };
       // One pass with the current max; the first tile of an item (no max yet)
       // and the rare tile that raises a row's max by more than the threshold
       // are redone after the max update (a second pass of the same code).
-      float v[N];
+      float v[NS];
       bool redo = tile == 0;
       bool stop = false;
 #pragma unroll 1
       for (int pass = 0; pass < 2; ++pass) {
         if (!redo || pass == 1) {   // probabilities with the current max
-          tmem_ldn<N>(sa, v);
+          tmem_ldn<NS>(sa, v);
           bool need = false;
           emit(v, need);
           if (pass == 1) break;
           redo = need;
         }
-        if (!named_sync_or(kBarSoftmax, 128, redo || !ok)) break;
-        if (named_sync_or(kBarSoftmax, 128, !ok)) {
+        if (!named_sync_or(bar, 128, redo || !ok)) break;
+        if (named_sync_or(bar, 128, !ok)) {
           stop = true;
           break;
         }
         // new running max of every row: max over this tile's 128 rows
-        tmem_ldn<N>(sa, v);
+        tmem_ldn<NS>(sa, v);
         scores(v);
-        colreduce<N, true>(v, lane, c.red[q4]);
-        named_sync(kBarSoftmax, 128);
-        if (t < N) {
-          const float mt = fmaxf(fmaxf(c.red[0][t], c.red[1][t]), fmaxf(c.red[2][t], c.red[3][t]));
-          const float mo = c.m[t], mn = fmaxf(mo, mt);
-          c.alpha[t] = mn == kNegInf ? 1.f : exp2f(mo - mn);
-          c.mnew[t] = mn;
+        colreduce_any<NS, true>(v, lane, c.red[q4] + c0);
+        named_sync(bar, 128);
+        if (t < NS) {
+          const int n = c0 + t;
+          const float mt = fmaxf(fmaxf(c.red[0][n], c.red[1][n]), fmaxf(c.red[2][n], c.red[3][n]));
+          const float mo = c.m[n], mn = fmaxf(mo, mt);
+          c.alpha[n] = mn == kNegInf ? 1.f : exp2f(mo - mn);
+          c.mnew[n] = mn;
         }
-        named_sync(kBarSoftmax, 128);
+        named_sync(bar, 128);
 #pragma unroll
-        for (int n = 0; n < N; ++n) lp[n] *= c.alpha[n];
+        for (int n = 0; n < NS; ++n) lp[n] *= c.alpha[c0 + n];
         if (tile > 0) {   // O^T holds this item's earlier tiles: rescale once PV(g-1) is done
           const bool ok2 = wait_bar(&c.pdone[(g - 1) & 1], ((g - 1) >> 1) & 1, c, p.hdr);
-          if (named_sync_or(kBarSoftmax, 128, !ok2)) {
+          if (named_sync_or(bar, 128, !ok2)) {
             stop = true;
             break;
           }
           tc_fence_after();
-          const uint32_t oa = lb + kColO;
+          const uint32_t oa = lb + kColO + c0;
 #pragma unroll 1
-          for (int hc = 0; hc < 2 * (N / 16); ++hc) {   // (half, 16-column chunk)
-            const int h = hc / (N / 16), cb = hc % (N / 16);
-            float o[16];
-            uint32_t w[16];
-            tmem_ld16(oa + h * 64 + cb * 16, o);
+          for (int hc = 0; hc < 2 * (NS / 8); ++hc) {   // (head-dim half, 8-column chunk)
+            const int h = hc / (NS / 8), cb = hc % (NS / 8);
+            float o[8];
+            uint32_t w[8];
+            tmem_ld8(oa + h * 64 + cb * 8, o);
 #pragma unroll
-            for (int k4 = 0; k4 < 16; k4 += 4) {
-              const float4 a4 = lds_f4(smem_u32(c.alpha) + 4 * (cb * 16 + k4));
+            for (int k4 = 0; k4 < 8; k4 += 4) {
+              const float4 a4 = lds_f4(smem_u32(c.alpha) + 4 * (c0 + cb * 8 + k4));
               w[k4] = __float_as_uint(o[k4] * a4.x);
               w[k4 + 1] = __float_as_uint(o[k4 + 1] * a4.y);
               w[k4 + 2] = __float_as_uint(o[k4 + 2] * a4.z);
               w[k4 + 3] = __float_as_uint(o[k4 + 3] * a4.w);
             }
-            tmem_st16(oa + h * 64 + cb * 16, w);
+            tmem_st8(oa + h * 64 + cb * 8, w);
           }
           tmem_st_wait();
         }
-        if (t < N) c.m[t] = c.mnew[t];
-        named_sync(kBarSoftmax, 128);
+        if (t < NS) c.m[c0 + t] = c.mnew[c0 + t];
+        named_sync(bar, 128);
         redo = true;
       }
       if (stop) {
@@ -971,7 +1031,7 @@ __device__ void role_softmax(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_
         break;
       }
 #pragma unroll
-      for (int n = 0; n < N; ++n) lp[n] += v[n];   // this row's share of l
+      for (int n = 0; n < NS; ++n) lp[n] += v[n];   // this row's share of l
       tc_fence_before();
       mbar_arrive(&c.sfree[g & 1]);
       fence_async_smem();
@@ -980,41 +1040,43 @@ __device__ void role_softmax(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_
     }
     if (failed) break;
     // ---- epilogue: l of every row, then O^T / l (zeros for an empty item)
-    colreduce<N, false>(lp, lane, c.red[q4]);
+    colreduce_any<NS, false>(lp, lane, c.red[q4] + c0);
     const bool ok = empty || wait_bar(&c.odone, oi & 1, c, p.hdr);
-    if (named_sync_or(kBarSoftmax, 128, !ok)) {
+    if (named_sync_or(bar, 128, !ok)) {
       failed = true;
       break;
     }
-    if (t < N) {
-      const float l = (c.red[0][t] + c.red[1][t]) + (c.red[2][t] + c.red[3][t]);
-      c.inv[t] = l > 0.f ? vg / l : 0.f;
-      c.mnew[t] = l;
+    if (t < NS) {
+      const int n = c0 + t;
+      const float l = (c.red[0][n] + c.red[1][n]) + (c.red[2][n] + c.red[3][n]);
+      c.inv[n] = l > 0.f ? vg / l : 0.f;
+      c.mnew[n] = l;
     }
-    named_sync(kBarSoftmax, 128);
+    named_sync(bar, 128);
     tc_fence_after();
-    const uint32_t oa = lb + kColO;
+    const uint32_t oa = lb + kColO + c0;
 #pragma unroll 1
     for (int h = 0; h < 2; ++h) {
-      float o[N];
+      float o[NS];
       if (!empty) {
-        tmem_ldn<N>(oa + h * 64, o);
+        tmem_ldn<NS>(oa + h * 64, o);
       } else {
 #pragma unroll
-        for (int n = 0; n < N; ++n) o[n] = 0.f;
+        for (int n = 0; n < NS; ++n) o[n] = 0.f;
       }
       store_rows(o, h * 128 + t);
     }
-    if (t < R && lo) {
-      const float l = c.mnew[t];
-      lo[c.orow[t]] = l > 0.f ? (c.m[t] + __log2f(l)) * 0.69314718055994531f : kNegInf;
+    if (t < NS && c0 + t < R && lo) {
+      const int n = c0 + t;
+      const float l = c.mnew[n];
+      lo[c.orow[n]] = l > 0.f ? (c.m[n] + __log2f(l)) * 0.69314718055994531f : kNegInf;
     }
     if (!empty) {
       tc_fence_before();
       mbar_arrive(&c.ofree);
       ++oi;
     }
-    named_sync(kBarSoftmax, 128);   // tables and sums read before the next item rewrites them
+    named_sync(bar, 128);   // tables and sums read before the next item rewrites them
   }
 }
 
@@ -1040,12 +1102,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&c.rawfree[s], 2 * kBlock);   // 16 K rows + 16 V rows
     }
     mbar_init(&c.vfull, 128);
-    mbar_init(&c.ofree, 128);
+    mbar_init(&c.ofree, 256);   // both softmax groups
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c.sfull[i], 1);
-      mbar_init(&c.sfree[i], 128);
-      mbar_init(&c.pfull[i], 128);
+      mbar_init(&c.sfree[i], 256);
+      mbar_init(&c.pfull[i], 256);
       mbar_init(&c.pdone[i], 2);   // both PV threads
       mbar_init(&c.kfull[i], 128);
       mbar_init(&c.kfree[i], 1);
@@ -1081,9 +1143,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (wg == 1) {
     setmaxnreg_to<kLaunchRegs, kRegK>();
     role_kdeq<DT, N>(p, smem, c, tmem, num_items, warp, lane);
-  } else if (wg == 2) {
+  } else if (wg == 2 || wg == 3) {
     setmaxnreg_to<kLaunchRegs, kRegSoftmax>();
-    role_softmax<DT, N>(p, smem, c, tmem, num_items, warp, lane);
+    role_softmax<DT, N>(p, smem, c, tmem, num_items, warp, lane, wg - 2);
   } else {
     setmaxnreg_to<kLaunchRegs, kRegV>();
     role_vdeq<DT, N>(p, smem, c, num_items, warp, lane);
