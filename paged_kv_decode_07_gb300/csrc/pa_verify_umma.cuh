@@ -208,6 +208,11 @@ __device__ __forceinline__ uint4 lds_u4(uint32_t a) {
                : "r"(a));
   return v;
 }
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
 __device__ __forceinline__ void sts_u4(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w));
 }
@@ -287,11 +292,11 @@ constexpr int kTile = 128;                 // tokens per QK tile (the MMA's M)
 constexpr int kTileBlocks = kTile / kBlock;
 constexpr int kThreads = 640;              // 5 warpgroups
 constexpr int kLaunchRegs = 96;            // per thread at launch: 65536 / 640, to a multiple of 8
-// Registers per thread of each warpgroup after the split: producer/MMA 64,
-// K dequant 104, each of the two softmax groups 120, V dequant 64.  Per SM
+// Registers per thread of each warpgroup after the split: producer/MMA 56,
+// K dequant 112, each of the two softmax groups 120, V dequant 64.  Per SM
 // sub-partition (one warp of each group) 472 <= 5 x 96, so every
 // setmaxnreg.inc is satisfied by the decreases.
-constexpr int kRegCtl = 64, kRegK = 104, kRegSoftmax = 120, kRegV = 64;
+constexpr int kRegCtl = 56, kRegK = 112, kRegSoftmax = 120, kRegV = 64;
 static_assert(kRegCtl + kRegK + 2 * kRegSoftmax + kRegV <= 5 * kLaunchRegs, "register split");
 static_assert(kLaunchRegs == 65536 / kThreads / 8 * 8, "launch register count");
 constexpr uint32_t kTmemCols = 512;
@@ -600,33 +605,43 @@ __device__ void role_pv(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t tme
 // Token row r of a raw stage dequantised to f16, 32 head-dim elements at a
 // time: sink(u, h) gets h[k] = (element 32u + 2k, element 32u + 2k + 1) as
 // f16x2 (low half first).  An invalid row yields zeros (codes and scales
-// are not read: poisoned slots may hold NaN scales).
-template <int DT, typename Sink>
+// are not read: poisoned slots may hold NaN scales).  Every lane runs the
+// same instruction sequence whether its row is valid or not (zeros are
+// selected, not branched to): a K sink is a warp-wide tcgen05.st, which
+// all 32 lanes must execute together.
+template <int DT, int UU, typename Sink>
 __device__ __forceinline__ void deq_row(uint32_t st, int code_off, int scale_off, int r,
                                         bool valid, Sink &&sink) {
+  static_assert(UU == 1 || UU == 2, "chunks in flight");
   const uint4 z = make_uint4(0, 0, 0, 0);
   if constexpr (DT == PA_KV_NVFP4) {
-    const uint4 sc = valid ? lds_u4(st + scale_off + r * 16) : z;
+    // chunks 2 u2 and 2 u2 + 1 use the row's scale bytes 4 u2 .. 4 u2 + 3
 #pragma unroll 1
-    for (int u = 0; u < 8; ++u) {
-      const uint4 w = valid ? lds_u4(st + code_off + tc::sw_off(r, 16 * u)) : z;
-      uint32_t h0[4], h1[4], h2[4], h3[4];
-      tc::e2m1x8_to_h2x4(w.x, h0);
-      tc::e2m1x8_to_h2x4(w.y, h1);
-      tc::e2m1x8_to_h2x4(w.z, h2);
-      tc::e2m1x8_to_h2x4(w.w, h3);
-      const uint32_t w4 = (u >> 1) == 0 ? sc.x : (u >> 1) == 1 ? sc.y : (u >> 1) == 2 ? sc.z : sc.w;
-      const uint32_t sw = w4 >> (16 * (u & 1));   // scale bytes 2u, 2u + 1
-      const uint32_t s0 = e4m3_to_h2_dup(sw & 0xffu), s1 = e4m3_to_h2_dup((sw >> 8) & 0xffu);
-      uint32_t h[16];
+    for (int u2 = 0; u2 < 4; ++u2) {
+      const uint32_t sw = valid ? lds_u32(st + scale_off + r * 16 + 4 * u2) : 0u;
+      uint32_t sd[4];
+      tc::e4m3x2_dup(sw & 0xffffu, sd[0], sd[1]);
+      tc::e4m3x2_dup(sw >> 16, sd[2], sd[3]);
+#pragma unroll UU
+      for (int uu = 0; uu < 2; ++uu) {
+        const int u = 2 * u2 + uu;
+        const uint4 w = valid ? lds_u4(st + code_off + tc::sw_off(r, 16 * u)) : z;
+        uint32_t h0[4], h1[4], h2[4], h3[4];
+        tc::e2m1x8_to_h2x4(w.x, h0);
+        tc::e2m1x8_to_h2x4(w.y, h1);
+        tc::e2m1x8_to_h2x4(w.z, h2);
+        tc::e2m1x8_to_h2x4(w.w, h3);
+        const uint32_t s0 = uu ? sd[2] : sd[0], s1 = uu ? sd[3] : sd[1];
+        uint32_t h[16];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        h[k] = hmul2_u32(h0[k], s0);
-        h[4 + k] = hmul2_u32(h1[k], s0);
-        h[8 + k] = hmul2_u32(h2[k], s1);
-        h[12 + k] = hmul2_u32(h3[k], s1);
+        for (int k = 0; k < 4; ++k) {
+          h[k] = hmul2_u32(h0[k], s0);
+          h[4 + k] = hmul2_u32(h1[k], s0);
+          h[8 + k] = hmul2_u32(h2[k], s1);
+          h[12 + k] = hmul2_u32(h3[k], s1);
+        }
+        sink(u, h);
       }
-      sink(u, h);
     }
   } else {   // FP8-E4M3: one byte per element, exact in f16
 #pragma unroll 1
@@ -715,7 +730,7 @@ __device__ void role_kdeq(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t t
       if (tile == 0) store_q<N>(qv, smem + Gm::OFF_Q, t);
       const int tok = x.t_begin + (tile * kTileBlocks + jb) * kBlock + r;
       const bool valid = have && c.rvalid[s] != 0 && tok < x.t_end;
-      deq_row<DT>(smem_u32(smem) + tp * Gm::RTILE, jb * Gm::CODE, Gm::R_KS + jb * Gm::SC, r, valid,
+      deq_row<DT, 2>(smem_u32(smem) + tp * Gm::RTILE, jb * Gm::CODE, Gm::R_KS + jb * Gm::SC, r, valid,
                   [&](int u, const uint32_t(&h)[16]) { tmem_st16(ta + 16 * u, h); });
       tmem_st_wait();
       if (tile == 0) fence_async_smem();   // Q, written by this thread, for the MMA
@@ -764,7 +779,7 @@ __device__ void role_vdeq(const AttnParams &p, uint8_t *smem, Ctl &c, int num_it
         const int tok = x.t_begin + (tile * kTileBlocks + jb) * kBlock + r;
         const bool valid = c.rvalid[s] != 0 && tok < x.t_end;
         const uint32_t vsl = smem_u32(smem) + Gm::OFF_V + vs * Gm::VSLOT + r * 128;
-        deq_row<DT>(smem_u32(smem) + tp * Gm::RTILE, Gm::R_V + jb * Gm::CODE, Gm::R_VS + jb * Gm::SC,
+        deq_row<DT, 1>(smem_u32(smem) + tp * Gm::RTILE, Gm::R_V + jb * Gm::CODE, Gm::R_VS + jb * Gm::SC,
                     r, valid, [&](int u, const uint32_t(&h)[16]) {
 #pragma unroll
                       for (int w = 0; w < 4; ++w)
