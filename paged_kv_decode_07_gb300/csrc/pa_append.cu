@@ -7,7 +7,9 @@
 //
 // Each warp takes four consecutive (token, kv head) rows; their K and V
 // (D bf16 each, 16 or 8 bytes per lane, coalesced) are loaded together,
-// encoded in registers and written as one contiguous code run per row.  Every rounding decision is
+// encoded in registers and written as one contiguous code run per row.
+// NVFP4 gives each lane one 16-element scale block instead (two or four
+// rows per warp step).  Every rounding decision is
 // that of the IEEE fp32 quotient (formed without a division per element,
 // see the bracket below), so the codes are the format definitions' own:
 //   int8  : s = fp16_RN(amax / 127), code = clamp(RN_even(x / s), +-127)
@@ -345,11 +347,126 @@ __global__ void __launch_bounds__(kAppendWarps * 32, 4) append_kernel(const Appe
   }
 }
 
+// ---- NVFP4 with one 16-element scale block per lane: D / 16 lanes per row
+// and 512 / D rows per warp step, so the block max needs no shuffle and the
+// scale work (bracketed E4M3 scale, reciprocal) is shared by 16 elements.
+// The decisions are those of encode_store<PA_KV_NVFP4> above.
+__device__ __forceinline__ void nvfp4_encode16(const uint4 (&u)[2], float g, bool store,
+                                               uint8_t *cdst, uint8_t *sdst) {
+  const uint32_t wv[8] = {u[0].x, u[0].y, u[0].z, u[0].w, u[1].x, u[1].y, u[1].z, u[1].w};
+  float x[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 f = bf16x2_to_f2(wv[i]);
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  // block scale = E4M3(RN(amax / RN(g * 6)))
+  const float den = __fmul_rn(g, 6.0f);
+  const float rden = rcp_approx(den);
+  uint32_t sc = e4m3x2_rn_sat(__fmul_rn(amax, __fmul_rn(rden, kBracketLo)), 0.f) & 0xFFu;
+  const uint32_t sc_hi = e4m3x2_rn_sat(__fmul_rn(amax, __fmul_rn(rden, kBracketHi)), 0.f) & 0xFFu;
+  if (!(g > 0.f && rden < kInf) || sc != sc_hi)
+    sc = g > 0.f ? (e4m3x2_rn_sat(__fdiv_rn(amax, den), 0.f) & 0xFFu) : 0u;
+  const float sg = __fmul_rn(e4m3_to_float(sc), g);
+  const float rsg = rcp_approx(sg);
+  const float rlo = __fmul_rn(rsg, kBracketLo), rhi = __fmul_rn(rsg, kBracketHi);
+  float lo0[8], lo1[8], hi0[8], hi1[8];
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {
+    const float2 a = fmul2(make_float2(x[i], x[i + 1]), make_float2(rlo, rlo));
+    const float2 b = fmul2(make_float2(x[i], x[i + 1]), make_float2(rhi, rhi));
+    const float2 c = fmul2(make_float2(x[8 + i], x[9 + i]), make_float2(rlo, rlo));
+    const float2 d = fmul2(make_float2(x[8 + i], x[9 + i]), make_float2(rhi, rhi));
+    lo0[i] = a.x; lo0[i + 1] = a.y;
+    hi0[i] = b.x; hi0[i + 1] = b.y;
+    lo1[i] = c.x; lo1[i + 1] = c.y;
+    hi1[i] = d.x; hi1[i + 1] = d.y;
+  }
+  // signed inputs: the code's sign bit is that of x / sg, -0 included
+  uint32_t c0 = e2m1x8_rn_sat(lo0), c1 = e2m1x8_rn_sat(lo1);
+  const bool ok = sg > 0.f && rsg < kInf && c0 == e2m1x8_rn_sat(hi0) && c1 == e2m1x8_rn_sat(hi1);
+  if (__any_sync(0xffffffffu, !ok) && !ok) {
+    float y0[8], y1[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      y0[i] = sg > 0.f ? __fdiv_rn(x[i], sg) : 0.f;
+      y1[i] = sg > 0.f ? __fdiv_rn(x[8 + i], sg) : 0.f;
+    }
+    c0 = e2m1x8_rn_sat(y0);
+    c1 = e2m1x8_rn_sat(y1);
+  }
+  if (!(sg > 0.f)) c0 = c1 = 0;   // the quotient is taken as +0
+  if (store) {
+    *reinterpret_cast<uint2 *>(cdst) = make_uint2(c0, c1);
+    *sdst = (uint8_t)sc;
+  }
+}
+
+// 3 CTAs per SM: the 8 K / V chunks a lane keeps in flight need more than 64 registers
+template <int D>
+__global__ void __launch_bounds__(kAppendWarps * 32, 3) append_nvfp4_kernel(const AppendParams p) {
+  constexpr int LPR = D / 16, RPS = 32 / LPR, STEPS = kRows / RPS;
+  static_assert(STEPS >= 1 && kRows % RPS == 0, "rows per warp");
+  const int lane = threadIdx.x & 31, sub = lane / LPR, ll = lane % LPR;
+  // rows < 2^30 (checked on the host): 32-bit indices
+  const int r0 = (blockIdx.x * kAppendWarps + (threadIdx.x >> 5)) * kRows;
+  const int Hkv = p.kv.hkv;
+  const int nrows = p.T * Hkv;
+  if (r0 >= nrows) return;   // the whole warp: every lane below runs the same steps
+  int64_t slot[STEPS];
+  int head[STEPS];
+  uint4 kx[STEPS][2], vx[STEPS][2];
+#pragma unroll
+  for (int s = 0; s < STEPS; ++s) {
+    const int r = r0 + s * RPS + sub;
+    const int t = r / Hkv;
+    head[s] = r - t * Hkv;
+    if (r < nrows) {
+      slot[s] = __ldg(p.slots + t);
+      const size_t src = (size_t)r * D + ll * 16;
+      kx[s][0] = __ldcs(reinterpret_cast<const uint4 *>(p.k_new + src));
+      kx[s][1] = __ldcs(reinterpret_cast<const uint4 *>(p.k_new + src + 8));
+      vx[s][0] = __ldcs(reinterpret_cast<const uint4 *>(p.v_new + src));
+      vx[s][1] = __ldcs(reinterpret_cast<const uint4 *>(p.v_new + src + 8));
+    } else {
+      slot[s] = -1;
+      kx[s][0] = kx[s][1] = vx[s][0] = vx[s][1] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  const int64_t nslots = (int64_t)p.kv.num_blocks * kBlock;
+#pragma unroll
+  for (int s = 0; s < STEPS; ++s) {
+    const bool bad = slot[s] < -1 || slot[s] >= nslots;
+    if (bad && ll == 0) set_err(p.hdr, PA_ERRF_BAD_SLOT);
+    const bool st = slot[s] >= 0 && !bad;   // -1: padded row (or past the end)
+    size_t row = 0;
+    if (st) {
+      const int blk = (int)(slot[s] >> 4), off = (int)slot[s] & (kBlock - 1);
+      row = ((size_t)blk * Hkv + head[s]) * kBlock + off;
+    }
+    nvfp4_encode16(kx[s], p.kv.kg, st, static_cast<uint8_t *>(const_cast<void *>(p.kv.k)) + row * (D / 2) + ll * 8,
+                   static_cast<uint8_t *>(const_cast<void *>(p.kv.ks)) + row * (D / 16) + ll);
+    nvfp4_encode16(vx[s], p.kv.vg, st, static_cast<uint8_t *>(const_cast<void *>(p.kv.v)) + row * (D / 2) + ll * 8,
+                   static_cast<uint8_t *>(const_cast<void *>(p.kv.vs)) + row * (D / 16) + ll);
+  }
+}
+
 template <int DT>
 cudaError_t launch_dt(const AppendParams &p, cudaStream_t s) {
   const int rows = p.T * p.kv.hkv;
   const int per_cta = kAppendWarps * kRows;
   const unsigned grid = (unsigned)((rows + per_cta - 1) / per_cta);
+  if constexpr (DT == PA_KV_NVFP4) {
+    if (p.kv.D == 128)
+      append_nvfp4_kernel<128><<<grid, kAppendWarps * 32, 0, s>>>(p);
+    else
+      append_nvfp4_kernel<256><<<grid, kAppendWarps * 32, 0, s>>>(p);
+    return cudaGetLastError();
+  }
   if (p.kv.D == 128)
     append_kernel<DT, 128><<<grid, kAppendWarps * 32, 0, s>>>(p);
   else
