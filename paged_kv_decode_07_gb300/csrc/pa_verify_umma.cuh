@@ -293,10 +293,10 @@ constexpr int kTileBlocks = kTile / kBlock;
 constexpr int kThreads = 640;              // 5 warpgroups
 constexpr int kLaunchRegs = 96;            // per thread at launch: 65536 / 640, to a multiple of 8
 // Registers per thread of each warpgroup after the split: producer/MMA 56,
-// K dequant 112, each of the two softmax groups 120, V dequant 64.  Per SM
-// sub-partition (one warp of each group) 472 <= 5 x 96, so every
+// K dequant 112, each of the two softmax groups 120, V dequant 72.  Per SM
+// sub-partition (one warp of each group) 480 = 5 x 96, so every
 // setmaxnreg.inc is satisfied by the decreases.
-constexpr int kRegCtl = 56, kRegK = 112, kRegSoftmax = 120, kRegV = 64;
+constexpr int kRegCtl = 56, kRegK = 112, kRegSoftmax = 120, kRegV = 72;
 static_assert(kRegCtl + kRegK + 2 * kRegSoftmax + kRegV <= 5 * kLaunchRegs, "register split");
 static_assert(kLaunchRegs == 65536 / kThreads / 8 * 8, "launch register count");
 constexpr uint32_t kTmemCols = 512;
@@ -779,7 +779,7 @@ __device__ void role_vdeq(const AttnParams &p, uint8_t *smem, Ctl &c, int num_it
         const int tok = x.t_begin + (tile * kTileBlocks + jb) * kBlock + r;
         const bool valid = c.rvalid[s] != 0 && tok < x.t_end;
         const uint32_t vsl = smem_u32(smem) + Gm::OFF_V + vs * Gm::VSLOT + r * 128;
-        deq_row<DT, 1>(smem_u32(smem) + tp * Gm::RTILE, Gm::R_V + jb * Gm::CODE, Gm::R_VS + jb * Gm::SC,
+        deq_row<DT, 2>(smem_u32(smem) + tp * Gm::RTILE, Gm::R_V + jb * Gm::CODE, Gm::R_VS + jb * Gm::SC,
                     r, valid, [&](int u, const uint32_t(&h)[16]) {
 #pragma unroll
                       for (int w = 0; w < 4; ++w)
