@@ -81,9 +81,10 @@ def profiled_traffic(workload: str):
     """dram bytes per launch of the attention kernel from the committed ncu
     summary for this workload, or None if absent or taken on other source."""
     lines = None
-    for kind in ("decode", "verify", "append"):
+    # decode_<workload>.md, verify_<workload>.md; append workloads carry their kind in the name
+    for fname in (f"decode_{workload}.md", f"verify_{workload}.md", f"{workload}.md"):
         try:
-            lines = open(os.path.join(ROOT, "profiles", f"{kind}_{workload}.md")).read().splitlines()
+            lines = open(os.path.join(ROOT, "profiles", fname)).read().splitlines()
             break
         except OSError:
             continue
