@@ -315,30 +315,33 @@ struct Geo {
   static constexpr int SROW = DT == PA_KV_NVFP4 ? D / 16 : 0;   // scale bytes per token row
   static constexpr int CODE = kBlock * ROW;
   static constexpr int SC = kBlock * SROW;
-  static constexpr int PAYLOAD = 2 * (CODE + SC);
-  // raw stage of one tile: [K codes of 8 blocks][V codes][K scales][V scales]
-  // (every 2 KB code box stays 1 KB aligned for the 128-byte swizzle)
-  static constexpr int RTILE = (kTileBlocks * PAYLOAD + 1023) / 1024 * 1024;
-  static constexpr int R_V = kTileBlocks * CODE, R_KS = 2 * kTileBlocks * CODE,
-                       R_VS = R_KS + kTileBlocks * SC;
-  // Ring slots belong to a block's position in its tile: raw stage
-  // (tile % NRT) * 8 + j holds block j of a tile, so each stage always has
+  // K and V codes arrive in two rings of raw stages, so that the K side of
+  // the next tiles is fetched while the V dequant (which trails by about a
+  // tile) still holds its stage.  Raw stage of one tile and side:
+  // [codes of 8 blocks][scales of 8 blocks] (every 2 KB code box stays 1 KB
+  // aligned for the 128-byte swizzle).
+  static constexpr int RSIDE = (kTileBlocks * (CODE + SC) + 1023) / 1024 * 1024;
+  static constexpr int R_SC = kTileBlocks * CODE;
+  // Ring slots belong to a block's position in its tile: stage
+  // (tile % NR) * 8 + j holds block j of a tile, so each stage always has
   // the same consumer threads and no waiter can run two phases ahead of a
   // stage (partial tiles leave stages unused instead of shifting the block
   // -> stage map).  The f16 V of a tile (8 blocks) is handed over as a whole.
-  static constexpr int NRT = DT == PA_KV_NVFP4 ? 3 : 1;          // tiles of raw stages
-  static constexpr int NR = NRT * kTileBlocks;
+  static constexpr int NRK = DT == PA_KV_NVFP4 ? 3 : 2;   // K tiles in flight
+  static constexpr int NRV = DT == PA_KV_NVFP4 ? 3 : 1;   // V tiles in flight
+  static constexpr int OFF_RK = 0, OFF_RV = NRK * RSIDE;
   static constexpr int VSLOT = kBlock * D * 2;                   // f16 V of one block
   static constexpr int NV = kTileBlocks;
   static constexpr int QCH = N * 128;   // one 64-wide K-major chunk of N rows
   static constexpr int QBUF = 4 * QCH;  // Q: 256 = 4 chunks of 64
   static constexpr int PBUF = 2 * QCH;  // P^T: 128 tokens = 2 chunks of 64
-  static constexpr int OFF_V = NRT * RTILE;
+  static constexpr int OFF_V = OFF_RV + NRV * RSIDE;
   static constexpr int OFF_Q = OFF_V + NV * VSLOT;
   static constexpr int OFF_P = OFF_Q + QBUF;
   static constexpr int BYTES = OFF_P + 2 * PBUF;
   static constexpr int SMEM = BYTES + 1024;   // + alignment slack
-  static_assert(QCH % 1024 == 0 && RTILE % 1024 == 0 && VSLOT % 1024 == 0 && CODE % 1024 == 0,
+  static_assert(NRK <= 3 && NRV <= 3, "ring sizes (control block)");
+  static_assert(QCH % 1024 == 0 && RSIDE % 1024 == 0 && VSLOT % 1024 == 0 && CODE % 1024 == 0,
                 "1 KB atoms");
   static_assert(SMEM + 4096 <= 227 * 1024, "shared memory (with the static control block)");
 };
@@ -357,7 +360,8 @@ constexpr int kMaxN = 48;
 constexpr int kMaxNR = 24;
 
 struct Ctl {
-  uint64_t rawfull[kMaxNR], rawfree[kMaxNR];   // raw stages: TMA -> K and V dequant
+  uint64_t rkfull[kMaxNR], rkfree[kMaxNR];     // K raw stages: TMA -> K dequant
+  uint64_t rvfull[kMaxNR], rvfree[kMaxNR];     // V raw stages: TMA -> V dequant
   uint64_t vfull, vfree;                       // f16 V tile: V dequant <-> PV
   uint64_t kfull[2], kfree[2];                 // K buffers in tensor memory: K dequant <-> QK
   uint64_t sfull[2], sfree[2];                 // S buffers: QK <-> softmax
@@ -366,7 +370,7 @@ struct Ctl {
   uint64_t done;                               // every MMA of the CTA complete
   uint32_t tmem;                               // tensor-memory base address
   int abort;                                   // a capped wait ran out somewhere
-  int rvalid[kMaxNR];                          // raw stage holds a valid block
+  int rkvalid[kMaxNR], rvvalid[kMaxNR];        // raw stage holds a valid block
   alignas(16) float m[kMaxN];                  // running max of each row (log2 domain)
   alignas(16) float mnew[kMaxN], alpha[kMaxN], inv[kMaxN];
   alignas(16) float red[4][kMaxN];
@@ -452,19 +456,26 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
 
 // ------------------------------------------------------------------ roles
 
-// warp 0, lanes 0-7: lane j copies block j of every tile into raw stage
-// (tile % NRT) * 8 + j (K / V code tiles by 2-D TMA with 128-byte swizzle,
-// NVFP4 block scales by 1-D bulk copies).  One lane per block position
+// warp 0: lane j (0-7) copies the K side of block j of every tile into K
+// stage (tile % NRK) * 8 + j, lane 8 + j the V side into V stage
+// (tile % NRV) * 8 + j (code tiles by 2-D TMA with 128-byte swizzle, NVFP4
+// block scales by 1-D bulk copies).  One lane per block position and side
 // issues a tile's copies in parallel and keeps its stage counters and the
 // next tile's block id in registers.
 template <int DT, int N>
 __device__ void role_producer(const AttnParams &p, const CUtensorMap *tmK, const CUtensorMap *tmV,
-                              uint8_t *smem, Ctl &c, int num_items, int jt) {
+                              uint8_t *smem, Ctl &c, int num_items, int jt, int side) {
   using Gm = Geo<DT, N>;
   const uint64_t pol = policy_evict_first();
-  uint32_t ruse[Gm::NRT];   // fills of this lane's raw stages so far
-#pragma unroll
-  for (int a = 0; a < Gm::NRT; ++a) ruse[a] = 0;
+  // this lane's ring: the K or the V side
+  const int nr = side ? Gm::NRV : Gm::NRK;
+  uint64_t *const full = side ? c.rvfull : c.rkfull;
+  uint64_t *const free_ = side ? c.rvfree : c.rkfree;
+  int *const rvalid = side ? c.rvvalid : c.rkvalid;
+  const CUtensorMap *const tm = side ? tmV : tmK;
+  const uint8_t *const scales = static_cast<const uint8_t *>(side ? p.kv.vs : p.kv.ks);
+  uint8_t *const base = smem + (side ? Gm::OFF_RV : Gm::OFF_RK);
+  uint32_t ruse[3] = {0u, 0u, 0u};   // fills of this lane's stages so far
   uint32_t g = 0;
   bool ok = true;
   for (int ii = blockIdx.x; ii < num_items && ok; ii += gridDim.x) {
@@ -477,45 +488,39 @@ __device__ void role_producer(const AttnParams &p, const CUtensorMap *tmK, const
       const int j2 = (tile + 1) * kTileBlocks + jt;
       nxt = j2 < x.n_blk ? x.trow[x.it.blk_begin + j2] : -1;
       if (jt >= nb) continue;
-      const int stage = (int)(g % Gm::NRT);
+      const int stage = (int)(g % (uint32_t)nr);
       const int s = stage * kTileBlocks + jt;
       uint32_t use = 0;
 #pragma unroll
-      for (int a = 0; a < Gm::NRT; ++a)
+      for (int a = 0; a < 3; ++a)
         if (a == stage) use = ruse[a]++;
-      if (!wait_bar(&c.rawfree[s], (use & 1) ^ 1, c, p.hdr)) {
+      if (!wait_bar(&free_[s], (use & 1) ^ 1, c, p.hdr)) {
         ok = false;
         break;
       }
       const bool v = phys >= 0 && phys < p.kv.num_blocks;
-      c.rvalid[s] = v;
+      rvalid[s] = v;
       if (!v) {
-        set_err(p.hdr, PA_ERRF_BAD_BLOCK_ID);
-        mbar_arrive(&c.rawfull[s]);
+        if (side == 0) set_err(p.hdr, PA_ERRF_BAD_BLOCK_ID);
+        mbar_arrive(&full[s]);
         continue;
       }
-      uint8_t *st = smem + stage * Gm::RTILE;
+      uint8_t *st = base + stage * Gm::RSIDE;
       const size_t tile_id = (size_t)phys * p.kv.hkv + x.kvh;
       const int y = (int)(tile_id * kBlock);
-      mbar_arrive_expect_tx(&c.rawfull[s], Gm::PAYLOAD);
+      mbar_arrive_expect_tx(&full[s], Gm::CODE + Gm::SC);
 #pragma unroll
-      for (int xo = 0; xo < Gm::ROW; xo += 128) {
-        tc::tma_rows(st + jt * Gm::CODE + xo * kBlock, tmK, xo, y, &c.rawfull[s], pol);
-        tc::tma_rows(st + Gm::R_V + jt * Gm::CODE + xo * kBlock, tmV, xo, y, &c.rawfull[s], pol);
-      }
-      if constexpr (Gm::SC > 0) {
-        bulk_g2s(st + Gm::R_KS + jt * Gm::SC, (const uint8_t *)p.kv.ks + tile_id * Gm::SC, Gm::SC,
-                 &c.rawfull[s], pol);
-        bulk_g2s(st + Gm::R_VS + jt * Gm::SC, (const uint8_t *)p.kv.vs + tile_id * Gm::SC, Gm::SC,
-                 &c.rawfull[s], pol);
-      }
+      for (int xo = 0; xo < Gm::ROW; xo += 128)
+        tc::tma_rows(st + jt * Gm::CODE + xo * kBlock, tm, xo, y, &full[s], pol);
+      if constexpr (Gm::SC > 0)
+        bulk_g2s(st + Gm::R_SC + jt * Gm::SC, scales + tile_id * Gm::SC, Gm::SC, &full[s], pol);
     }
   }
   // the last fill of each of this lane's stages may still be in flight after
   // a failure: let the copies land before the CTA exits
 #pragma unroll
-  for (int a = 0; a < Gm::NRT; ++a)
-    if (ruse[a] > 0) drain_wait(&c.rawfull[a * kTileBlocks + jt], (ruse[a] - 1) & 1);
+  for (int a = 0; a < 3; ++a)
+    if (ruse[a] > 0) drain_wait(&full[a * kTileBlocks + jt], (ruse[a] - 1) & 1);
 }
 
 // Two MMA-issuing threads, each with its own accumulators and commit
@@ -699,7 +704,7 @@ __device__ void role_kdeq(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t t
   using Gm = Geo<DT, N>;
   const int q4 = warp & 3, t = q4 * 32 + lane, jb = t >> 4, r = t & 15;
   const uint32_t ta0 = tmem + ((uint32_t)(q4 * 32) << 16) + kColK;
-  uint32_t g = 0, ru[Gm::NRT] = {};   // uses of this row's raw stages
+  uint32_t g = 0, ru[Gm::NRK] = {};   // uses of this row's raw stages
   bool failed = false;
   for (int ii = blockIdx.x; ii < num_items && !failed; ii += gridDim.x) {
     const Item x = load_item(p, ii);
@@ -707,13 +712,13 @@ __device__ void role_kdeq(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t t
     for (int tile = 0; tile < x.ntiles; ++tile) {
       const int nb = min(kTileBlocks, x.n_blk - tile * kTileBlocks);
       const bool have = jb < nb;
-      const uint32_t tp = g % Gm::NRT;
+      const uint32_t tp = g % Gm::NRK;
       const int s = (int)tp * kTileBlocks + jb;
       uint4 qv[N / 4];
       if (tile == 0) load_q<N>(p, x, t, qv);   // in flight while the previous QK finishes
       uint32_t use = 0;
 #pragma unroll
-      for (int i = 0; i < Gm::NRT; ++i)
+      for (int i = 0; i < Gm::NRK; ++i)
         if (i == (int)tp) use = ru[i];
       // K buffer g % 2 is free once QK(g - 2) completed; the q tile of a new
       // item may be written once QK(g - 1), the last of the previous item, is
@@ -721,7 +726,7 @@ __device__ void role_kdeq(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t t
       bool ok = wait_bar(&c.kfree[kb], ((g >> 1) & 1) ^ 1, c, p.hdr);
       if (ok && tile == 0 && g > 0) ok = wait_bar(&c.kfree[kb ^ 1], ((g - 1) >> 1) & 1, c, p.hdr);
       const uint32_t ta = ta0 + kb * 128;
-      if (ok && have) ok = wait_bar(&c.rawfull[s], use & 1, c, p.hdr);
+      if (ok && have) ok = wait_bar(&c.rkfull[s], use & 1, c, p.hdr);
       if (named_sync_or(kBarK, 128, !ok)) {   // the whole group stops together
         failed = true;
         break;
@@ -729,17 +734,17 @@ __device__ void role_kdeq(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t t
       tc_fence_after();
       if (tile == 0) store_q<N>(qv, smem + Gm::OFF_Q, t);
       const int tok = x.t_begin + (tile * kTileBlocks + jb) * kBlock + r;
-      const bool valid = have && c.rvalid[s] != 0 && tok < x.t_end;
-      deq_row<DT, 2>(smem_u32(smem) + tp * Gm::RTILE, jb * Gm::CODE, Gm::R_KS + jb * Gm::SC, r, valid,
+      const bool valid = have && c.rkvalid[s] != 0 && tok < x.t_end;
+      deq_row<DT, 2>(smem_u32(smem) + Gm::OFF_RK + tp * Gm::RSIDE, jb * Gm::CODE, Gm::R_SC + jb * Gm::SC, r, valid,
                   [&](int u, const uint32_t(&h)[16]) { tmem_st16(ta + 16 * u, h); });
       tmem_st_wait();
       if (tile == 0) fence_async_smem();   // Q, written by this thread, for the MMA
       tc_fence_before();
       mbar_arrive(&c.kfull[kb]);
       if (have) {
-        mbar_arrive(&c.rawfree[s]);
+        mbar_arrive(&c.rkfree[s]);
 #pragma unroll
-        for (int i = 0; i < Gm::NRT; ++i)
+        for (int i = 0; i < Gm::NRK; ++i)
           if (i == (int)tp) ++ru[i];
       }
       ++g;
@@ -754,7 +759,7 @@ __device__ void role_vdeq(const AttnParams &p, uint8_t *smem, Ctl &c, int num_it
                           int lane) {
   using Gm = Geo<DT, N>;
   const int t = (warp & 3) * 32 + lane, jb = t >> 4, r = t & 15;
-  uint32_t g = 0, ru[Gm::NRT] = {};   // uses of this row's raw stages
+  uint32_t g = 0, ru[Gm::NRV] = {};   // uses of this row's raw stages
   bool ok = true;
   for (int ii = blockIdx.x; ii < num_items && ok; ii += gridDim.x) {
     const Item x = load_item(p, ii);
@@ -765,21 +770,21 @@ __device__ void role_vdeq(const AttnParams &p, uint8_t *smem, Ctl &c, int num_it
       ok = wait_bar(&c.vfree, (g & 1) ^ 1, c, p.hdr);
       if (!ok) break;
       if (jb < nb) {
-        const uint32_t tp = g % Gm::NRT;
+        const uint32_t tp = g % Gm::NRV;
         const int s = (int)tp * kTileBlocks + jb, vs = jb;
         uint32_t use = 0;
 #pragma unroll
-        for (int i = 0; i < Gm::NRT; ++i)
+        for (int i = 0; i < Gm::NRV; ++i)
           if (i == (int)tp) use = ru[i];
-        ok = wait_bar(&c.rawfull[s], use & 1, c, p.hdr);
+        ok = wait_bar(&c.rvfull[s], use & 1, c, p.hdr);
         if (!ok) break;
 #pragma unroll
-        for (int i = 0; i < Gm::NRT; ++i)
+        for (int i = 0; i < Gm::NRV; ++i)
           if (i == (int)tp) ++ru[i];
         const int tok = x.t_begin + (tile * kTileBlocks + jb) * kBlock + r;
-        const bool valid = c.rvalid[s] != 0 && tok < x.t_end;
+        const bool valid = c.rvvalid[s] != 0 && tok < x.t_end;
         const uint32_t vsl = smem_u32(smem) + Gm::OFF_V + vs * Gm::VSLOT + r * 128;
-        deq_row<DT, 2>(smem_u32(smem) + tp * Gm::RTILE, Gm::R_V + jb * Gm::CODE, Gm::R_VS + jb * Gm::SC,
+        deq_row<DT, 2>(smem_u32(smem) + Gm::OFF_RV + tp * Gm::RSIDE, jb * Gm::CODE, Gm::R_SC + jb * Gm::SC,
                     r, valid, [&](int u, const uint32_t(&h)[16]) {
 #pragma unroll
                       for (int w = 0; w < 4; ++w)
@@ -787,7 +792,7 @@ __device__ void role_vdeq(const AttnParams &p, uint8_t *smem, Ctl &c, int num_it
                                h[4 * w], h[4 * w + 1], h[4 * w + 2], h[4 * w + 3]);
                     });
         fence_async_smem();
-        mbar_arrive(&c.rawfree[s]);
+        mbar_arrive(&c.rvfree[s]);
       }
       mbar_arrive(&c.vfull);   // every V thread, every tile
     }
@@ -1112,9 +1117,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
 #pragma unroll
-    for (int s = 0; s < Gm::NR; ++s) {
-      mbar_init(&c.rawfull[s], 1);
-      mbar_init(&c.rawfree[s], 2 * kBlock);   // 16 K rows + 16 V rows
+    for (int s = 0; s < Gm::NRK * kTileBlocks; ++s) {
+      mbar_init(&c.rkfull[s], 1);
+      mbar_init(&c.rkfree[s], kBlock);   // the block's 16 K rows
+    }
+#pragma unroll
+    for (int s = 0; s < Gm::NRV * kTileBlocks; ++s) {
+      mbar_init(&c.rvfull[s], 1);
+      mbar_init(&c.rvfree[s], kBlock);   // the block's 16 V rows
     }
     mbar_init(&c.vfull, 128);
     mbar_init(&c.ofree, 256);   // both softmax groups
@@ -1146,7 +1156,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (wg == 0) {
     setmaxnreg_to<kLaunchRegs, kRegCtl>();
     if (warp == 0) {
-      if (lane < kTileBlocks) role_producer<DT, N>(p, &tmK, &tmV, smem, c, num_items, lane);
+      if (lane < 2 * kTileBlocks)
+        role_producer<DT, N>(p, &tmK, &tmV, smem, c, num_items, lane & (kTileBlocks - 1),
+                             lane / kTileBlocks);
       __syncwarp();
     } else if (warp == 1) {
       if (lane == 0) role_qk<DT, N>(p, smem, c, tmem, num_items);
