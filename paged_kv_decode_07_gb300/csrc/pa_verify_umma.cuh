@@ -327,8 +327,8 @@ struct Geo {
   // the same consumer threads and no waiter can run two phases ahead of a
   // stage (partial tiles leave stages unused instead of shifting the block
   // -> stage map).  The f16 V of a tile (8 blocks) is handed over as a whole.
-  static constexpr int NRK = DT == PA_KV_NVFP4 ? 3 : 2;   // K tiles in flight
-  static constexpr int NRV = DT == PA_KV_NVFP4 ? 3 : 1;   // V tiles in flight
+  static constexpr int NRK = DT == PA_KV_NVFP4 ? 4 : 2;   // K tiles in flight
+  static constexpr int NRV = DT == PA_KV_NVFP4 ? 2 : 1;   // V tiles in flight
   static constexpr int OFF_RK = 0, OFF_RV = NRK * RSIDE;
   static constexpr int VSLOT = kBlock * D * 2;                   // f16 V of one block
   static constexpr int NV = kTileBlocks;
@@ -340,7 +340,7 @@ struct Geo {
   static constexpr int OFF_P = OFF_Q + QBUF;
   static constexpr int BYTES = OFF_P + 2 * PBUF;
   static constexpr int SMEM = BYTES + 1024;   // + alignment slack
-  static_assert(NRK <= 3 && NRV <= 3, "ring sizes (control block)");
+  static_assert(NRK <= 4 && NRV <= 4, "ring sizes (control block)");
   static_assert(QCH % 1024 == 0 && RSIDE % 1024 == 0 && VSLOT % 1024 == 0 && CODE % 1024 == 0,
                 "1 KB atoms");
   static_assert(SMEM + 4096 <= 227 * 1024, "shared memory (with the static control block)");
@@ -357,7 +357,7 @@ __device__ __forceinline__ uint32_t kmaj_off(int row, int k, int chunk) {
 // ------------------------------------------------------------ shared state
 
 constexpr int kMaxN = 48;
-constexpr int kMaxNR = 24;
+constexpr int kMaxNR = 32;
 
 struct Ctl {
   uint64_t rkfull[kMaxNR], rkfree[kMaxNR];     // K raw stages: TMA -> K dequant
@@ -475,7 +475,7 @@ __device__ void role_producer(const AttnParams &p, const CUtensorMap *tmK, const
   const CUtensorMap *const tm = side ? tmV : tmK;
   const uint8_t *const scales = static_cast<const uint8_t *>(side ? p.kv.vs : p.kv.ks);
   uint8_t *const base = smem + (side ? Gm::OFF_RV : Gm::OFF_RK);
-  uint32_t ruse[3] = {0u, 0u, 0u};   // fills of this lane's stages so far
+  uint32_t ruse[4] = {0u, 0u, 0u, 0u};   // fills of this lane's stages so far
   uint32_t g = 0;
   bool ok = true;
   for (int ii = blockIdx.x; ii < num_items && ok; ii += gridDim.x) {
@@ -492,7 +492,7 @@ __device__ void role_producer(const AttnParams &p, const CUtensorMap *tmK, const
       const int s = stage * kTileBlocks + jt;
       uint32_t use = 0;
 #pragma unroll
-      for (int a = 0; a < 3; ++a)
+      for (int a = 0; a < 4; ++a)
         if (a == stage) use = ruse[a]++;
       if (!wait_bar(&free_[s], (use & 1) ^ 1, c, p.hdr)) {
         ok = false;
@@ -519,7 +519,7 @@ __device__ void role_producer(const AttnParams &p, const CUtensorMap *tmK, const
   // the last fill of each of this lane's stages may still be in flight after
   // a failure: let the copies land before the CTA exits
 #pragma unroll
-  for (int a = 0; a < 3; ++a)
+  for (int a = 0; a < 4; ++a)
     if (ruse[a] > 0) drain_wait(&full[a * kTileBlocks + jt], (ruse[a] - 1) & 1);
 }
 
