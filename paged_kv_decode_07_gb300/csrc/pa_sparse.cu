@@ -129,10 +129,12 @@ __global__ void __launch_bounds__(512) means_kernel(const KvView kv, const int *
   }
 }
 
-// One lane per sparse block: a CTA of 128 threads scores 128 consecutive
-// blocks of one (b, h), walking each block's mean row (contiguous, L1-cached
-// across the float4 steps, eight loads in flight) against the G query rows
-// broadcast from shared memory -- no cross-lane reduction.
+// Eight lanes per sparse block: a CTA of 128 threads scores 128 consecutive
+// blocks of one (b, h), four blocks per warp step.  Lane l8 of a block reads
+// float4 l8, l8 + 8, ... of the block's mean row, so the four blocks of a
+// load instruction are four whole 128-byte lines (coalesced); the G query
+// rows come from shared memory and the eight partial dots of each head are
+// added by three shuffles.
 constexpr int kScoreThreads = 128;
 constexpr int kScoreCta = kScoreThreads;   // blocks per CTA
 
@@ -154,30 +156,46 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(
   __syncthreads();
   const int L = seq_len_of(seq_lens, b, capacity);
   const int nsb = (L + sb - 1) / sb;
-  const int j = c * kScoreCta + threadIdx.x;
-  if (j >= max_nsb) return;
-  float sc = kNegInf;
-  if (j < nsb) {
-    const float4 *m = reinterpret_cast<const float4 *>(means + (((size_t)b * max_nsb + j) * H + h) * D);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane >> 3, l8 = lane & 7;
+  const int per = D / 32;   // float4 of a row per lane
+  for (int step = 0; step < kScoreCta / 16; ++step) {
+    const int j0 = c * kScoreCta + step * 16 + warp * 4;   // the warp's first block
+    if (j0 >= max_nsb) break;                               // the whole warp
+    const int j = j0 + sub;
     float acc[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) acc[g] = 0.f;
-    for (int d0 = 0; d0 < D / 4; d0 += 8) {
+    if (j < nsb) {
+      const float4 *m = reinterpret_cast<const float4 *>(means + (((size_t)b * max_nsb + j) * H + h) * D);
       float4 x[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) x[i] = m[d0 + i];
-#pragma unroll
       for (int i = 0; i < 8; ++i)
+        if (i < per) x[i] = m[l8 + 8 * i];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float4 y = sq[g][d0 + i];
-          acc[g] = fmaf(x[i].x, y.x, fmaf(x[i].y, y.y, fmaf(x[i].z, y.z, fmaf(x[i].w, y.w, acc[g]))));
+      for (int i = 0; i < 8; ++i) {
+        if (i < per) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float4 y = sq[g][l8 + 8 * i];
+            acc[g] = fmaf(x[i].x, y.x, fmaf(x[i].y, y.y, fmaf(x[i].z, y.z, fmaf(x[i].w, y.w, acc[g]))));
+          }
         }
+      }
     }
 #pragma unroll
-    for (int g = 0; g < G; ++g) sc = fmaxf(sc, acc[g]);
+    for (int g = 0; g < G; ++g) {
+      acc[g] += __shfl_xor_sync(0xffffffffu, acc[g], 1);
+      acc[g] += __shfl_xor_sync(0xffffffffu, acc[g], 2);
+      acc[g] += __shfl_xor_sync(0xffffffffu, acc[g], 4);
+    }
+    float sc = kNegInf;
+    if (j < nsb) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) sc = fmaxf(sc, acc[g]);
+    }
+    if (l8 == 0 && j < max_nsb) scores[((size_t)b * H + h) * max_nsb + j] = sc;
   }
-  scores[((size_t)b * H + h) * max_nsb + j] = sc;
 }
 
 // (score, index) -> key ordered like (score descending, index ascending)
