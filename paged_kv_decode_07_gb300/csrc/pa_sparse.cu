@@ -206,12 +206,16 @@ __device__ __forceinline__ unsigned long long sel_key(float s, int j) {
 }
 
 // One CTA of 256 threads per (b, h), each thread holding up to 16
-// (score, index) keys in registers.  The keys are unique, so the top n are
-// exactly the keys >= the n-th largest, which is found bit by bit from the
-// top: keep a bit when at least n keys are >= the prefix with it set (warp
-// ballots, per-warp counts in shared memory, one barrier per bit).  Bits
-// 31..12 are 1 in every key (index < 4096) and are not searched.  A bitmap
-// of the winners gives each one its rank in ascending block order.
+// (score, index) keys in registers as two words (score key, index key).
+// The keys are unique, so the top n are exactly the keys >= the n-th
+// largest, which is found bit by bit from the top: keep a bit when at least
+// n keys are >= the prefix with it set (warp ballots, per-warp counts in
+// shared memory, one barrier per bit).  While the score word is searched
+// the prefix's index word is 0, so comparing score words alone gives the
+// same counts; when exactly n keys then reach the score prefix (no tie at
+// the boundary) it is the answer and the index word is not searched.
+// Index bits 31..12 are 1 in every key (index < 4096) and are not searched.
+// A bitmap of the winners gives each one its rank in ascending block order.
 __global__ void __launch_bounds__(kSelThreads) select_kernel(
     const int *tables, int stride, const int *seq_lens, int B, int H, int sb, int max_nsb,
     int top_k, const float *scores, int *selected, int *vtables, int vstride, int *vlens,
@@ -236,40 +240,52 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   }
   const int n = min(top_k, nsb);
   const float *sc = scores + ((size_t)b * H + h) * max_nsb;
-  unsigned long long key[kPer];
+  uint32_t khi[kPer], klo[kPer];   // score word, index word; 0 / 0 is below every real key
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int j = tid + i * kSelThreads;
-    key[i] = j < nsb ? sel_key(sc[j], j) : 0ull;   // 0 is below every real key
+    const unsigned long long k = j < nsb ? sel_key(sc[j], j) : 0ull;
+    khi[i] = (uint32_t)(k >> 32);
+    klo[i] = (uint32_t)k;
   }
   for (int i = tid; i < 4096 / 32; i += kSelThreads) s_flag[i] = 0;
-  unsigned long long thr = 0;   // the n-th largest key (n < nsb), else 0 = take all
+  // the n-th largest key (n < nsb), else 0 / 0 = take all
+  uint32_t thr_hi = 0, thr_lo = 0;
+  int buf = 0;
+  // keys of the whole CTA for which ge(i) holds (one barrier; the next call
+  // writes the other buffer, so no second barrier is needed)
+  auto count_ge = [&](auto ge) {
+    int cnt = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) cnt += __popc(__ballot_sync(0xffffffffu, ge(i)));
+    if (lane == 0) s_cnt[buf][warp] = cnt;
+    __syncthreads();
+    int tot = 0;
+#pragma unroll
+    for (int w = 0; w < kWarpsSel; ++w) tot += s_cnt[buf][w];
+    buf ^= 1;
+    return tot;
+  };
   if (n < nsb) {
-    int buf = 0;
-    for (int bit = 63; bit >= 0; --bit) {
-      if (bit == 31) {            // index bits 31..12 are set in every key
-        thr |= 0xFFFFF000ull;
-        bit = 12;
-        continue;
+    for (int bit = 31; bit >= 0; --bit) {   // the score word
+      const uint32_t cand = thr_hi | (1u << bit);
+      if (count_ge([&](int i) { return khi[i] >= cand; }) >= n) thr_hi = cand;
+    }
+    if (count_ge([&](int i) { return khi[i] >= thr_hi; }) != n) {   // a tie at the boundary
+      thr_lo = 0xFFFFF000u;
+      for (int bit = 11; bit >= 0; --bit) {   // the index word
+        const uint32_t cand = thr_lo | (1u << bit);
+        if (count_ge([&](int i) { return khi[i] > thr_hi || (khi[i] == thr_hi && klo[i] >= cand); }) >= n)
+          thr_lo = cand;
       }
-      const unsigned long long cand = thr | (1ull << bit);
-      int cnt = 0;
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) cnt += __popc(__ballot_sync(0xffffffffu, key[i] >= cand));
-      if (lane == 0) s_cnt[buf][warp] = cnt;
-      __syncthreads();
-      int tot = 0;
-#pragma unroll
-      for (int w = 0; w < kWarpsSel; ++w) tot += s_cnt[buf][w];
-      if (tot >= n) thr = cand;
-      buf ^= 1;   // the next bit writes the other buffer: no second barrier
     }
   }
   __syncthreads();
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int j = tid + i * kSelThreads;
-    if (j < nsb && key[i] >= thr) atomicOr(&s_flag[j >> 5], 1u << (j & 31));
+    if (j < nsb && (khi[i] > thr_hi || (khi[i] == thr_hi && klo[i] >= thr_lo)))
+      atomicOr(&s_flag[j >> 5], 1u << (j & 31));
   }
   __syncthreads();
   if (warp == 0) {   // exclusive prefix of the bitmap's word counts
