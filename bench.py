@@ -22,6 +22,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -67,13 +68,23 @@ def measured_peaks():
         return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
 
 
+def code_only(text: str) -> str:
+    """C++ / CUDA source without its comments and with runs of white space
+    collapsed: what the compiled kernel depends on."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(files=None) -> str:
-    """sha256 prefix over the named files of csrc/ (default: all of them)."""
+    """sha256 prefix over the code (comments and white space aside) of the
+    named files of csrc/ (default: all of them).  A profile summary records it;
+    an edit to the code makes the summary stale, an edit to a comment does not."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_07_gb300", "csrc")
     for f in sorted(files or os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode() + code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

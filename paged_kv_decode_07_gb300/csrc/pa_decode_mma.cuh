@@ -1,6 +1,7 @@
 // pa_decode_mma.cuh -- split-K paged decode attention on the tensor cores
-// (mma.sync m16n8k16, f16 operands, fp32 accumulation) for the int8,
-// NVFP4 and FP8-E4M3 KV formats.
+// (mma.sync m16n8k16, fp32 accumulation) for every KV format: f16 operands
+// dequantised from the int8, NVFP4 and FP8-E4M3 codes, bf16 operands read
+// straight from bf16 KV.
 //
 // Why tensor cores for decode: with GQA the G query heads of one kv head
 // share every key and value, so per (token, kv head) the scores and the PV
@@ -12,7 +13,8 @@
 //
 // Work split is the CUDA-core kernel's (one CTA of 4 warps per work item,
 // each warp streams whole 16-token blocks through its own ring of shared
-// memory stages filled by 1-D bulk copies).  Per block a warp computes
+// memory stages filled by 2-D TMA, or by 1-D bulk copies where a row is not
+// a multiple of 128 bytes).  Per block a warp computes
 //   S^T [16 tokens x 8 heads] = K [16 x D] . Q^T [D x 8]      (M = tokens)
 //   O^T [D x 8 heads]        += V^T [D x 16] . P^T [16 x 8]   (M = head dim)
 // with G <= 8 query heads in the N = 8 columns.  Operand fragments are
@@ -24,7 +26,10 @@
 // contiguous bytes of a key row and the query fragments use the same
 // permuted head-dim order; for PV the head-dim rows are permuted the same
 // way and un-permuted when the output is written.  The scores' fragment
-// layout is turned into PV's B fragment with 8 shuffles per block.
+// layout is turned into PV's B fragment by one movmatrix transpose per 8
+// tokens.  bf16 KV skips the dequant: K and V^T fragments come from the
+// swizzled tiles by ldmatrix (.trans for V, natural head-dim order), q is
+// used as bf16 and P enters PV as a bf16 hi + lo pair.
 // Scales: int8 per-token scales multiply the score (K) and the
 // probability (V); the NVFP4 block scale multiplies the f16 codes (one
 // exact f16x2 multiply per pair); softmax_scale * log2 e and the NVFP4 /
