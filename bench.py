@@ -2,18 +2,23 @@
 """Benchmark of paged-KV decode attention on GB300.
 
 One step = one pa_decode call (device planner -> attention kernel -> LSE
-merge) over one batch of the synthetic int8 workload: 32 sequences with
-seq_lens uniform in [1024, 32768], 24 query / 4 kv heads, head dim 256,
-int8 KV with per-(token, kv head) fp16 scales, blocks drawn at random from
-a shared pool, bf16 q and out.  Inputs are resident in HBM when timing
-starts; the KV pool (~1.1 GB) is larger than the 129 MB L2, so every step
-streams it from HBM.
+merge) over one batch of the largest synthetic workload: the skewed
+continuous batch of 256 sequences with seq_lens log-uniform in [16,
+131072] (about 3.7 M keys), 24 query / 4 kv heads, head dim 256, bf16 KV
+whose blocks are interleaved across sequences in one pool (append order),
+bf16 q and out.  Inputs are resident in HBM when timing starts; the KV pool
+(~15 GB) is far larger than the 129 MB L2, so every step streams it from
+HBM.
 
 Prints ONE JSON line (rank 0).  Metric: achieved algorithmic HBM GB/s
 (KV codes + scales of every valid token, table entries, q and out, divided
 by the step time), with KV tokens/s and % of the measured copy bandwidth
-beside it.  `--impl reference` times the fp64 CPU oracle on a bounded
-sample of the same workload instead (the baseline arm).
+beside it.  The same line carries `per_config`: every other workload of
+the problem statement (the 1 MB bf16 case, the int8 1K-32K batch, the
+NVFP4 262K decode, the NVFP4 8-token verify and the FP8 decode / verify)
+timed the same way, each with its kernel time, step time, µs per call and
+roofline fraction.  `--impl reference` times the fp64 CPU oracle on a
+bounded sample of the headline workload instead (the baseline arm).
 """
 from __future__ import annotations
 
@@ -33,7 +38,15 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "int8_b32_l1k_32k_d256"
+DEFAULT_WORKLOAD = "bf16_skewed_b256_l16_128k_d256"
+# the other workloads timed on the same line (`per_config`)
+PER_CONFIG = ("bf16_b1_l1000_d128", "int8_b32_l1k_32k_d256", "nvfp4_b4_l262k_d256",
+              "nvfp4_verify_q8_b4_ctx64k_d256", "fp8_b32_l1k_32k_d256",
+              "fp8_verify_q8_b4_ctx64k_d256")
+L2_BYTES = 129 << 20
+# pools smaller than this are rotated over copies whose total exceeds it, so
+# that every call reads its KV from HBM rather than from L2
+ROTATE_TOTAL_BYTES = 2 * L2_BYTES
 METRIC = "paged decode attention: achieved HBM GB/s (% of peak) and KV tokens/s, 1×GB300"
 FALLBACK_HBM_GBS = 6800.0
 
@@ -545,7 +558,130 @@ def run_ours(args, world, rank, local):
         }
         if wo_info:
             line["wo"] = wo_info
+        if world == 1 and not args.no_per_config and args.op == "decode" and not sparse:
+            del wl, kv, ws, out
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+            line["per_config"] = [time_config(n, args, dev, peak, peak_kind)
+                                  for n in PER_CONFIG if n != args.workload]
         print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------- other workloads
+
+def _pool_bytes(kv) -> int:
+    return sum(t.numel() * t.element_size()
+               for t in (kv.k_cache, kv.v_cache, kv.k_scale, kv.v_scale) if t is not None)
+
+
+def time_config(name, args, dev, peak, peak_kind):
+    """Times one workload the way the headline is timed (steps back to back
+    with CUDA events around all of them; the attention kernel alone with
+    events recorded on its stream by the library) and returns its
+    `per_config` entry.  Pools smaller than twice the L2 are rotated over
+    copies, one per call, so that every call reads its KV from HBM; for them
+    the device time per call is also taken from a CUDA graph of one call per
+    copy, replayed (what a serving loop that captures its decode step pays)."""
+    import torch
+
+    from paged_kv_decode_07_gb300 import pa
+    from paged_kv_decode_07_gb300 import workloads as W
+    spec = W.spec(name)
+    wl = W.make_workload(name, device=dev)
+    kv0 = pa.KvCache.from_workload(wl)
+    lens = wl.seq_lens.cpu().tolist()
+    ab = algorithmic_bytes(dict(spec, B_eff=wl.B), lens)
+    pool = _pool_bytes(kv0)
+    ncopy = 1 if pool >= ROTATE_TOTAL_BYTES else -(-ROTATE_TOTAL_BYTES // pool)
+    kvs = [kv0] + [pa.KvCache(kv0.dtype, kv0.k_cache.clone(), kv0.v_cache.clone(),
+                              None if kv0.k_scale is None else kv0.k_scale.clone(),
+                              None if kv0.v_scale is None else kv0.v_scale.clone(),
+                              kv0.k_global, kv0.v_global) for _ in range(ncopy - 1)]
+    call = pa.verify if wl.Q > 1 else pa.decode
+    out = torch.empty((wl.B, wl.Q, wl.Hq, wl.D), dtype=torch.bfloat16, device=dev)
+    maxlen = wl.max_seq_len()
+    ws = torch.empty(pa.workspace_bytes(kvs[0], wl.B, wl.Q, wl.Hq, maxlen), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i, events=None):
+        call(kvs[i % ncopy], wl.q, wl.block_tables, wl.seq_lens, wl.softmax_scale, out=out,
+             max_seq_len=maxlen, workspace=ws, events=events)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    flags = pa.read_error(ws)
+    if flags:
+        raise RuntimeError(f"{name}: device error flags {flags:#x}")
+    steps = max(args.steps, ncopy) if ncopy > 1 else args.steps
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(steps):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms_step = t0.elapsed_time(t1) / steps
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in kev:
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        step(i, events=kev[i])
+    torch.cuda.synchronize()
+    kern_ms = sum(a.elapsed_time(b) for a, b in kev) / steps
+    entry = {
+        "workload": name, "kv_dtype": wl.dtype, "batch": wl.B, "q_len": wl.Q,
+        "kv_tokens": ab["tokens"], "algorithmic_bytes": ab["total"],
+        "kernel_ms": kern_ms, "achieved_gbs": ab["total"] / (kern_ms * 1e-3) / 1e9,
+        "frac": ab["total"] / (kern_ms * 1e-3) / 1e9 / peak, "peak_gbs": peak,
+        "peak_kind": peak_kind,
+        "step_ms": ms_step, "us_per_call": ms_step * 1e3,
+        "step_gbs": ab["total"] / (ms_step * 1e-3) / 1e9,
+        "kv_tokens_per_s": ab["tokens"] / (ms_step * 1e-3),
+        "traffic": profiled_traffic(name),
+        "l2": ("inputs larger than L2 (KV pool %.2f GB)" % (pool / 1e9)) if ncopy == 1 else
+              ("%d pool copies of %.2f MB rotated, one per call (%.0f MB > L2)"
+               % (ncopy, pool / 1e6, ncopy * pool / 1e6)),
+    }
+    if wl.Q > 1:
+        flop = 0
+        for L in lens:   # QK and PV over the keys each query row sees
+            flop += sum(4 * wl.Hq * wl.D * (L - wl.Q + 1 + i) for i in range(wl.Q))
+        entry["tflops"] = flop / (kern_ms * 1e-3) / 1e12
+    if ncopy > 1:
+        # one graph of one call per pool copy, replayed: device time per call
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step(0)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            for i in range(ncopy):
+                step(i)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        reps = max(1, args.steps // 4)
+        t0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        entry["us_per_call_graph"] = t0.elapsed_time(t1) * 1e3 / (reps * ncopy)
+        entry["us_per_call"] = entry["us_per_call_graph"]
+        entry["us_per_call_eager"] = ms_step * 1e3
+        del g
+    del kvs, kv0, wl, ws, out
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return entry
 
 
 # ------------------------------------------------------------- KV append
@@ -709,6 +845,8 @@ def main():
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only the headline workload")
     ap.add_argument("--ref-tokens", type=int, default=60000,
                     help="keys in the oracle's bounded sample")
     ap.add_argument("--cpu-tokens", type=int, default=1 << 40,

@@ -167,14 +167,17 @@ int pa_decode(const pa_kv_cache *kv, const pa_problem *prob, const pa_options *o
  * fixed device array of PA_NOALLOC_SCRATCH_BYTES inside the library, held
  * by every GPU that loads it until the process exits; nothing is allocated
  * per call.  The PagedAttention paper has no counterpart to this entry
- * point.  Same arguments, semantics and results as pa_decode with default
- * options.  Returns PA_ERR_WORKSPACE_TOO_SMALL, with nothing launched, when
- * the call would need more workspace than PA_NOALLOC_SCRATCH_BYTES (about
- * (2 * batch + 300) * Hkv * G * D * 4 bytes for the default plan).  The
- * first call on each device (with that device current) looks up the
- * array's device address; make that first call before any stream capture.
- * All calls share the array: calls that can overlap on the GPU race.  The
- * device error flags of these calls cannot be read back. */
+ * point.  Same arguments, semantics, status codes and results as pa_decode
+ * with default options.  Returns PA_ERR_WORKSPACE_TOO_SMALL, with nothing
+ * launched, when the call would need more workspace than
+ * PA_NOALLOC_SCRATCH_BYTES (about (2 * batch + 300) * Hkv * G * D * 4 bytes
+ * for the default plan).  The first call on each device (with that device
+ * current) looks up the array's device address and keeps it; make that
+ * first call before any stream capture.  The kept address is that of the
+ * device's current primary context: after cudaDeviceReset, do not call this
+ * entry point on that device again in the same process.  All calls share
+ * the array: calls that can overlap on the GPU race.  The device error
+ * flags of these calls cannot be read back. */
 #define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
 int pa_decode_noalloc(const pa_kv_cache *kv, const pa_problem *prob, pa_stream_t stream);
 

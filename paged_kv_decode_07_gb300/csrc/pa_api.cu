@@ -267,7 +267,7 @@ int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *
   // auto target: about 8 items per SM for the one-CTA-per-item kernels; the
   // persistent tcgen05 verify kernel pays a fixed cost per item (its q tile,
   // epilogue and first-tile rescale), so it gets about 2 per SM
-  int auto_target = 1184;
+  int auto_target = kDefaultTargetItems;
   if (umma) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) == cudaSuccess &&

@@ -18,6 +18,9 @@ constexpr int kMaxG = 8;              // query heads per kv head handled in one 
 constexpr int kMaxQLen = 16;
 constexpr int kHdrWords = 64;         // 256-byte workspace header
 constexpr int kMaxTargetItems = 4096;
+// work items the planner aims at when the caller names no target: about 8
+// per SM for the one-CTA-per-item decode kernels
+constexpr int kDefaultTargetItems = 1184;
 constexpr uint32_t kWaitCap = 1u << 22;   // iteration cap of every in-kernel wait
 constexpr float kNegInf = -__builtin_huge_valf();
 

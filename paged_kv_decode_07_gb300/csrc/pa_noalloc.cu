@@ -14,8 +14,11 @@
 // name is only a stand-in for the device symbol.  The first call on each
 // device (with that device current) resolves the real device address with
 // cudaGetSymbolAddress and caches it; that first call should therefore come
-// before any stream capture.  No call allocates: no cudaMalloc, no
-// cudaFree, no allocating library routine.
+// before any stream capture.  The cached address belongs to the device's
+// current primary context: after cudaDeviceReset (or any teardown of that
+// context) the module is loaded afresh at another address, so a process
+// that resets a device must not call this entry point on it again.  No call
+// allocates: no cudaMalloc, no cudaFree, no allocating library routine.
 //
 // All calls share the one array and it keeps the previous call's contents.
 // Nothing in it has to start at zero (the planner rewrites the header, the
@@ -30,7 +33,6 @@ namespace {
 
 constexpr size_t kScratchBytes = PA_NOALLOC_SCRATCH_BYTES;
 constexpr int kMaxDevices = 64;
-constexpr int kDefaultTargetItems = 1184;   // the planner's own default target
 
 static __device__ __align__(256) uint8_t g_scratch[kScratchBytes];
 
@@ -58,12 +60,11 @@ extern "C" int pa_decode_noalloc(const pa_kv_cache *kv, const pa_problem *prob,
   pa_options opt;
   opt.kernel = 0;
   opt.split_blocks = 0;
-  opt.target_items = kDefaultTargetItems;
+  opt.target_items = pa::kDefaultTargetItems;
   opt.event_begin = nullptr;
   opt.event_end = nullptr;
-  const size_t need = pa_workspace_bytes(kv, prob, &opt);
-  if (need == 0) return PA_ERR_INVALID_ARG;
-  if (need > kScratchBytes) return PA_ERR_WORKSPACE_TOO_SMALL;
+  // pa_decode validates the arguments and the workspace size (returning its
+  // own status codes, with nothing launched, when either is wrong)
   void *ws = nullptr;
   const int st = scratch_address(&ws);
   if (st != PA_OK) return st;
