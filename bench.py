@@ -343,7 +343,8 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", torch.cuda.current_device())
     spec = W.spec(args.workload)
     # weak scaling: every rank runs its own full batch (different seed)
-    wl = W.make_workload(args.workload, device=dev, seed=1000 + spec["id"] + 7919 * rank)
+    wl = W.make_workload(args.workload, device=dev, seed=1000 + spec["id"] + 7919 * rank,
+                         B=args.batch or None)
     kv = pa.KvCache.from_workload(wl)
     lens = wl.seq_lens.cpu().tolist()
     sp = dict(spec, B_eff=wl.B)
@@ -558,6 +559,8 @@ def run_ours(args, world, rank, local):
         }
         if wo_info:
             line["wo"] = wo_info
+        if args.batch:
+            line["config"]["batch_override"] = args.batch
         if world == 1 and not args.no_per_config and args.op == "decode" and not sparse:
             del wl, kv, ws, out
             torch.cuda.synchronize()
@@ -847,6 +850,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="time only the headline workload")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="sequences of the headline workload (default: its recipe's; a smaller "
+                         "batch of the same distribution is for profiling captures)")
     ap.add_argument("--ref-tokens", type=int, default=60000,
                     help="keys in the oracle's bounded sample")
     ap.add_argument("--cpu-tokens", type=int, default=1 << 40,

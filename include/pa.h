@@ -146,7 +146,18 @@ typedef struct pa_options {
   void *event_begin;       /* optional cudaEvent_t recorded just before the attention
                               kernel (after the planner) -- for timing that kernel */
   void *event_end;         /* optional cudaEvent_t recorded just after it */
+  int32_t test_flags;      /* 0 normally.  PA_TEST_EXPIRE_WAIT (tensor-core decode,
+                              kernel 2 or auto decode; else PA_ERR_UNSUPPORTED): every warp
+                              of the attention kernel withholds the copy of its first KV
+                              block, so its wait for that block runs out after a short cap
+                              (about a thousand polls); the kernel then records
+                              PA_ERRF_WAIT_TIMEOUT, lets the copies it did issue land and
+                              returns.  The outputs of such a call are meaningless.  It
+                              exercises the capped-wait failure path without faulting or
+                              hanging the GPU.  Other bits: PA_ERR_INVALID_ARG. */
 } pa_options;
+
+#define PA_TEST_EXPIRE_WAIT 0x1
 
 /* Bytes of device workspace a pa_decode / pa_verify call with these
  * arguments needs (an upper bound computed from batch, q_len, heads and

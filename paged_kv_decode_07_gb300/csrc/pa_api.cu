@@ -219,6 +219,8 @@ int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *
   const int kernel = o ? o->kernel : 0;
   if (kernel < 0 || kernel > 4) return PA_ERR_INVALID_ARG;
   if (o && (o->split_blocks < 0 || o->target_items < 0)) return PA_ERR_INVALID_ARG;
+  const int test_flags = o ? o->test_flags : 0;
+  if (test_flags & ~PA_TEST_EXPIRE_WAIT) return PA_ERR_INVALID_ARG;
   if (p->batch == 0) return PA_OK;
   const int G = p->num_q_heads / kv->num_kv_heads;
   // Kernel choice.  auto: tensor cores (the CUDA cores cannot issue the
@@ -247,6 +249,8 @@ int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *
     // 0.192 vs 0.304 ms, FP8 0.295 vs 0.298 ms for the mma.sync tiles)
     umma = dense && umma_supported(kv->dtype, kv->head_dim, Q);
   }
+  // the expired-wait test mode is built into the tensor-core decode kernel only
+  if ((test_flags & PA_TEST_EXPIRE_WAIT) && !(use_tc && !dense && !umma)) return PA_ERR_UNSUPPORTED;
   const int mode = dense ? 2 : 1;   // dense verify runs as row groups of up to 48 rows
   const int RG = dense ? row_groups(Q, G) : 1;
   if (!ws) return PA_ERR_INVALID_ARG;
@@ -312,6 +316,7 @@ int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *
   ap.virt = mode;
   ap.RG = RG;
   ap.R = L.R;
+  ap.test_expire = (test_flags & PA_TEST_EXPIRE_WAIT) ? 1 : 0;
 
   if (launch_plan(pp, stream) != cudaSuccess) return PA_ERR_CUDA;
   if (o && o->event_begin &&

@@ -321,8 +321,16 @@ __global__ void __launch_bounds__(kThreads, 3)
   int tab_cache = -1, tab_chunk = -1;
   uint32_t valid_bits = 0;
   bool failed = false;
+  // test mode (PA_TEST_EXPIRE_WAIT): the copy of each warp's first block is
+  // never issued, so the wait for it runs out after kTestWaitCap polls
+  const bool withhold = p.test_expire != 0;
+  const uint32_t wait_cap = withhold ? kTestWaitCap : kWaitCap;
 
   auto issue = [&](int j) {
+    if (withhold && j == 0) {   // warp-uniform: nothing issued, nothing arrives
+      valid_bits &= ~1u;
+      return;
+    }
     const int chunk = j >> 5;
     if (chunk != tab_chunk) {
       const int jj = chunk * 32 + lane;
@@ -379,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 3)
 
   for (int j = 0; j < n_local; ++j) {
     const int s = j % NSTAGE;
-    const bool arrived = mbar_wait(&bars[warp][s], (j / NSTAGE) & 1);
+    const bool arrived = mbar_wait(&bars[warp][s], (j / NSTAGE) & 1, wait_cap);
     if (!__all_sync(0xffffffffu, arrived)) {
       failed = true;
       if (lane == 0) set_err(p.hdr, PA_ERRF_WAIT_TIMEOUT);
@@ -658,7 +666,12 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
   }
   if (failed) {
-    for (int j = 0; j < issued; ++j) (void)mbar_wait(&bars[warp][j % NSTAGE], (j / NSTAGE) & 1);
+    // let every copy this warp issued land before the CTA exits.  Only the
+    // last fill of each stage can still be in flight (a stage is refilled
+    // after its previous fill was consumed), and only its phase may be
+    // waited on: an older phase's parity repeats and would read as pending.
+    for (int j = max(issued - NSTAGE, withhold ? 1 : 0); j < issued; ++j)
+      (void)mbar_wait(&bars[warp][j % NSTAGE], (j / NSTAGE) & 1);
   }
 
   // ---- per-warp totals

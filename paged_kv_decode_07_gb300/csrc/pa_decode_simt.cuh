@@ -411,7 +411,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p)
     }
   }
   if (failed) {   // let copies still in flight land before the stages are reused
-    for (int j = 0; j < issued; ++j) (void)mbar_wait(&bars[warp][j % NSTAGE], (j / NSTAGE) & 1);
+    // (only the last fill of each stage can be in flight; an older phase's
+    // parity repeats and would read as pending)
+    for (int j = max(issued - NSTAGE, 0); j < issued; ++j)
+      (void)mbar_wait(&bars[warp][j % NSTAGE], (j / NSTAGE) & 1);
   }
 
   // ---- per-warp totals: l over lanes, o over row groups

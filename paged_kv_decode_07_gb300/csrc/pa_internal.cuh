@@ -22,6 +22,7 @@ constexpr int kMaxTargetItems = 4096;
 // per SM for the one-CTA-per-item decode kernels
 constexpr int kDefaultTargetItems = 1184;
 constexpr uint32_t kWaitCap = 1u << 22;   // iteration cap of every in-kernel wait
+constexpr uint32_t kTestWaitCap = 1u << 10;   // cap of the waits a PA_TEST_EXPIRE_WAIT call expires
 constexpr float kNegInf = -__builtin_huge_valf();
 
 // workspace header words
@@ -80,6 +81,7 @@ struct AttnParams {
   int virt;                 // plan mode: 1 virtual, 0 dense, 2 row groups
   int R;                    // rows per item: G (virtual), Q*G (dense), rows per group (mode 2)
   int RG;                   // row groups per sequence (mode 2), else 1
+  int test_expire;          // PA_TEST_EXPIRE_WAIT: first copies withheld, short wait cap
 };
 
 struct PlanParams {
@@ -133,8 +135,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // bounded wait; false if the cap was hit
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitCap; ++i)
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          uint32_t cap = kWaitCap) {
+  for (uint32_t i = 0; i < cap; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }

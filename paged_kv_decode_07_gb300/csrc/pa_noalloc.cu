@@ -63,6 +63,7 @@ extern "C" int pa_decode_noalloc(const pa_kv_cache *kv, const pa_problem *prob,
   opt.target_items = pa::kDefaultTargetItems;
   opt.event_begin = nullptr;
   opt.event_end = nullptr;
+  opt.test_flags = 0;
   // pa_decode validates the arguments and the workspace size (returning its
   // own status codes, with nothing launched, when either is wrong)
   void *ws = nullptr;

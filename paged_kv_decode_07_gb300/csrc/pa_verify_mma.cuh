@@ -428,8 +428,9 @@ __global__ void __launch_bounds__(kThreads, NT == 2 ? 4 : 2)
     // block j+1's B1 orders these reads of stage s and of P before stage s is
     // refilled and before P is rewritten
   }
-  if (s_fail && tid == 0) {
-    for (int j = 0; j < issued; ++j) (void)mbar_wait(&bars[j % NSTAGE], (j / NSTAGE) & 1);
+  if (s_fail && tid == 0) {   // only the last fill of each stage can be in flight
+    for (int j = max(issued - NSTAGE, 0); j < issued; ++j)
+      (void)mbar_wait(&bars[j % NSTAGE], (j / NSTAGE) & 1);
   }
 
   // ---- finish: row sums and max per column, then O / l

@@ -493,11 +493,16 @@ __device__ void role_producer(const AttnParams &p, const CUtensorMap *tmK, const
       uint32_t use = 0;
 #pragma unroll
       for (int a = 0; a < 4; ++a)
-        if (a == stage) use = ruse[a]++;
+        if (a == stage) use = ruse[a];
       if (!wait_bar(&free_[s], (use & 1) ^ 1, c, p.hdr)) {
         ok = false;
         break;
       }
+      // counted once the stage is this lane's to fill: the drain below waits
+      // for the phase of the last fill actually issued
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+        if (a == stage) ++ruse[a];
       const bool v = phys >= 0 && phys < p.kv.num_blocks;
       rvalid[s] = v;
       if (!v) {

@@ -35,6 +35,8 @@ PA_ERRF_WAIT_TIMEOUT = 0x10
 PA_ERRF_PLAN_OVERFLOW = 0x20
 PA_ERRF_BAD_SLOT = 0x40
 
+PA_TEST_EXPIRE_WAIT = 0x1
+
 EXPORTED = ("pa_workspace_bytes", "pa_decode", "pa_verify", "pa_merge", "pa_dequant_gather",
             "pa_append_kv", "pa_block_means", "pa_sparse_workspace_bytes", "pa_decode_sparse",
             "pa_decode_wo_workspace_bytes", "pa_decode_wo",
@@ -79,7 +81,7 @@ class _Wo(ctypes.Structure):
 class _Options(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("split_blocks", ctypes.c_int32),
                 ("target_items", ctypes.c_int32), ("event_begin", ctypes.c_void_p),
-                ("event_end", ctypes.c_void_p)]
+                ("event_end", ctypes.c_void_p), ("test_flags", ctypes.c_int32)]
 
 
 _lib = None
@@ -176,12 +178,12 @@ class KvCache:
                         float(self.v_global))
 
 
-def _options(kernel=0, split_blocks=0, target_items=0, events=None):
+def _options(kernel=0, split_blocks=0, target_items=0, events=None, test_flags=0):
     eb = ee = None
     if events is not None:
         eb = ctypes.c_void_p(events[0].cuda_event)
         ee = ctypes.c_void_p(events[1].cuda_event)
-    return _Options(int(kernel), int(split_blocks), int(target_items), eb, ee)
+    return _Options(int(kernel), int(split_blocks), int(target_items), eb, ee, int(test_flags))
 
 
 def _problem(kv: KvCache, q, block_tables, seq_lens, softmax_scale, out, lse, max_seq_len):
@@ -201,7 +203,7 @@ def workspace_bytes(kv: KvCache, batch: int, q_len: int, num_q_heads: int, max_s
 
 def _attend(fn_name, kv, q, block_tables, seq_lens, softmax_scale, *, out=None, out_fp32=False,
             return_lse=False, max_seq_len=None, workspace=None, kernel=0, split_blocks=0,
-            target_items=0, events=None, stream=None):
+            target_items=0, events=None, stream=None, test_flags=0):
     B, Q, Hq, D = q.shape
     if out is None:
         out = torch.empty((B, Q, Hq, D), dtype=torch.float32 if out_fp32 else torch.bfloat16,
@@ -209,7 +211,7 @@ def _attend(fn_name, kv, q, block_tables, seq_lens, softmax_scale, *, out=None, 
     lse = torch.empty((B, Q, Hq), dtype=torch.float32, device=q.device) if return_lse else None
     if max_seq_len is None:
         max_seq_len = int(block_tables.shape[1]) * kv.block_size
-    opts = _options(kernel, split_blocks, target_items, events)
+    opts = _options(kernel, split_blocks, target_items, events, test_flags)
     kvs = kv.struct()
     prob = _problem(kv, q, block_tables, seq_lens, softmax_scale, out, lse, max_seq_len)
     need = int(lib().pa_workspace_bytes(ctypes.byref(kvs), ctypes.byref(prob), ctypes.byref(opts)))

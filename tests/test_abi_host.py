@@ -188,3 +188,17 @@ def test_wo_argument_checks(L):
                           1 << 30, None) == pa.PA_ERR_INVALID_ARG
     assert L.pa_decode_wo(ctypes.byref(kv), ctypes.byref(p), ctypes.byref(wo), None, F, 64,
                           None) == pa.PA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_test_flags_are_checked_on_the_host(L):
+    """PA_TEST_EXPIRE_WAIT is built into the tensor-core decode kernel only;
+    other kernels and unknown bits are refused before anything is launched."""
+    def opts(kernel, flags):
+        return pa._Options(kernel, 0, 0, None, None, flags)
+    assert call(L, "pa_decode", kv_struct(), prob_struct(), opts=opts(0, 0x2)) == pa.PA_ERR_INVALID_ARG
+    assert call(L, "pa_decode", kv_struct(), prob_struct(),
+                opts=opts(1, pa.PA_TEST_EXPIRE_WAIT)) == pa.PA_ERR_UNSUPPORTED
+    assert call(L, "pa_verify", kv_struct(dtype=2), prob_struct(Q=8),
+                opts=opts(0, pa.PA_TEST_EXPIRE_WAIT)) == pa.PA_ERR_UNSUPPORTED    # tcgen05 verify
+    assert call(L, "pa_verify", kv_struct(dtype=1), prob_struct(Q=8),
+                opts=opts(2, pa.PA_TEST_EXPIRE_WAIT)) == pa.PA_ERR_UNSUPPORTED    # dense tiles
