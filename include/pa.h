@@ -127,7 +127,7 @@ typedef struct pa_problem {
 
 /* Optional knobs; pass NULL for defaults. */
 typedef struct pa_options {
-  int32_t kernel;          /* 0 auto: decode (every format) -> 2;
+  int32_t kernel;          /* 0 auto: decode (every format) -> 2, or 5 for a small problem;
                               int8 verify (head_dim 256) -> 2 (dense tiles);
                               bf16 verify -> 2 (one unit per query token);
                               NVFP4 / FP8 verify (head_dim 256) -> 4.
@@ -138,7 +138,13 @@ typedef struct pa_options {
                               tensor-core kernel with verify run as one unit per query
                               token; 4 verify on the tcgen05 tensor cores (accumulators
                               in tensor memory; NVFP4 / FP8, head_dim 256, q_len > 1;
-                              else PA_ERR_UNSUPPORTED) */
+                              else PA_ERR_UNSUPPORTED); 5 single-launch decode (pa_decode
+                              only): one cluster of up to 8 CTAs per (sequence, kv head),
+                              no planner and no merge kernel, the partials merged in
+                              distributed shared memory; auto mode picks it when every
+                              sequence has at most 1,024 keys (max_seq_len) and batch x
+                              kv heads x cluster size <= 148.  It uses only the first
+                              256 bytes of the workspace. */
   int32_t split_blocks;    /* 0 auto; >0 = fixed number of 16-token blocks per partition
                               (a value >= the longest sequence's block count disables
                               split-K) */

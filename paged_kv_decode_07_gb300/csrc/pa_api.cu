@@ -17,6 +17,23 @@ cudaError_t launch_decode_tc_int8(const AttnParams &p, int grid, cudaStream_t s)
 cudaError_t launch_decode_tc_nvfp4(const AttnParams &p, int grid, cudaStream_t s);
 cudaError_t launch_decode_tc_fp8(const AttnParams &p, int grid, cudaStream_t s);
 
+cudaError_t launch_decode_tc_cluster_bf16(const AttnParams &p, int P, cudaStream_t s);
+cudaError_t launch_decode_tc_cluster_int8(const AttnParams &p, int P, cudaStream_t s);
+cudaError_t launch_decode_tc_cluster_nvfp4(const AttnParams &p, int P, cudaStream_t s);
+cudaError_t launch_decode_tc_cluster_fp8(const AttnParams &p, int P, cudaStream_t s);
+
+// the single-launch decode: one thread-block cluster of P CTAs per
+// (sequence, kv head), partials merged in distributed shared memory
+cudaError_t launch_decode_tc_cluster(const AttnParams &p, int P, cudaStream_t s) {
+  switch (p.kv.dtype) {
+    case PA_KV_BF16: return launch_decode_tc_cluster_bf16(p, P, s);
+    case PA_KV_INT8: return launch_decode_tc_cluster_int8(p, P, s);
+    case PA_KV_NVFP4: return launch_decode_tc_cluster_nvfp4(p, P, s);
+    case PA_KV_FP8: return launch_decode_tc_cluster_fp8(p, P, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_decode_tc(const AttnParams &p, int grid, cudaStream_t s) {
   switch (p.kv.dtype) {
     case PA_KV_BF16: return launch_decode_tc_bf16(p, grid, s);
@@ -91,6 +108,12 @@ namespace {
 
 constexpr int kVersion = 100;
 constexpr int kMinSplitBlocks = 8;       // partitions never shorter than 128 tokens (auto mode)
+// single-launch decode: at most 8 CTAs per cluster (the portable limit), a
+// CTA's 4 warps taking up to 2 blocks each in auto mode, and the whole grid
+// resident at once (one CTA per SM)
+constexpr int kClusterMax = 8;
+constexpr int kClusterBlocksPerCta = 8;
+constexpr int kClusterMaxCtas = 148;
 constexpr size_t kAlign = 256;
 
 size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -217,7 +240,7 @@ int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *
   st = check_problem(kv, p, verify ? kMaxQLen : 1);
   if (st) return st;
   const int kernel = o ? o->kernel : 0;
-  if (kernel < 0 || kernel > 4) return PA_ERR_INVALID_ARG;
+  if (kernel < 0 || kernel > 5) return PA_ERR_INVALID_ARG;
   if (o && (o->split_blocks < 0 || o->target_items < 0)) return PA_ERR_INVALID_ARG;
   const int test_flags = o ? o->test_flags : 0;
   if (test_flags & ~PA_TEST_EXPIRE_WAIT) return PA_ERR_INVALID_ARG;
@@ -229,8 +252,12 @@ int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *
   // runs as one dense tile of q_len * G rows when supported; otherwise every
   // kernel runs it as a virtual batch (one unit per query token).
   const int Q = p->q_len;
-  bool use_tc, dense = false, umma = false;
-  if (kernel == 4) {
+  bool use_tc, dense = false, umma = false, single = false;
+  if (kernel == 5) {
+    if (verify || Q != 1 || !tc_supported(kv->dtype, kv->head_dim, G) || extra_err)
+      return PA_ERR_UNSUPPORTED;
+    use_tc = single = true;
+  } else if (kernel == 4) {
     if (!umma_supported(kv->dtype, kv->head_dim, Q) || !tc_supported(kv->dtype, kv->head_dim, G))
       return PA_ERR_UNSUPPORTED;
     use_tc = dense = umma = true;
@@ -249,8 +276,54 @@ int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *
     // 0.192 vs 0.304 ms, FP8 0.295 vs 0.298 ms for the mma.sync tiles)
     umma = dense && umma_supported(kv->dtype, kv->head_dim, Q);
   }
+  // single-launch decode for small problems (auto mode): every sequence's
+  // blocks fit 8 per CTA of a cluster of at most 8, and all clusters run at
+  // once; the planner and the merge kernel (two launches) are then pure
+  // latency
+  const int maxblk_all = ceil_div(std::max(p->max_seq_len, 1), kBlock);
+  int cluster = std::min(kClusterMax, std::max(1, ceil_div(maxblk_all, kClusterBlocksPerCta)));
+  if (kernel == 0 && use_tc && !dense && !verify && Q == 1 && !extra_err &&
+      !(o && (o->split_blocks > 0 || o->target_items > 0)) &&
+      maxblk_all <= kClusterMax * kClusterBlocksPerCta &&
+      (long long)p->batch * kv->num_kv_heads * cluster <= kClusterMaxCtas)
+    single = true;
   // the expired-wait test mode is built into the tensor-core decode kernel only
   if ((test_flags & PA_TEST_EXPIRE_WAIT) && !(use_tc && !dense && !umma)) return PA_ERR_UNSUPPORTED;
+  if (single) {
+    // no plan, no partials: only the header (error flags, cleared first)
+    if (!ws) return PA_ERR_INVALID_ARG;
+    if (!aligned16(ws)) return PA_ERR_INVALID_ARG;
+    if (ws_bytes < (size_t)kHdrWords * 4) return PA_ERR_WORKSPACE_TOO_SMALL;
+    AttnParams ap;
+    std::memset(&ap, 0, sizeof ap);
+    ap.kv = view_of(kv);
+    ap.q = static_cast<const __nv_bfloat16 *>(p->q);
+    ap.B = p->batch;
+    ap.Q = 1;
+    ap.Hq = p->num_q_heads;
+    ap.G = G;
+    ap.tables = p->block_tables;
+    ap.stride = p->block_table_stride;
+    ap.seq_lens = p->seq_lens;
+    ap.scale_log2 = p->softmax_scale * 1.4426950408889634f;
+    ap.out = p->out;
+    ap.out_fp32 = p->out_fp32 ? 1 : 0;
+    ap.lse_out = p->lse_out;
+    ap.hdr = static_cast<uint32_t *>(ws);
+    ap.virt = 1;
+    ap.RG = 1;
+    ap.R = G;
+    ap.test_expire = (test_flags & PA_TEST_EXPIRE_WAIT) ? 1 : 0;
+    if (cudaMemsetAsync(ws, 0, 16, stream) != cudaSuccess) return PA_ERR_CUDA;
+    if (o && o->event_begin &&
+        cudaEventRecord(static_cast<cudaEvent_t>(o->event_begin), stream) != cudaSuccess)
+      return PA_ERR_CUDA;
+    if (launch_decode_tc_cluster(ap, cluster, stream) != cudaSuccess) return PA_ERR_CUDA;
+    if (o && o->event_end &&
+        cudaEventRecord(static_cast<cudaEvent_t>(o->event_end), stream) != cudaSuccess)
+      return PA_ERR_CUDA;
+    return PA_OK;
+  }
   const int mode = dense ? 2 : 1;   // dense verify runs as row groups of up to 48 rows
   const int RG = dense ? row_groups(Q, G) : 1;
   if (!ws) return PA_ERR_INVALID_ARG;

@@ -96,7 +96,9 @@ __device__ __forceinline__ void tma_rows(void *dst, const CUtensorMap *map, int 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 
-template <int DT, int D>
+// CL: the single-launch variant (one thread-block cluster per sequence and
+// kv head, partials merged through distributed shared memory)
+template <int DT, int D, bool CL = false>
 struct Geo {
   static constexpr bool BF16 = DT == PA_KV_BF16;              // ldmatrix fragments, no dequant
   static constexpr bool BYTE_CODES = DT == PA_KV_INT8 || DT == PA_KV_FP8;   // one byte per element
@@ -118,9 +120,14 @@ struct Geo {
   static constexpr int STAGE = SW ? (PAYLOAD + 1023) / 1024 * 1024 : PAYLOAD;
   // byte formats: 2 stages so that 3 CTAs (12 warps) fit per SM; NVFP4: 3;
   // bf16 (16 KB per block at D = 256): 1, for 3 CTAs per SM
-  static constexpr int NSTAGE = BF16 ? 1 : (BYTE_CODES ? 2 : 3);
+  // (single-launch variant: 2 stages, so that a warp's first two blocks are
+  // in flight together)
+  static constexpr int NSTAGE = CL ? 2 : (BF16 ? 1 : (BYTE_CODES ? 2 : 3));
   static constexpr int WARP_BYTES = NSTAGE * STAGE;
-  static constexpr int SMEM = kWarps * WARP_BYTES + (SW ? 1024 : 0);
+  // single-launch variant: the CTA's merged rows [8][D] and their LSE [8],
+  // read by the other CTAs of its cluster
+  static constexpr int MERGE = CL ? 8 * D * 4 + 8 * 4 : 0;
+  static constexpr int SMEM = kWarps * WARP_BYTES + MERGE + (SW ? 1024 : 0);
   static_assert(KG >= 1 && VG >= 1 && CODE % 16 == 0 && SC % 16 == 0, "geometry");
   static_assert(WARP_BYTES >= 8 * D * 4, "stage area holds the warp's O for the merge");
 };
@@ -239,11 +246,52 @@ __device__ __forceinline__ int sw_off(int row, int byte) {
          (byte & 15);
 }
 
-template <int DT, int D, int R>
+// ---- thread-block clusters (single-launch variant)
+constexpr int kMaxCluster = 8;   // CTAs per cluster (the portable limit)
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_index() {
+  uint32_t r;
+  asm("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+// every thread of every CTA of the cluster; shared-memory writes before it
+// are visible to the cluster's reads after it
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// a shared-memory address of this CTA -> the same offset in CTA `rank`
+__device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// CL = false: one CTA per planned work item (partials merged by the merge
+// kernel).  CL = true: the single-launch variant for small problems -- no
+// planner and no merge kernel: cluster i handles (sequence i / Hkv, kv head
+// i % Hkv), its CTAs split the sequence's blocks evenly, and after the
+// in-CTA merge each CTA merges one slice of the head dim over the cluster's
+// partials, read from the other CTAs' shared memory.
+template <int DT, int D, int R, bool CL = false>
 __global__ void __launch_bounds__(kThreads, 3)
     decode_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV) {
-  using Gm = Geo<DT, D>;
+  using Gm = Geo<DT, D, CL>;
   constexpr int KG = Gm::KG, KS = Gm::KS, VE = Gm::VE, VB = Gm::VB, VG = Gm::VG;
   constexpr int NSTAGE = Gm::NSTAGE, ROW = Gm::ROW, SROW = Gm::SROW;
   constexpr float kRescale = 8.0f;
@@ -254,18 +302,48 @@ __global__ void __launch_bounds__(kThreads, 3)
   __shared__ __align__(8) uint64_t bars[kWarps][NSTAGE];
   __shared__ float s_m[kWarps][8], s_l[kWarps][8];
 
-  griddep_launch();   // the merge may start launching once every CTA has begun
-  griddep_wait();     // the plan of this call is complete
-  const uint32_t num_items = p.hdr[HDR_NUM_ITEMS];
-  if (blockIdx.x >= num_items) return;
-  const WorkItem it = p.items[blockIdx.x];
+  WorkItem it;
+  int len;
+  if constexpr (CL) {
+    // the cluster's (sequence, kv head) and this CTA's share of its blocks
+    const int cid = (int)cluster_index(), rank = (int)cluster_rank(), nr = (int)cluster_size();
+    const int unit = cid / p.kv.hkv;
+    int L = p.seq_lens[unit];
+    uint32_t e = 0;
+    if (L < 0) {
+      e |= PA_ERRF_NEG_LEN;
+      L = 0;
+    }
+    const long long cap = (long long)p.stride * kBlock;
+    if (L > cap) {
+      e |= PA_ERRF_LEN_OVER_CAPACITY;
+      L = (int)cap;
+    }
+    if (e && rank == 0 && threadIdx.x == 0) set_err(p.hdr, e);
+    const int nblk = (L + kBlock - 1) / kBlock, chunk = (nblk + nr - 1) / nr;
+    it.unit = unit;
+    it.kvh = cid % p.kv.hkv;
+    it.blk_begin = min(nblk, rank * chunk);
+    it.blk_end = min(nblk, it.blk_begin + chunk);
+    it.part = rank;
+    it.parts = nr;
+    it.slot = -1;
+    it.pad = 0;
+    len = L;
+  } else {
+    griddep_launch();   // the merge may start launching once every CTA has begun
+    griddep_wait();     // the plan of this call is complete
+    const uint32_t num_items = p.hdr[HDR_NUM_ITEMS];
+    if (blockIdx.x >= num_items) return;
+    it = p.items[blockIdx.x];
+    len = p.units[it.unit].len;
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = lane >> 2, c = lane & 3;
   const int Q = p.Q;
   const int b = p.virt ? it.unit / Q : it.unit;
   const int qi = p.virt ? it.unit % Q : 0;
-  const int len = p.units[it.unit].len;
   const int kvh = it.kvh;
   const int Hkv = p.kv.hkv;
 
@@ -727,7 +805,11 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
     const float out = L > 0.f ? acc / L * vg : 0.f;
     const float lse = L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : kNegInf;
-    if (it.parts <= 1) {
+    if constexpr (CL) {   // this CTA's partial, for the cluster merge below
+      float *mo = reinterpret_cast<float *>(smem + kWarps * Gm::WARP_BYTES);
+      mo[h * D + d] = out;
+      if (d == 0) mo[8 * D + h] = lse;
+    } else if (it.parts <= 1) {
       const size_t row = ((size_t)b * Q + qi) * p.Hq + (size_t)kvh * G + h;
       if (p.out_fp32)
         reinterpret_cast<float *>(p.out)[row * D + d] = out;
@@ -739,6 +821,51 @@ __global__ void __launch_bounds__(kThreads, 3)
       p.part_o[prow * D + d] = out;
       if (d == 0) p.part_lse[prow] = lse;
     }
+  }
+  if constexpr (CL) {
+    // LSE merge of the cluster's partials: this CTA takes head-dim slice
+    // [d0, d1) of every row
+    cluster_sync_all();
+    const int rank = (int)cluster_rank(), nr = (int)cluster_size();
+    const int per = (D + nr - 1) / nr, d0 = rank * per, d1 = min(D, d0 + per);
+    const uint32_t mo = smem_u32(smem + kWarps * Gm::WARP_BYTES);
+    for (int idx = threadIdx.x; idx < R * per; idx += kThreads) {
+      const int h = idx / per, d = d0 + idx % per;
+      if (d >= d1) continue;
+      // all 2 * nr remote loads are issued before any result is used (an
+      // empty partial holds o = 0 and lse = -inf, both defined)
+      float lj[kMaxCluster], oj[kMaxCluster];
+#pragma unroll
+      for (int j = 0; j < kMaxCluster; ++j) {
+        if (j < nr) {
+          lj[j] = ld_cluster_f32(map_rank(mo + (uint32_t)(8 * D + h) * 4, (uint32_t)j));
+          oj[j] = ld_cluster_f32(map_rank(mo + (uint32_t)(h * D + d) * 4, (uint32_t)j));
+        }
+      }
+      float M = kNegInf;
+#pragma unroll
+      for (int j = 0; j < kMaxCluster; ++j)
+        if (j < nr) M = fmaxf(M, lj[j]);
+      float acc = 0.f, wsum = 0.f;
+      if (M != kNegInf) {
+#pragma unroll
+        for (int j = 0; j < kMaxCluster; ++j) {
+          if (j < nr) {
+            const float w = lj[j] == kNegInf ? 0.f : __expf(lj[j] - M);
+            acc += w * oj[j];
+            wsum += w;
+          }
+        }
+      }
+      const float out = wsum > 0.f ? acc / wsum : 0.f;
+      const size_t row = ((size_t)b * Q + qi) * p.Hq + (size_t)kvh * G + h;
+      if (p.out_fp32)
+        reinterpret_cast<float *>(p.out)[row * D + d] = out;
+      else
+        reinterpret_cast<__nv_bfloat16 *>(p.out)[row * D + d] = __float2bfloat16_rn(out);
+      if (d == 0 && p.lse_out) p.lse_out[row] = wsum > 0.f ? M + __logf(wsum) : kNegInf;
+    }
+    cluster_sync_all();   // no CTA leaves while another still reads its partial
   }
 }
 
@@ -757,6 +884,50 @@ cudaError_t launch_one(const AttnParams &p, int grid, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, grid, kThreads, Gm::SMEM, s, p, tk, tv);
+}
+
+// single-launch variant: B * Hkv clusters of P <= kMaxCluster CTAs
+template <int DT, int D, int R>
+cudaError_t launch_cluster_one(const AttnParams &p, int P, cudaStream_t s) {
+  using Gm = Geo<DT, D, true>;
+  auto kern = decode_kernel<DT, D, R, true>;
+  CUtensorMap tk, tv;
+  std::memset(&tk, 0, sizeof tk);
+  std::memset(&tv, 0, sizeof tv);
+  if constexpr (Gm::SW) {
+    const uint64_t rows = (uint64_t)p.kv.num_blocks * p.kv.hkv * kBlock;
+    if (!make_row_map(&tk, p.kv.k, Gm::ROW, rows) || !make_row_map(&tv, p.kv.v, Gm::ROW, rows))
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
+  if (e != cudaSuccess) return e;
+  const long long grid = (long long)p.B * p.kv.hkv * P;
+  if (P < 1 || P > kMaxCluster || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Gm::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)P;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p, tk, tv);
+}
+
+template <int DT>
+cudaError_t launch_cluster_dtype(const AttnParams &p, int P, cudaStream_t s) {
+  const int D = p.kv.D, R = p.R;
+#define PA_TC_CASE(DD, RR) \
+  if (D == DD && R == RR) return launch_cluster_one<DT, DD, RR>(p, P, s);
+  PA_TC_CASE(128, 1) PA_TC_CASE(128, 2) PA_TC_CASE(128, 4) PA_TC_CASE(128, 6)
+  PA_TC_CASE(128, 8) PA_TC_CASE(256, 1) PA_TC_CASE(256, 2) PA_TC_CASE(256, 4)
+  PA_TC_CASE(256, 6) PA_TC_CASE(256, 8)
+#undef PA_TC_CASE
+  return cudaErrorInvalidValue;
 }
 
 template <int DT>

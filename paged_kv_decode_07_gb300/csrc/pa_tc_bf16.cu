@@ -6,4 +6,7 @@ namespace pa {
 cudaError_t launch_decode_tc_bf16(const AttnParams &p, int grid, cudaStream_t s) {
   return tc::launch_dtype<PA_KV_BF16>(p, grid, s);
 }
+cudaError_t launch_decode_tc_cluster_bf16(const AttnParams &p, int P, cudaStream_t s) {
+  return tc::launch_cluster_dtype<PA_KV_BF16>(p, P, s);
+}
 }  // namespace pa

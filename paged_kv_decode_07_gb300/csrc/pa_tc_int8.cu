@@ -7,4 +7,7 @@ namespace pa {
 cudaError_t launch_decode_tc_int8(const AttnParams &p, int grid, cudaStream_t s) {
   return tc::launch_dtype<PA_KV_INT8>(p, grid, s);
 }
+cudaError_t launch_decode_tc_cluster_int8(const AttnParams &p, int P, cudaStream_t s) {
+  return tc::launch_cluster_dtype<PA_KV_INT8>(p, P, s);
+}
 }  // namespace pa

@@ -78,7 +78,7 @@ def test_invalid_arguments_are_rejected_on_the_host(L, fn):
     assert call(L, fn, kv_struct(), prob_struct(B=-1)) == pa.PA_ERR_INVALID_ARG
     assert call(L, fn, kv_struct(), prob_struct(), ws=None) == pa.PA_ERR_INVALID_ARG
     assert call(L, fn, kv_struct(), prob_struct(), ws_bytes=64) == pa.PA_ERR_WORKSPACE_TOO_SMALL
-    bad_opts = pa._Options(5, 0, 0, None, None)
+    bad_opts = pa._Options(6, 0, 0, None, None)
     assert call(L, fn, kv_struct(), prob_struct(), opts=bad_opts) == pa.PA_ERR_INVALID_ARG
     # an empty batch is a no-op
     assert call(L, fn, kv_struct(), prob_struct(B=0)) == pa.PA_OK
@@ -202,3 +202,15 @@ def test_test_flags_are_checked_on_the_host(L):
                 opts=opts(0, pa.PA_TEST_EXPIRE_WAIT)) == pa.PA_ERR_UNSUPPORTED    # tcgen05 verify
     assert call(L, "pa_verify", kv_struct(dtype=1), prob_struct(Q=8),
                 opts=opts(2, pa.PA_TEST_EXPIRE_WAIT)) == pa.PA_ERR_UNSUPPORTED    # dense tiles
+
+
+def test_single_launch_kernel_choice_is_checked_on_the_host(L):
+    """kernel 5 (single-launch decode) takes pa_decode only; 6 is unknown."""
+    def opts(kernel):
+        return pa._Options(kernel, 0, 0, None, None, 0)
+    assert call(L, "pa_verify", kv_struct(), prob_struct(Q=2), opts=opts(5)) == pa.PA_ERR_UNSUPPORTED
+    assert call(L, "pa_verify", kv_struct(), prob_struct(Q=1), opts=opts(5)) == pa.PA_ERR_UNSUPPORTED
+    assert call(L, "pa_decode", kv_struct(), prob_struct(), opts=opts(6)) == pa.PA_ERR_INVALID_ARG
+    assert call(L, "pa_decode", kv_struct(), prob_struct(), opts=opts(5), ws=None) == pa.PA_ERR_INVALID_ARG
+    assert call(L, "pa_decode", kv_struct(), prob_struct(), opts=opts(5),
+                ws_bytes=128) == pa.PA_ERR_WORKSPACE_TOO_SMALL

@@ -20,17 +20,18 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
+@pytest.mark.parametrize("kernel", [2, 5])   # planned split-K, single launch
 @pytest.mark.parametrize("name", ["bf16_skewed_b256_l16_128k_d256", "int8_b32_l1k_32k_d256",
                                   "nvfp4_b4_l262k_d256", "fp8_b32_l1k_32k_d256"])
-def test_expired_wait_is_reported_and_the_context_stays_usable(name):
+def test_expired_wait_is_reported_and_the_context_stays_usable(name, kernel):
     wl = W.make_workload(name, device=DEV, seq_lens=[3000, 17, 640, 1])
-    out, ws = run(wl, kernel=2, test_flags=pa.PA_TEST_EXPIRE_WAIT)
+    out, ws = run(wl, kernel=kernel, test_flags=pa.PA_TEST_EXPIRE_WAIT)
     torch.cuda.synchronize()                      # returns: no hang, no fault
     flags = pa.read_error(ws)
     assert flags & pa.PA_ERRF_WAIT_TIMEOUT, f"flags {flags:#x}"
     assert flags & ~pa.PA_ERRF_WAIT_TIMEOUT == 0, f"flags {flags:#x}"
     # the same workspace, an ordinary call: correct and no flags
-    o32, lse, _ = run(wl, out_fp32=True, return_lse=True, kernel=2, workspace=ws)
+    o32, lse, _ = run(wl, out_fp32=True, return_lse=True, kernel=kernel, workspace=ws)
     torch.cuda.synchronize()
     assert pa.read_error(ws) == 0
     ref_o, ref_l = oracle_rows(wl)

@@ -13,12 +13,13 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-@pytest.mark.parametrize("name,fn", [("int8_b32_l1k_32k_d256", "decode"),
-                                     ("bf16_skewed_b256_l16_128k_d256", "decode"),
-                                     ("nvfp4_verify_q8_b4_ctx64k_d256", "verify"),
-                                     ("fp8_verify_q8_b4_ctx64k_d256", "verify")])
-def test_capture_and_replay_with_new_inputs(name, fn):
-    lens = [2000, 517, 33, 1200]
+@pytest.mark.parametrize("name,fn,lens", [
+    ("int8_b32_l1k_32k_d256", "decode", [2000, 517, 33, 1200]),
+    ("bf16_skewed_b256_l16_128k_d256", "decode", [2000, 517, 33, 1200]),
+    ("nvfp4_verify_q8_b4_ctx64k_d256", "verify", [2000, 517, 33, 1200]),
+    ("fp8_verify_q8_b4_ctx64k_d256", "verify", [2000, 517, 33, 1200]),
+    ("bf16_b1_l1000_d128", "decode", [1000, 517, 33, 700])])   # single-launch decode
+def test_capture_and_replay_with_new_inputs(name, fn, lens):
     wl = W.make_workload(name, device=DEV, seq_lens=lens)
     kv = pa.KvCache.from_workload(wl)
     call = pa.decode if fn == "decode" else pa.verify

@@ -39,10 +39,13 @@ def _fn(wl):
 def _kernels(dtype, q_len=1):
     """0 = auto; 1 = CUDA-core kernel; 2 = tensor-core kernel (verify: dense
     tile); 3 = tensor-core kernel with verify as one unit per query token;
-    4 = tcgen05 verify (NVFP4 / FP8, q_len > 1)."""
+    4 = tcgen05 verify (NVFP4 / FP8, q_len > 1); 5 = single-launch decode
+    (one thread-block cluster per sequence and kv head, q_len 1)."""
     if dtype in ("nvfp4", "fp8") and q_len > 1:
         return [0, 1, 2, 3, 4]
-    return [0, 1, 2, 3]
+    if q_len > 1:
+        return [0, 1, 2, 3]
+    return [0, 1, 2, 3, 5]
 
 
 REDUCED_CASES = [(n, k) for n in REDUCED
@@ -132,8 +135,8 @@ def test_dequant_gather_bit_exact(dt):
     assert np.array_equal(vg.view(np.uint32), rv.view(np.uint32))
 
 
-@pytest.mark.parametrize("dt,kernel", [("bf16", 1), ("bf16", 2), ("int8", 1), ("int8", 2),
-                                       ("nvfp4", 1), ("nvfp4", 2), ("fp8", 1), ("fp8", 2)])
+@pytest.mark.parametrize("dt,kernel", [(d, k) for d in ("bf16", "int8", "nvfp4", "fp8")
+                                       for k in (1, 2, 5)])
 @pytest.mark.parametrize("shape", [(8, 8, 128), (16, 8, 128), (12, 2, 256), (4, 4, 256),
                                    (32, 4, 256), (2, 1, 128)])
 def test_gqa_and_head_dim_variants(dt, kernel, shape):
@@ -204,3 +207,35 @@ def test_umma_verify_full_size(name):
     compare_lse(lse, ref_l, name)
     del wl
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("dt", ["bf16", "int8", "nvfp4", "fp8"])
+def test_small_problem_runs_as_one_launch(dt):
+    """Auto mode sends a problem whose sequences have at most 1,024 keys
+    (and whose clusters fit on the GPU at once) to the single-launch
+    decode: no plan is written (the header's item count stays 0), and the
+    result matches the oracle, including a padded row and a one-key row."""
+    lens = [1000, 1, 0, 1024]   # 4 sequences x 4 kv heads x clusters of 8 = 128 CTAs
+    wl = W.make_workload(DECODE_NAMES[dt], device=DEV, seq_lens=lens)
+    o32, lse, ws = run(wl, out_fp32=True, return_lse=True)
+    ob, ws2 = run(wl)
+    torch.cuda.synchronize()
+    assert pa.read_error(ws) == 0
+    assert pa.header(ws)[1] == 0, "planned: the single-launch path was not taken"
+    ref_o, ref_l = oracle_rows(wl)
+    compare(o32, ref_o, f"{dt} single launch")
+    compare_lse(lse, ref_l, f"{dt} single launch")
+    assert bf16_matches_fp32(ob, o32), "bf16 output is not RNE of the fp32 output"
+
+
+def test_single_launch_reports_bad_lengths():
+    """Length errors of the single-launch path reach the header: a sequence
+    longer than its table's capacity is clamped and flagged."""
+    wl = W.make_workload("bf16_b1_l1000_d128", device=DEV, seq_lens=[300, 200])
+    seq = wl.seq_lens.clone()
+    seq[1] = wl.block_tables.shape[1] * 16 + 40
+    kv = pa.KvCache.from_workload(wl)
+    out, ws = pa.decode(kv, wl.q, wl.block_tables, seq, wl.softmax_scale, kernel=5,
+                        max_seq_len=300)
+    torch.cuda.synchronize()
+    assert pa.read_error(ws) & pa.PA_ERRF_LEN_OVER_CAPACITY
