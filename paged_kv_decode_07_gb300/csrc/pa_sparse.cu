@@ -129,12 +129,13 @@ __global__ void __launch_bounds__(512) means_kernel(const KvView kv, const int *
   }
 }
 
-// Eight lanes per sparse block: a CTA of 128 threads scores 128 consecutive
-// blocks of one (b, h), four blocks per warp step.  Lane l8 of a block reads
-// float4 l8, l8 + 8, ... of the block's mean row, so the four blocks of a
-// load instruction are four whole 128-byte lines (coalesced); the G query
-// rows come from shared memory and the eight partial dots of each head are
-// added by three shuffles.
+// Eight lanes per sparse block, two blocks per lane group: a CTA of 128
+// threads scores 128 consecutive blocks of one (b, h), eight blocks per warp
+// step.  Lane l8 of a group reads float4 l8, l8 + 8, ... of its two blocks'
+// mean rows, so the four groups of a load instruction read four whole
+// 128-byte lines (coalesced); every query float4 read from shared memory
+// serves both blocks, and the eight partial dots of each head are added by
+// three shuffles.
 constexpr int kScoreThreads = 128;
 constexpr int kScoreCta = kScoreThreads;   // blocks per CTA
 
@@ -155,46 +156,58 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(
   }
   __syncthreads();
   const int L = seq_len_of(seq_lens, b, capacity);
-  const int nsb = (L + sb - 1) / sb;
+  // blocks beyond the means' capacity have no mean (the selection flags them)
+  const int nsb = min((L + sb - 1) / sb, max_nsb);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sub = lane >> 3, l8 = lane & 7;
   const int per = D / 32;   // float4 of a row per lane
-  for (int step = 0; step < kScoreCta / 16; ++step) {
-    const int j0 = c * kScoreCta + step * 16 + warp * 4;   // the warp's first block
+  for (int step = 0; step < kScoreCta / 32; ++step) {
+    const int j0 = c * kScoreCta + step * 32 + warp * 8;   // the warp's first block
     if (j0 >= max_nsb) break;                               // the whole warp
-    const int j = j0 + sub;
-    float acc[G];
+    const int ja = j0 + sub, jb = ja + 4;                   // this group's two blocks
+    float acc[2][G];
 #pragma unroll
-    for (int g = 0; g < G; ++g) acc[g] = 0.f;
-    if (j < nsb) {
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int g = 0; g < G; ++g) acc[u][g] = 0.f;
+    float4 x[2][8];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int j = u ? jb : ja;
       const float4 *m = reinterpret_cast<const float4 *>(means + (((size_t)b * max_nsb + j) * H + h) * D);
-      float4 x[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        if (i < per) x[i] = m[l8 + 8 * i];
+        x[u][i] = (i < per && j < nsb) ? m[l8 + 8 * i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (i < per) {
+    for (int i = 0; i < 8; ++i) {
+      if (i < per) {
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float4 y = sq[g][l8 + 8 * i];
-            acc[g] = fmaf(x[i].x, y.x, fmaf(x[i].y, y.y, fmaf(x[i].z, y.z, fmaf(x[i].w, y.w, acc[g]))));
-          }
+        for (int g = 0; g < G; ++g) {
+          const float4 y = sq[g][l8 + 8 * i];
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            acc[u][g] = fmaf(x[u][i].x, y.x, fmaf(x[u][i].y, y.y,
+                        fmaf(x[u][i].z, y.z, fmaf(x[u][i].w, y.w, acc[u][g]))));
         }
       }
     }
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      acc[g] += __shfl_xor_sync(0xffffffffu, acc[g], 1);
-      acc[g] += __shfl_xor_sync(0xffffffffu, acc[g], 2);
-      acc[g] += __shfl_xor_sync(0xffffffffu, acc[g], 4);
-    }
-    float sc = kNegInf;
-    if (j < nsb) {
+    for (int u = 0; u < 2; ++u) {
+      const int j = u ? jb : ja;
 #pragma unroll
-      for (int g = 0; g < G; ++g) sc = fmaxf(sc, acc[g]);
+      for (int g = 0; g < G; ++g) {
+        acc[u][g] += __shfl_xor_sync(0xffffffffu, acc[u][g], 1);
+        acc[u][g] += __shfl_xor_sync(0xffffffffu, acc[u][g], 2);
+        acc[u][g] += __shfl_xor_sync(0xffffffffu, acc[u][g], 4);
+      }
+      float sc = kNegInf;
+      if (j < nsb) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) sc = fmaxf(sc, acc[u][g]);
+      }
+      if (l8 == 0 && j < max_nsb) scores[((size_t)b * H + h) * max_nsb + j] = sc;
     }
-    if (l8 == 0 && j < max_nsb) scores[((size_t)b * H + h) * max_nsb + j] = sc;
   }
 }
 

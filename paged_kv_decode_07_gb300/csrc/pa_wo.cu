@@ -11,27 +11,32 @@
 // fp32; it enters the MMA as two bf16 terms hi = bf16(o), lo = bf16(o - hi)
 // (o - hi - lo is below 2^-16 |o|), W exactly.
 //
-// Grid: (N / 64 column tiles) x (k splits) x (64-row blocks of M).  A CTA
-// of 4 warps streams its W[k range, 64 columns] and o[64 rows, k range] in
-// 64-deep k chunks by 2-D TMA (128-byte swizzle, conflict-free ldmatrix /
-// fragment reads) through a 4-stage mbarrier ring; warp w takes the w-th
-// k16 step of every chunk over all 64 columns, so each element of o is
-// split into hi / lo once per CTA, and the four warps' sums are added in
-// shared memory at the end.  Split partials go to the workspace and a
-// second kernel adds them in fixed order (deterministic).  With programmatic
-// dependent launch the W tiles of the first stages are requested before the
-// attention's output is complete.
+// Grid: (N / 256 column tiles) x (k splits) x (64-row blocks of M), about
+// one CTA per SM.  A CTA of 4 warps streams its W[k range, 256 columns]
+// (four 64-column TMA boxes per 64-deep k chunk, 128-byte swizzle) and
+// o[64 rows, k range] through a 4-stage mbarrier ring; warp w owns columns
+// 64 w .. 64 w + 63 over the whole k range, so no sums are exchanged and
+// each o chunk is read once per 256 columns (the wider the tile, the fewer
+// times the 4-byte o is re-read from L2 next to the 2-byte W).  Split
+// partials go to the workspace and a second kernel adds them in fixed
+// order (deterministic).  With programmatic dependent launch the W tiles of
+// the first stages are requested before the attention's output is complete.
 #include "pa_decode_mma.cuh"
 
 namespace pa {
 namespace {
 
 constexpr int kWoThreads = 128;
-constexpr int kWoN = 64;       // columns per CTA: one 128-byte TMA box of W
-constexpr int kWoK = 64;       // k per chunk: one k16 step per warp
+constexpr int kWoWarps = 4;
+constexpr int kWoBoxN = 64;    // columns per TMA box of W (128 bytes of bf16)
+constexpr int kWoBoxes = 4;    // boxes per chunk: 256 columns per CTA
+constexpr int kWoN = kWoBoxes * kWoBoxN;
+constexpr int kWoWarpN = kWoN / kWoWarps;   // 64 columns (8 n8 tiles) per warp
+constexpr int kWoK = 64;       // k per chunk: four k16 steps
 constexpr int kWoStages = 4;
 constexpr int kWoRows = 64;    // rows of o per CTA at most (4 m16 tiles)
-constexpr int kWoWBytes = kWoK * kWoN * 2;           // 8 KB
+constexpr int kWoBoxBytes = kWoK * kWoBoxN * 2;      // 8 KB
+constexpr int kWoWBytes = kWoBoxes * kWoBoxBytes;    // 32 KB
 // one 32-k fp32 box of o holds MT * 16 rows of 128 bytes
 template <int MT>
 struct WoGeo {
@@ -39,7 +44,6 @@ struct WoGeo {
   static constexpr int Stage = kWoWBytes + 2 * ABox;   // multiple of 1024
   static constexpr int Smem = kWoStages * Stage + 1024;
   static_assert(Stage % 1024 == 0, "swizzled boxes need 1024-byte alignment");
-  static_assert(kWoStages * Stage >= 4 * MT * 16 * kWoN * 4, "room for the warps' sums");
 };
 
 struct WoParams {
@@ -116,10 +120,13 @@ __global__ void __launch_bounds__(kWoThreads) wo_kernel(const WoParams p,
   const uint64_t pol = policy_evict_first();   // W: read once
   const uint64_t pol_o = policy_evict_last();   // o: read by every column tile
   auto chunk_k = [&](int c) { return (c0 + (c + rot) % nch) * kWoK; };
-  auto issue_w = [&](int c) {   // thread 0: W rows of the c-th chunk
+  auto issue_w = [&](int c) {   // thread 0: W rows of the c-th chunk, four boxes
     uint8_t *st = smem + (c % kWoStages) * Gm::Stage;
     mbar_arrive_expect_tx(&bars[c % kWoStages], Gm::Stage);
-    tc::tma_rows(st, &tmW, n0, chunk_k(c), &bars[c % kWoStages], pol);
+#pragma unroll
+    for (int w = 0; w < kWoBoxes; ++w)
+      tc::tma_rows(st + w * kWoBoxBytes, &tmW, n0 + w * kWoBoxN, chunk_k(c), &bars[c % kWoStages],
+                   pol);
   };
   auto issue_a = [&](int c) {   // thread 0: o rows m0 .. m0 + 16 MT - 1, two 32-k boxes
     uint8_t *st = smem + (c % kWoStages) * Gm::Stage + kWoWBytes;
@@ -134,7 +141,7 @@ __global__ void __launch_bounds__(kWoThreads) wo_kernel(const WoParams p,
   if (tid == 0)
     for (int c = 0; c < pro; ++c) issue_a(c);
 
-  // warp w: k16 step w of every chunk, all 64 columns (8 n8 tiles)
+  // warp w: columns 64 w .. 64 w + 63 (8 n8 tiles), every k16 step
   float acc[MT][8][4];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
@@ -144,7 +151,7 @@ __global__ void __launch_bounds__(kWoThreads) wo_kernel(const WoParams p,
       for (int e = 0; e < 4; ++e) acc[mt][j][e] = 0.f;
 
   // ldmatrix.trans row address: thread i -> matrix i / 8 = (k half, n half), row i % 8
-  const int lm_k = warp * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+  const int lm_k = ((lane >> 3) & 1) * 8 + (lane & 7);   // + 16 ks for k16 step ks
   const int lm_n = (lane >> 4) * 8;   // + 16 h for the h-th x4
 
   int issued = pro;
@@ -158,29 +165,33 @@ __global__ void __launch_bounds__(kWoThreads) wo_kernel(const WoParams p,
       break;
     }
     const uint8_t *st = smem + (c % kWoStages) * Gm::Stage;
-    const uint32_t wbase = smem_u32(st);
+    const uint32_t wbase = smem_u32(st) + warp * kWoBoxBytes;   // this warp's box
     const uint8_t *abase = st + kWoWBytes;
-    uint32_t b[4][4];   // four ldmatrix.x4: n8 tiles (2h, 2h + 1)
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const int n = lm_n + 16 * h;
-      ldsm_x4_trans(wbase + lm_k * 128 + (((n >> 3) ^ (lm_k & 7)) << 4), b[h][0], b[h][1],
-                    b[h][2], b[h][3]);
-    }
+    for (int ks = 0; ks < kWoK / 16; ++ks) {
+      const int kr = ks * 16 + lm_k;
+      uint32_t b[4][4];   // four ldmatrix.x4: n8 tiles (2h, 2h + 1)
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      const int r = mt * 16 + g, k = warp * 16 + 2 * t;
-      uint32_t ah[4], al[4];
-      split_bf16(*reinterpret_cast<const float2 *>(abase + a_off<MT>(r, k)), ah[0], al[0]);
-      split_bf16(*reinterpret_cast<const float2 *>(abase + a_off<MT>(r + 8, k)), ah[1], al[1]);
-      split_bf16(*reinterpret_cast<const float2 *>(abase + a_off<MT>(r, k + 8)), ah[2], al[2]);
-      split_bf16(*reinterpret_cast<const float2 *>(abase + a_off<MT>(r + 8, k + 8)), ah[3],
-                 al[3]);
+      for (int h = 0; h < 4; ++h) {
+        const int n = lm_n + 16 * h;
+        ldsm_x4_trans(wbase + kr * 128 + (((n >> 3) ^ (kr & 7)) << 4), b[h][0], b[h][1], b[h][2],
+                      b[h][3]);
+      }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t b0 = b[j >> 1][2 * (j & 1)], b1 = b[j >> 1][2 * (j & 1) + 1];
-        mma_bf16(acc[mt][j], ah[0], ah[1], ah[2], ah[3], b0, b1);
-        mma_bf16(acc[mt][j], al[0], al[1], al[2], al[3], b0, b1);
+      for (int mt = 0; mt < MT; ++mt) {
+        const int r = mt * 16 + g, k = ks * 16 + 2 * t;
+        uint32_t ah[4], al[4];
+        split_bf16(*reinterpret_cast<const float2 *>(abase + a_off<MT>(r, k)), ah[0], al[0]);
+        split_bf16(*reinterpret_cast<const float2 *>(abase + a_off<MT>(r + 8, k)), ah[1], al[1]);
+        split_bf16(*reinterpret_cast<const float2 *>(abase + a_off<MT>(r, k + 8)), ah[2], al[2]);
+        split_bf16(*reinterpret_cast<const float2 *>(abase + a_off<MT>(r + 8, k + 8)), ah[3],
+                   al[3]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t b0 = b[j >> 1][2 * (j & 1)], b1 = b[j >> 1][2 * (j & 1) + 1];
+          mma_bf16(acc[mt][j], ah[0], ah[1], ah[2], ah[3], b0, b1);
+          mma_bf16(acc[mt][j], al[0], al[1], al[2], al[3], b0, b1);
+        }
       }
     }
     __syncthreads();   // stage consumed by every warp
@@ -190,37 +201,32 @@ __global__ void __launch_bounds__(kWoThreads) wo_kernel(const WoParams p,
       ++issued;
     }
   }
-  if (s_fail) {
+  if (s_fail) {   // only the last fill of each stage can still be in flight
     if (tid == 0)
-      for (int c = 0; c < issued; ++c) (void)mbar_wait(&bars[c % kWoStages], (c / kWoStages) & 1);
+      for (int c = max(issued - kWoStages, 0); c < issued; ++c)
+        (void)mbar_wait(&bars[c % kWoStages], (c / kWoStages) & 1);
     return;
   }
-  // ---- the four warps' sums meet in shared memory (the stage ring is idle now)
-  float *red = reinterpret_cast<float *>(smem);   // [warp][MT * 16 rows][64 columns]
-  constexpr int kRed = MT * 16 * kWoN;
+  // ---- this warp's 64 columns, straight from the accumulators
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
     for (int j = 0; j < 8; ++j)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const int row = mt * 16 + g + 8 * hh, col = j * 8 + 2 * t;
-        *reinterpret_cast<float2 *>(red + warp * kRed + row * kWoN + col) =
-            make_float2(acc[mt][j][2 * hh], acc[mt][j][2 * hh + 1]);
+        const int m = m0 + mt * 16 + g + 8 * hh;
+        const int n = n0 + warp * kWoWarpN + j * 8 + 2 * t;   // N is a multiple of 8: n + 1 < N too
+        if (m >= p.M || n >= p.N) continue;
+        const float v0 = acc[mt][j][2 * hh], v1 = acc[mt][j][2 * hh + 1];
+        if (p.splits > 1)
+          *reinterpret_cast<float2 *>(p.part + ((size_t)s * p.M + m) * p.N + n) = make_float2(v0, v1);
+        else if (p.y_fp32)
+          *reinterpret_cast<float2 *>(static_cast<float *>(p.y) + (size_t)m * p.N + n) =
+              make_float2(v0, v1);
+        else
+          *reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(p.y) + (size_t)m * p.N + n) =
+              __floats2bfloat162_rn(v0, v1);
       }
-  __syncthreads();
-  for (int i = tid; i < kRed; i += kWoThreads) {
-    const int row = i / kWoN, col = i % kWoN;
-    const int m = m0 + row, n = n0 + col;
-    if (m >= p.M || n >= p.N) continue;
-    const float v = ((red[i] + red[kRed + i]) + red[2 * kRed + i]) + red[3 * kRed + i];
-    if (p.splits > 1)
-      p.part[((size_t)s * p.M + m) * p.N + n] = v;
-    else if (p.y_fp32)
-      static_cast<float *>(p.y)[(size_t)m * p.N + n] = v;
-    else
-      static_cast<__nv_bfloat16 *>(p.y)[(size_t)m * p.N + n] = __float2bfloat16_rn(v);
-  }
 }
 
 // y = sum over splits of the partials, in split order
@@ -272,8 +278,14 @@ int wo_splits(int M, int K, int N, int requested) {
   const int chunks = K / kWoK;
   const int ntiles = (N + kWoN - 1) / kWoN;
   const int mblocks = (M + kWoRows - 1) / kWoRows;
-  int sp = requested > 0 ? requested : (2 * 152 + ntiles * mblocks - 1) / (ntiles * mblocks);
-  sp = std::max(1, std::min(sp, std::max(1, chunks / 8)));   // at least 8 chunks per split
+  // about one CTA per SM (each holds a 4-stage ring of about 40-48 KB
+  // stages, so one fits per SM); at least 4 chunks per split
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    sms = 148;
+  int sp = requested > 0 ? requested : std::max(1, sms / (ntiles * mblocks));
+  sp = std::max(1, std::min(sp, std::max(1, chunks / 4)));
   return std::min(sp, chunks);
 }
 
@@ -294,7 +306,7 @@ cudaError_t launch_wo(const float *o, int M, int K, const void *w, int N, int sp
   p.hdr = hdr;
   CUtensorMap tw;
   std::memset(&tw, 0, sizeof tw);
-  if (!make_map_2d(&tw, w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)N, (uint64_t)K, kWoN,
+  if (!make_map_2d(&tw, w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)N, (uint64_t)K, kWoBoxN,
                    kWoK))
     return cudaErrorInvalidValue;
   const int mblocks = (M + kWoRows - 1) / kWoRows;
