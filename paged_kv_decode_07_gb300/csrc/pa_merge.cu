@@ -28,10 +28,13 @@ __device__ __forceinline__ void store4(void *out, int out_fp32, size_t off, floa
 // Merges `parts` partials of one row with one CTA of kThreads threads.
 // po points at partial 0 of the row, consecutive partials `pstride` floats
 // apart; pl likewise with lstride.  The weights exp(lse_p - M) are computed
-// once per partial into shared memory (chunks of kChunk), then every thread
-// accumulates its float4 columns over the chunk, four partials per step so
-// that the loads of one step are in flight together.
-constexpr int kThreads = 64;
+// once per partial into shared memory (chunks of kChunk).  The threads form
+// kThreads / (D / 4) groups, each thread owning one float4 column: group k
+// accumulates partials k, k + groups, ... (four loads in flight per step),
+// so a row with hundreds of partials (a 262K-key sequence split into
+// partitions) is read by the whole CTA at once; the groups' sums are then
+// added in fixed order.
+constexpr int kThreads = 256;
 constexpr int kChunk = 512;
 
 __device__ void merge_row(const float *po, size_t pstride, const float *pl, size_t lstride,
@@ -40,6 +43,7 @@ __device__ void merge_row(const float *po, size_t pstride, const float *pl, size
   __shared__ float s_w[kChunk];
   __shared__ float s_red[kThreads / 32];
   __shared__ float s_M;
+  __shared__ float4 s_acc[kThreads];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   float M = kNegInf;
   for (int q = tid; q < parts; q += kThreads) M = fmaxf(M, pl[(size_t)q * lstride]);
@@ -60,10 +64,11 @@ __device__ void merge_row(const float *po, size_t pstride, const float *pl, size
     if (lse_out && tid == 0) lse_out[lse_off] = kNegInf;
     return;
   }
-  constexpr int kCols = 4;   // float4 column groups per thread (D <= 1024)
-  float4 acc[kCols];
-#pragma unroll
-  for (int k = 0; k < kCols; ++k) acc[k] = make_float4(0, 0, 0, 0);
+  const int cols = D / 4;                       // float4 columns (D <= 1024: cols <= kThreads)
+  const int groups = max(1, kThreads / cols);   // partial groups
+  const int col = tid % cols, grp = tid / cols;
+  const bool active = grp < groups && col < cols;
+  float4 acc = make_float4(0, 0, 0, 0);
   float wsum = 0.f;
   for (int q0 = 0; q0 < parts; q0 += kChunk) {
     const int n = min(kChunk, parts - q0);
@@ -74,45 +79,49 @@ __device__ void merge_row(const float *po, size_t pstride, const float *pl, size
     }
     __syncthreads();
     for (int q = 0; q < n; ++q) wsum += s_w[q];
+    if (!active) continue;
+    const float *base = po + (size_t)q0 * pstride + 4 * col;
+    int q = grp;
+    for (; q + 3 * groups < n; q += 4 * groups) {
+      float4 v[4];
 #pragma unroll
-    for (int k = 0; k < kCols; ++k) {
-      const int d = (k * kThreads + tid) * 4;
-      if (d >= D) break;
-      const float *base = po + (size_t)q0 * pstride + d;
-      int q = 0;
-      for (; q + 4 <= n; q += 4) {
-        float4 v[4];
+      for (int u = 0; u < 4; ++u)
+        v[u] = *reinterpret_cast<const float4 *>(base + (size_t)(q + u * groups) * pstride);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = *reinterpret_cast<const float4 *>(base + (size_t)(q + u) * pstride);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float w = s_w[q + u];
-          if (w != 0.f) {   // an empty partial may hold anything
-            acc[k].x += w * v[u].x;
-            acc[k].y += w * v[u].y;
-            acc[k].z += w * v[u].z;
-            acc[k].w += w * v[u].w;
-          }
+      for (int u = 0; u < 4; ++u) {
+        const float w = s_w[q + u * groups];
+        if (w != 0.f) {   // an empty partial may hold anything
+          acc.x += w * v[u].x;
+          acc.y += w * v[u].y;
+          acc.z += w * v[u].z;
+          acc.w += w * v[u].w;
         }
       }
-      for (; q < n; ++q) {
-        const float w = s_w[q];
-        if (w == 0.f) continue;
-        float4 v = *reinterpret_cast<const float4 *>(base + (size_t)q * pstride);
-        acc[k].x += w * v.x;
-        acc[k].y += w * v.y;
-        acc[k].z += w * v.z;
-        acc[k].w += w * v.w;
-      }
+    }
+    for (; q < n; q += groups) {
+      const float w = s_w[q];
+      if (w == 0.f) continue;
+      const float4 v = *reinterpret_cast<const float4 *>(base + (size_t)q * pstride);
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+      acc.z += w * v.z;
+      acc.w += w * v.w;
     }
   }
-  const float inv = 1.f / wsum;
-#pragma unroll
-  for (int k = 0; k < kCols; ++k) {
-    const int d = (k * kThreads + tid) * 4;
-    if (d >= D) break;
-    store4(out, out_fp32, out_off + d,
-           make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv));
+  // the groups' sums of each column, added in group order
+  s_acc[tid] = acc;
+  __syncthreads();
+  if (grp == 0 && col < cols) {
+    float4 t = s_acc[col];
+    for (int k = 1; k < groups; ++k) {
+      const float4 u = s_acc[k * cols + col];
+      t.x += u.x;
+      t.y += u.y;
+      t.z += u.z;
+      t.w += u.w;
+    }
+    const float inv = 1.f / wsum;
+    store4(out, out_fp32, out_off + 4 * col, make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv));
   }
   if (lse_out && tid == 0) lse_out[lse_off] = M + __logf(wsum);
 }
