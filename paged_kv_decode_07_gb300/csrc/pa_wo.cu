@@ -9,7 +9,9 @@
 // on the tensor cores (mma.sync m16n8k16, bf16 operands, fp32
 // accumulation) so that the issue slots stay free for the copies.  o is
 // fp32; it enters the MMA as two bf16 terms hi = bf16(o), lo = bf16(o - hi)
-// (o - hi - lo is below 2^-16 |o|), W exactly.
+// (o - hi - lo is below 2^-16 |o|), W exactly.  Each o chunk is split once
+// per CTA into bf16 hi / lo tiles in shared memory, from which every warp
+// takes its A fragments by ldmatrix.
 //
 // Grid: (N / 256 column tiles) x (k splits) x (64-row blocks of M), about
 // one CTA per SM.  A CTA of 4 warps streams its W[k range, 256 columns]
@@ -42,7 +44,10 @@ template <int MT>
 struct WoGeo {
   static constexpr int ABox = MT * 16 * 128;
   static constexpr int Stage = kWoWBytes + 2 * ABox;   // multiple of 1024
-  static constexpr int Smem = kWoStages * Stage + 1024;
+  // the current chunk's o as bf16 hi and lo tiles [MT * 16 rows][64 k],
+  // 128-byte rows with the 128-byte swizzle (conflict-free ldmatrix)
+  static constexpr int XTile = MT * 16 * 128;
+  static constexpr int Smem = kWoStages * Stage + 2 * XTile + 1024;
   static_assert(Stage % 1024 == 0, "swizzled boxes need 1024-byte alignment");
 };
 
@@ -63,6 +68,13 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
 }
 
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint32_t &r1,
@@ -154,6 +166,8 @@ __global__ void __launch_bounds__(kWoThreads) wo_kernel(const WoParams p,
   const int lm_k = ((lane >> 3) & 1) * 8 + (lane & 7);   // + 16 ks for k16 step ks
   const int lm_n = (lane >> 4) * 8;   // + 16 h for the h-th x4
 
+  uint8_t *const xhi = smem + kWoStages * Gm::Stage, *const xlo = xhi + Gm::XTile;
+  const uint32_t xhi_s = smem_u32(xhi), xlo_s = smem_u32(xlo);
   int issued = pro;
   for (int c = 0; c < nch; ++c) {
     const bool ok = mbar_wait(&bars[c % kWoStages], (c / kWoStages) & 1);
@@ -167,6 +181,22 @@ __global__ void __launch_bounds__(kWoThreads) wo_kernel(const WoParams p,
     const uint8_t *st = smem + (c % kWoStages) * Gm::Stage;
     const uint32_t wbase = smem_u32(st) + warp * kWoBoxBytes;   // this warp's box
     const uint8_t *abase = st + kWoWBytes;
+    // o of the chunk -> bf16 hi and lo tiles, each element once per CTA:
+    // thread i takes 8 consecutive k of one row (one 16-byte piece of each tile)
+    for (int i = tid; i < MT * 16 * 8; i += kWoThreads) {
+      const int row = i >> 3, kc = i & 7;
+      const float4 x0 = *reinterpret_cast<const float4 *>(abase + a_off<MT>(row, kc * 8));
+      const float4 x1 = *reinterpret_cast<const float4 *>(abase + a_off<MT>(row, kc * 8 + 4));
+      uint32_t hi[4], lo[4];
+      split_bf16(make_float2(x0.x, x0.y), hi[0], lo[0]);
+      split_bf16(make_float2(x0.z, x0.w), hi[1], lo[1]);
+      split_bf16(make_float2(x1.x, x1.y), hi[2], lo[2]);
+      split_bf16(make_float2(x1.z, x1.w), hi[3], lo[3]);
+      const int off = row * 128 + ((kc ^ (row & 7)) << 4);
+      *reinterpret_cast<uint4 *>(xhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4 *>(xlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    __syncthreads();   // the chunk's hi / lo tiles are complete
 #pragma unroll
     for (int ks = 0; ks < kWoK / 16; ++ks) {
       const int kr = ks * 16 + lm_k;
@@ -179,13 +209,14 @@ __global__ void __launch_bounds__(kWoThreads) wo_kernel(const WoParams p,
       }
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        const int r = mt * 16 + g, k = ks * 16 + 2 * t;
+        // A fragments: matrix i = lanes 8i .. 8i + 7 -> rows (l & 7) + 8 ((l >> 3) & 1),
+        // k chunk 2 ks + (l >> 4)
+        const int ar = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int akc = 2 * ks + (lane >> 4);
+        const uint32_t aoff = (uint32_t)(ar * 128 + ((akc ^ (ar & 7)) << 4));
         uint32_t ah[4], al[4];
-        split_bf16(*reinterpret_cast<const float2 *>(abase + a_off<MT>(r, k)), ah[0], al[0]);
-        split_bf16(*reinterpret_cast<const float2 *>(abase + a_off<MT>(r + 8, k)), ah[1], al[1]);
-        split_bf16(*reinterpret_cast<const float2 *>(abase + a_off<MT>(r, k + 8)), ah[2], al[2]);
-        split_bf16(*reinterpret_cast<const float2 *>(abase + a_off<MT>(r + 8, k + 8)), ah[3],
-                   al[3]);
+        ldsm_x4(xhi_s + aoff, ah[0], ah[1], ah[2], ah[3]);
+        ldsm_x4(xlo_s + aoff, al[0], al[1], al[2], al[3]);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint32_t b0 = b[j >> 1][2 * (j & 1)], b1 = b[j >> 1][2 * (j & 1) + 1];
