@@ -5,40 +5,43 @@
 // W_O GEMV, with a K-parallel split, CUTE_WO_SPLIT).
 //
 // At decode sizes (M = tokens <= a few dozen, K = Hq * D, N = hidden) the
-// product streams W once: it is bound by HBM, not by arithmetic, and runs
-// on the tensor cores (mma.sync m16n8k16, bf16 operands, fp32
-// accumulation) so that the issue slots stay free for the copies.  o is
-// fp32; it enters the MMA as two bf16 terms hi = bf16(o), lo = bf16(o - hi)
-// (o - hi - lo is below 2^-16 |o|), W exactly.  Each o chunk is split once
-// per CTA into bf16 hi / lo tiles in shared memory, from which every warp
-// takes its A fragments by ldmatrix.
+// product streams W once: it is bound by HBM, not by arithmetic.  It runs on
+// the tcgen05 tensor cores with the accumulators in tensor memory, in the
+// transposed form y^T = W^T . o^T:
+//   A = W^T [M = 128 hidden columns x K = 16] straight from the TMA boxes of
+//       W (bf16, MN-major: W rows are k, contiguous in the hidden index);
+//   B = o^T [K = 16 x N = 2 rows]: o is fp32 and enters as two bf16 terms,
+//       hi = bf16(o) and lo = bf16(o - hi) (o - hi - lo is below 2^-16 |o|),
+//       stacked as the N = 2 x rows columns of one K-major operand, so that one
+//       MMA takes both terms; y = column r + column rows + r.
+// W enters exactly.
 //
 // Grid: (N / 256 column tiles) x (k splits) x (64-row blocks of M), about
-// one CTA per SM.  A CTA of 4 warps streams its W[k range, 256 columns]
-// (four 64-column TMA boxes per 64-deep k chunk, 128-byte swizzle) and
-// o[64 rows, k range] through a 4-stage mbarrier ring; warp w owns columns
-// 64 w .. 64 w + 63 over the whole k range, so no sums are exchanged and
-// each o chunk is read once per 256 columns (the wider the tile, the fewer
-// times the 4-byte o is re-read from L2 next to the 2-byte W).  Split
-// partials go to the workspace and a second kernel adds them in fixed
+// one CTA per SM.  A CTA streams its W[k range, 256 columns] (four
+// 64-column TMA boxes per 64-deep k chunk, 128-byte swizzle) and o[rows,
+// k range] through a 4-stage mbarrier ring.  Warp 0 lane 0 issues the copies
+// and, per chunk, 2 x 4 MMAs (two M = 128 tiles, four k16 steps) into two
+// tensor-memory accumulators; warps 1-3 convert each o chunk into the bf16
+// hi / lo tiles (double-buffered) meanwhile; all four warps read the
+// accumulators at the end.  Each o chunk is read once per 256 columns.
+// Split partials go to the workspace and a second kernel adds them in fixed
 // order (deterministic).  With programmatic dependent launch the W tiles of
 // the first stages are requested before the attention's output is complete.
-#include "pa_decode_mma.cuh"
+#include "pa_verify_umma.cuh"   // tcgen05 helpers (pa::umma)
 
 namespace pa {
 namespace {
 
 constexpr int kWoThreads = 128;
-constexpr int kWoWarps = 4;
 constexpr int kWoBoxN = 64;    // columns per TMA box of W (128 bytes of bf16)
 constexpr int kWoBoxes = 4;    // boxes per chunk: 256 columns per CTA
 constexpr int kWoN = kWoBoxes * kWoBoxN;
-constexpr int kWoWarpN = kWoN / kWoWarps;   // 64 columns (8 n8 tiles) per warp
 constexpr int kWoK = 64;       // k per chunk: four k16 steps
 constexpr int kWoStages = 4;
 constexpr int kWoRows = 64;    // rows of o per CTA at most (4 m16 tiles)
 constexpr int kWoBoxBytes = kWoK * kWoBoxN * 2;      // 8 KB
 constexpr int kWoWBytes = kWoBoxes * kWoBoxBytes;    // 32 KB
+constexpr uint32_t kWoTmemCols = 256;   // two M = 128 tiles of up to N = 128 fp32 columns
 // one 32-k fp32 box of o holds MT * 16 rows of 128 bytes
 template <int MT>
 struct WoGeo {
@@ -47,7 +50,9 @@ struct WoGeo {
   // the current chunk's o as bf16 hi and lo tiles [MT * 16 rows][64 k],
   // 128-byte rows with the 128-byte swizzle (conflict-free ldmatrix)
   static constexpr int XTile = MT * 16 * 128;
-  static constexpr int Smem = kWoStages * Stage + 2 * XTile + 1024;
+  // two X buffers (hi and lo tiles each), so that a chunk's conversion does
+  // not wait for the previous chunk's MMAs
+  static constexpr int Smem = kWoStages * Stage + 4 * XTile + 1024;
   static_assert(Stage % 1024 == 0, "swizzled boxes need 1024-byte alignment");
 };
 
@@ -60,29 +65,6 @@ struct WoParams {
   int y_fp32;
   uint32_t *hdr;
 };
-
-__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                        uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint32_t &r1,
-                                              uint32_t &r2, uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
 
 // (x0, x1) -> bf16x2 hi (x0 in the low half) and the bf16x2 of the remainders
 __device__ __forceinline__ void split_bf16(float2 x, uint32_t &hi, uint32_t &lo) {
@@ -101,21 +83,50 @@ __device__ __forceinline__ int a_off(int row, int k) {
          ((k * 4) & 15);
 }
 
+// capped wait that also gives up once another thread of the CTA gave up
+__device__ __forceinline__ bool wo_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+#pragma unroll 1
+  for (uint32_t i = 0; i < kWaitCap; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+  }
+  *abort = 1;
+  return false;
+}
+
+// Warp 0 lane 0 issues the copies and the MMAs; warps 1-3 turn each o chunk
+// into the bf16 hi / lo tiles of the B operand.  Per chunk c (stage c % 4,
+// X buffer c % 2):
+//   full[st]  TMA -> converters (o box) and MMA thread (W boxes)
+//   xfull[b]  converters -> MMA thread (96 arrivals)
+//   xfree[b]  MMA commit -> converters (X b may be rewritten)
+//   done[st]  MMA commit -> the refill of stage st
+// All 4 warps read the accumulators in the epilogue (warp w: lanes 32 w ..).
 template <int MT>
-__global__ void __launch_bounds__(kWoThreads) wo_kernel(const WoParams p,
-                                                        const __grid_constant__ CUtensorMap tmW,
-                                                        const __grid_constant__ CUtensorMap tmA) {
+__global__ void __launch_bounds__(kWoThreads, 1) wo_kernel(const WoParams p,
+                                                           const __grid_constant__ CUtensorMap tmW,
+                                                           const __grid_constant__ CUtensorMap tmA) {
+  using namespace umma;
+  using Gm = WoGeo<MT>;
+  constexpr int kRows = MT * 16;       // rows of o per CTA
+  constexpr int kN = 2 * kRows;        // MMA N: hi rows, then lo rows
+  constexpr int kTiles = kWoN / 128;   // M = 128 column tiles of W per CTA
+  constexpr int kConv = kWoThreads - 32;   // converter threads (warps 1-3)
+  // instruction descriptor: D fp32, A and B bf16, A MN-major, B K-major
+  constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) |
+                              ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+  static_assert(kN % 16 == 0 && kN <= 128, "MMA N (two tiles fit the tensor-memory columns)");
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  __shared__ __align__(8) uint64_t bars[kWoStages];
-  __shared__ int s_fail;
+  __shared__ __align__(8) uint64_t full[kWoStages], done[kWoStages], xfull[2], xfree[2], fin;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  volatile int *const abort = &s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, t = lane & 3;
   const int nt = blockIdx.x % p.ntiles;
   const int s = (blockIdx.x / p.ntiles) % p.splits;
   const int mb = blockIdx.x / (p.ntiles * p.splits);
-  using Gm = WoGeo<MT>;
   const int n0 = nt * kWoN, m0 = mb * kWoRows;
   const int c0 = s * p.chunks_per_split;
   const int nch = max(0, min(p.chunks_per_split, p.K / kWoK - c0));
@@ -124,140 +135,160 @@ __global__ void __launch_bounds__(kWoThreads) wo_kernel(const WoParams p,
   const int rot = nch > 0 ? (nt * 5) % nch : 0;
 
   if (tid == 0) {
-    for (int i = 0; i < kWoStages; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < kWoStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&done[i], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&xfull[b], kConv);
+      mbar_init(&xfree[b], 1);
+    }
+    mbar_init(&fin, 1);
     fence_mbar_init();
-    s_fail = 0;
+    s_abort = 0;
   }
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, kWoTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
-  const uint64_t pol = policy_evict_first();   // W: read once
-  const uint64_t pol_o = policy_evict_last();   // o: read by every column tile
-  auto chunk_k = [&](int c) { return (c0 + (c + rot) % nch) * kWoK; };
-  auto issue_w = [&](int c) {   // thread 0: W rows of the c-th chunk, four boxes
-    uint8_t *st = smem + (c % kWoStages) * Gm::Stage;
-    mbar_arrive_expect_tx(&bars[c % kWoStages], Gm::Stage);
-#pragma unroll
-    for (int w = 0; w < kWoBoxes; ++w)
-      tc::tma_rows(st + w * kWoBoxBytes, &tmW, n0 + w * kWoBoxN, chunk_k(c), &bars[c % kWoStages],
-                   pol);
-  };
-  auto issue_a = [&](int c) {   // thread 0: o rows m0 .. m0 + 16 MT - 1, two 32-k boxes
-    uint8_t *st = smem + (c % kWoStages) * Gm::Stage + kWoWBytes;
-    const int k = chunk_k(c);
-    tc::tma_rows(st, &tmA, k, m0, &bars[c % kWoStages], pol_o);
-    tc::tma_rows(st + Gm::ABox, &tmA, k + 32, m0, &bars[c % kWoStages], pol_o);
-  };
-  const int pro = min(kWoStages, nch);
-  if (tid == 0)
-    for (int c = 0; c < pro; ++c) issue_w(c);   // W does not depend on the attention
-  griddep_wait();                                // o of this call is complete
-  if (tid == 0)
-    for (int c = 0; c < pro; ++c) issue_a(c);
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  uint8_t *const xbase = smem + kWoStages * Gm::Stage;   // X[b]: hi rows then lo rows
 
-  // warp w: columns 64 w .. 64 w + 63 (8 n8 tiles), every k16 step
-  float acc[MT][8][4];
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();   // W: read once
+      const uint64_t pol_o = policy_evict_last();   // o: read by every column tile
+      auto chunk_k = [&](int c) { return (c0 + (c + rot) % nch) * kWoK; };
+      auto issue = [&](int c, bool w_part, bool o_part) {
+        uint8_t *st = smem + (c % kWoStages) * Gm::Stage;
+        if (w_part) {
+          mbar_arrive_expect_tx(&full[c % kWoStages], Gm::Stage);
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
+          for (int w = 0; w < kWoBoxes; ++w)
+            tc::tma_rows(st + w * kWoBoxBytes, &tmW, n0 + w * kWoBoxN, chunk_k(c),
+                         &full[c % kWoStages], pol);
+        }
+        if (o_part) {   // o rows m0 .. m0 + 16 MT - 1, two 32-k boxes
+          const int k = chunk_k(c);
+          tc::tma_rows(st + kWoWBytes, &tmA, k, m0, &full[c % kWoStages], pol_o);
+          tc::tma_rows(st + kWoWBytes + Gm::ABox, &tmA, k + 32, m0, &full[c % kWoStages], pol_o);
+        }
+      };
+      const int pro = min(kWoStages, nch);
+      for (int c = 0; c < pro; ++c) issue(c, true, false);   // W does not depend on the attention
+      griddep_wait();                                         // o of this call is complete
+      for (int c = 0; c < pro; ++c) issue(c, false, true);
+      int issued = pro, mmas = 0;
+      for (int c = 0; c < nch; ++c) {
+        const int st = c % kWoStages;
+        if (!wo_wait(&full[st], (c / kWoStages) & 1, abort) ||
+            !wo_wait(&xfull[c & 1], (c >> 1) & 1, abort))
+          break;
+        tc_fence_after();
+        const uint32_t wst = smem_u32(smem + st * Gm::Stage);
+        const uint32_t xb = smem_u32(xbase + (c & 1) * 2 * Gm::XTile);
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+        for (int mi = 0; mi < kTiles; ++mi)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[mt][j][e] = 0.f;
-
-  // ldmatrix.trans row address: thread i -> matrix i / 8 = (k half, n half), row i % 8
-  const int lm_k = ((lane >> 3) & 1) * 8 + (lane & 7);   // + 16 ks for k16 step ks
-  const int lm_n = (lane >> 4) * 8;   // + 16 h for the h-th x4
-
-  uint8_t *const xhi = smem + kWoStages * Gm::Stage, *const xlo = xhi + Gm::XTile;
-  const uint32_t xhi_s = smem_u32(xhi), xlo_s = smem_u32(xlo);
-  int issued = pro;
-  for (int c = 0; c < nch; ++c) {
-    const bool ok = mbar_wait(&bars[c % kWoStages], (c / kWoStages) & 1);
-    if (__syncthreads_or(!ok)) {
-      if (tid == 0) {
-        set_err(p.hdr, PA_ERRF_WAIT_TIMEOUT);
-        s_fail = 1;
+          for (int ks = 0; ks < kWoK / 16; ++ks) {
+            // A = W^T of columns 128 mi .. + 127 (two 64-column boxes LBO
+            // apart, 8-row k groups 1024 bytes apart), chunk rows 16 ks .. + 15
+            const uint64_t ad = sdesc(wst + 2 * mi * kWoBoxBytes + ks * 2048, kWoBoxBytes, 1024);
+            // B = [hi; lo] rows, k 16 ks .. + 15: 32 bytes into each 128-byte row
+            const uint64_t bd = sdesc(xb + ks * 32, 16, 1024);
+            mma_ss(tmem + (uint32_t)(mi * kN), ad, bd, kIdesc, (c > 0 || ks > 0) ? 1u : 0u);
+          }
+        tc_commit(&done[st]);       // the stage may be refilled once these MMAs completed
+        tc_commit(&xfree[c & 1]);   // and X[c % 2] rewritten
+        ++mmas;
+        // refill the previous chunk's stage: its o box was converted (its xfull
+        // was waited for) and its W is read once its MMAs are done
+        if (c >= 1 && issued < nch) {
+          const int pc = c - 1;
+          if (!wo_wait(&done[pc % kWoStages], (pc / kWoStages) & 1, abort)) break;
+          issue(issued, true, true);
+          ++issued;
+        }
       }
-      break;
+      // every MMA complete before the accumulators are read (and released);
+      // the copies still in flight land before the CTA exits
+      tc_commit(&fin);
+      (void)mbar_wait(&fin, 0);
+      for (int c = max(issued - kWoStages, mmas); c < issued; ++c)
+        (void)mbar_wait(&full[c % kWoStages], (c / kWoStages) & 1);
+      if (*abort) set_err(p.hdr, PA_ERRF_WAIT_TIMEOUT);
     }
-    const uint8_t *st = smem + (c % kWoStages) * Gm::Stage;
-    const uint32_t wbase = smem_u32(st) + warp * kWoBoxBytes;   // this warp's box
-    const uint8_t *abase = st + kWoWBytes;
-    // o of the chunk -> bf16 hi and lo tiles, each element once per CTA:
-    // thread i takes 8 consecutive k of one row (one 16-byte piece of each tile)
-    for (int i = tid; i < MT * 16 * 8; i += kWoThreads) {
-      const int row = i >> 3, kc = i & 7;
-      const float4 x0 = *reinterpret_cast<const float4 *>(abase + a_off<MT>(row, kc * 8));
-      const float4 x1 = *reinterpret_cast<const float4 *>(abase + a_off<MT>(row, kc * 8 + 4));
-      uint32_t hi[4], lo[4];
-      split_bf16(make_float2(x0.x, x0.y), hi[0], lo[0]);
-      split_bf16(make_float2(x0.z, x0.w), hi[1], lo[1]);
-      split_bf16(make_float2(x1.x, x1.y), hi[2], lo[2]);
-      split_bf16(make_float2(x1.z, x1.w), hi[3], lo[3]);
-      const int off = row * 128 + ((kc ^ (row & 7)) << 4);
-      *reinterpret_cast<uint4 *>(xhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4 *>(xlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
-    __syncthreads();   // the chunk's hi / lo tiles are complete
-#pragma unroll
-    for (int ks = 0; ks < kWoK / 16; ++ks) {
-      const int kr = ks * 16 + lm_k;
-      uint32_t b[4][4];   // four ldmatrix.x4: n8 tiles (2h, 2h + 1)
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int n = lm_n + 16 * h;
-        ldsm_x4_trans(wbase + kr * 128 + (((n >> 3) ^ (kr & 7)) << 4), b[h][0], b[h][1], b[h][2],
-                      b[h][3]);
+    __syncwarp();
+  } else {
+    // converters: o of chunk c -> bf16 hi and lo tiles, each element once per
+    // CTA; thread i takes 8 consecutive k of one row (one 16-byte piece of each)
+    const int ct = tid - 32;
+    for (int c = 0; c < nch; ++c) {
+      const int st = c % kWoStages;
+      if (!wo_wait(&full[st], (c / kWoStages) & 1, abort)) break;
+      if (c >= 2 && !wo_wait(&xfree[c & 1], ((c >> 1) - 1) & 1, abort)) break;
+      const uint8_t *abase = smem + st * Gm::Stage + kWoWBytes;
+      uint8_t *const xhi = xbase + (c & 1) * 2 * Gm::XTile, *const xlo = xhi + Gm::XTile;
+      for (int i = ct; i < kRows * 8; i += kConv) {
+        const int row = i >> 3, kc = i & 7;
+        const float4 x0 = *reinterpret_cast<const float4 *>(abase + a_off<MT>(row, kc * 8));
+        const float4 x1 = *reinterpret_cast<const float4 *>(abase + a_off<MT>(row, kc * 8 + 4));
+        uint32_t hi[4], lo[4];
+        split_bf16(make_float2(x0.x, x0.y), hi[0], lo[0]);
+        split_bf16(make_float2(x0.z, x0.w), hi[1], lo[1]);
+        split_bf16(make_float2(x1.x, x1.y), hi[2], lo[2]);
+        split_bf16(make_float2(x1.z, x1.w), hi[3], lo[3]);
+        const int off = row * 128 + ((kc ^ (row & 7)) << 4);
+        *reinterpret_cast<uint4 *>(xhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(xlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
+      fence_async_smem();   // generic-proxy writes of X -> visible to the tensor cores
+      mbar_arrive(&xfull[c & 1]);
+    }
+  }
+  __syncthreads();   // the MMA thread has seen `fin`
+  tc_fence_after();
+  if (!*abort) {
+    // warp w reads tensor-memory lanes 32 w .. + 31: W columns n0 + 128 mi + 32 w + lane;
+    // column r of the tile is token row r of hi, column kRows + r of lo
+#pragma unroll 1
+    for (int mi = 0; mi < kTiles; ++mi) {
+      const int n = n0 + 128 * mi + 32 * warp + lane;
+      const uint32_t ta = tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(mi * kN);
+#pragma unroll 1
+      for (int r0 = 0; r0 < kRows; r0 += 16) {
+        float h[16], l[16];
+        if (nch > 0) {   // warp-uniform
+          tmem_ld16(ta + r0, h);
+          tmem_ld16(ta + kRows + r0, l);
+        } else {
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        // A fragments: matrix i = lanes 8i .. 8i + 7 -> rows (l & 7) + 8 ((l >> 3) & 1),
-        // k chunk 2 ks + (l >> 4)
-        const int ar = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int akc = 2 * ks + (lane >> 4);
-        const uint32_t aoff = (uint32_t)(ar * 128 + ((akc ^ (ar & 7)) << 4));
-        uint32_t ah[4], al[4];
-        ldsm_x4(xhi_s + aoff, ah[0], ah[1], ah[2], ah[3]);
-        ldsm_x4(xlo_s + aoff, al[0], al[1], al[2], al[3]);
+          for (int j = 0; j < 16; ++j) h[j] = l[j] = 0.f;
+        }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t b0 = b[j >> 1][2 * (j & 1)], b1 = b[j >> 1][2 * (j & 1) + 1];
-          mma_bf16(acc[mt][j], ah[0], ah[1], ah[2], ah[3], b0, b1);
-          mma_bf16(acc[mt][j], al[0], al[1], al[2], al[3], b0, b1);
+        for (int j = 0; j < 16; ++j) {
+          const int m = m0 + r0 + j;
+          if (m >= p.M || n >= p.N) continue;
+          const float v = h[j] + l[j];
+          if (p.splits > 1)
+            p.part[((size_t)s * p.M + m) * p.N + n] = v;
+          else if (p.y_fp32)
+            static_cast<float *>(p.y)[(size_t)m * p.N + n] = v;
+          else
+            static_cast<__nv_bfloat16 *>(p.y)[(size_t)m * p.N + n] = __float2bfloat16_rn(v);
         }
       }
     }
-    __syncthreads();   // stage consumed by every warp
-    if (tid == 0 && issued < nch) {
-      issue_w(issued);
-      issue_a(issued);
-      ++issued;
-    }
   }
-  if (s_fail) {   // only the last fill of each stage can still be in flight
-    if (tid == 0)
-      for (int c = max(issued - kWoStages, 0); c < issued; ++c)
-        (void)mbar_wait(&bars[c % kWoStages], (c / kWoStages) & 1);
-    return;
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kWoTmemCols);
   }
-  // ---- this warp's 64 columns, straight from the accumulators
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int m = m0 + mt * 16 + g + 8 * hh;
-        const int n = n0 + warp * kWoWarpN + j * 8 + 2 * t;   // N is a multiple of 8: n + 1 < N too
-        if (m >= p.M || n >= p.N) continue;
-        const float v0 = acc[mt][j][2 * hh], v1 = acc[mt][j][2 * hh + 1];
-        if (p.splits > 1)
-          *reinterpret_cast<float2 *>(p.part + ((size_t)s * p.M + m) * p.N + n) = make_float2(v0, v1);
-        else if (p.y_fp32)
-          *reinterpret_cast<float2 *>(static_cast<float *>(p.y) + (size_t)m * p.N + n) =
-              make_float2(v0, v1);
-        else
-          *reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(p.y) + (size_t)m * p.N + n) =
-              __floats2bfloat162_rn(v0, v1);
-      }
 }
 
 // y = sum over splits of the partials, in split order
