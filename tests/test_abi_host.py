@@ -214,3 +214,9 @@ def test_single_launch_kernel_choice_is_checked_on_the_host(L):
     assert call(L, "pa_decode", kv_struct(), prob_struct(), opts=opts(5), ws=None) == pa.PA_ERR_INVALID_ARG
     assert call(L, "pa_decode", kv_struct(), prob_struct(), opts=opts(5),
                 ws_bytes=128) == pa.PA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_group_sizes_without_a_kernel_are_refused(L):
+    """G = 3 (or 5, 7) query heads per kv head has no kernel instantiation: refused on the host."""
+    for Hq, hkv in ((12, 4), (20, 4), (28, 4)):
+        assert call(L, "pa_decode", kv_struct(hkv=hkv), prob_struct(Hq=Hq)) == pa.PA_ERR_UNSUPPORTED
