@@ -25,10 +25,12 @@
 //
 // One persistent CTA per SM walks its work items (the planner's split-K
 // partitions) with warp-specialised roles:
-//   warp 0       producer: TMA copies of each 16-token block's K / V codes
-//                (and NVFP4 block scales) into a ring of raw stages
+//   warps 0, 3   producers (K side, V side): TMA copies of each 16-token
+//                block's codes (and NVFP4 block scales) into rings of raw
+//                stages; the two sides sit in different warps so that a
+//                wait on one ring never holds back the copies of the other
 //   warp 1       tensor-memory allocation; one thread issues the QK MMAs
-//   warps 2, 3   one thread each issues the PV MMAs of one head-dim half
+//   warp 2       one thread issues the PV MMAs (both head-dim halves)
 //   warps 4-7    K dequant: token row t of the tile -> TMEM lane t (f16x2)
 //   warps 8-15   softmax, two groups of 4 warps, each with half of the N
 //                columns: S^T from tensor memory, masks, online softmax in
@@ -36,7 +38,9 @@
 //                shared memory; at the end of an item O^T / l to the output
 //                or to the split-K partials (merged afterwards)
 //   warps 16-19  V dequant: token rows -> the f16 V tile in shared memory
-//                (MN-major A operand layout)
+//                (MN-major A operand layout), one half tile (64 tokens) at
+//                a time, two threads per row, so that the PV MMAs of one
+//                half run while the other half is dequantised
 // A warp reaches the tensor-memory lanes 32 (warp % 4) .. + 31, so each
 // group of 4 consecutive warps covers all 128 lanes.
 // Hand-offs are mbarriers (tcgen05.commit for the MMA side); every wait is
@@ -362,7 +366,7 @@ constexpr int kMaxNR = 32;
 struct Ctl {
   uint64_t rkfull[kMaxNR], rkfree[kMaxNR];     // K raw stages: TMA -> K dequant
   uint64_t rvfull[kMaxNR], rvfree[kMaxNR];     // V raw stages: TMA -> V dequant
-  uint64_t vfull, vfree;                       // f16 V tile: V dequant <-> PV
+  uint64_t vfull[2], vfree[2];                 // f16 V half tiles: V dequant <-> PV
   uint64_t kfull[2], kfree[2];                 // K buffers in tensor memory: K dequant <-> QK
   uint64_t sfull[2], sfree[2];                 // S buffers: QK <-> softmax
   uint64_t pfull[2], pdone[2];                 // P buffers: softmax <-> PV
@@ -456,12 +460,12 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
 
 // ------------------------------------------------------------------ roles
 
-// warp 0: lane j (0-7) copies the K side of block j of every tile into K
-// stage (tile % NRK) * 8 + j, lane 8 + j the V side into V stage
-// (tile % NRV) * 8 + j (code tiles by 2-D TMA with 128-byte swizzle, NVFP4
-// block scales by 1-D bulk copies).  One lane per block position and side
-// issues a tile's copies in parallel and keeps its stage counters and the
-// next tile's block id in registers.
+// warp 0 (K side) or warp 3 (V side): lane j (0-7) copies its side of block
+// j of every tile into stage (tile % NRK) * 8 + j (K) or (tile % NRV) * 8 +
+// j (V) (code tiles by 2-D TMA with 128-byte swizzle, NVFP4 block scales by
+// 1-D bulk copies).  One lane per block position issues a tile's copies in
+// parallel and keeps its stage counters and the next tile's block id in
+// registers.
 template <int DT, int N>
 __device__ void role_producer(const AttnParams &p, const CUtensorMap *tmK, const CUtensorMap *tmV,
                               uint8_t *smem, Ctl &c, int num_items, int jt, int side) {
@@ -565,19 +569,23 @@ __device__ void role_qk(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t tme
   drain_wait(&c.done, 0);
 }
 
-// warps 2 and 3, one thread each: O^T[half h] += V^T(g)[half h] . P^T(g) per
-// 16-token block (each issuing thread is limited to about one MMA per 100+
-// cycles whatever N, so the two head-dim halves of PV go to two threads;
-// V-free, P-done and O-done take one commit from each)
+// warp 2, one thread: O^T[half h] += V^T(g)[half h] . P^T(g) per 16-token
+// block and head-dim half h (the MMAs of a block run at the tensor pipe's
+// rate for shared-memory operands, about 95 cycles each at N <= 48, so one
+// issuing thread keeps up).  The V tile arrives in two half tiles of four
+// blocks: the MMAs of a half start once its dequant is done, and the half's
+// buffer is handed back once they complete.
 template <int DT, int N>
 __device__ void role_pv(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t tmem,
-                        int num_items, int h) {
+                        int num_items) {
   using Gm = Geo<DT, N>;
   constexpr uint32_t IPV = idesc_f16(kTile, N, true);
   const uint32_t sP = smem_u32(smem + Gm::OFF_P);
   const uint64_t dP0 = sdesc(sP, 16, 1024), dP1 = sdesc(sP + Gm::PBUF, 16, 1024);
-  const uint64_t dV = sdesc(smem_u32(smem + Gm::OFF_V) + h * 4096, 2048, 1024);
-  const uint32_t dO = tmem + kColO + h * 64;
+  // head-dim half 1 starts 4 KB (two 64-wide chunks) into each block's slot
+  const uint64_t dV = sdesc(smem_u32(smem + Gm::OFF_V), 2048, 1024);
+  constexpr uint64_t kHalf1 = 4096 >> 4;
+  const uint32_t dO = tmem + kColO;
   uint32_t g = 0, oi = 0;
   bool ok = true;
   for (int ii = blockIdx.x; ii < num_items && ok; ii += gridDim.x) {
@@ -587,21 +595,29 @@ __device__ void role_pv(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t tme
       const int nb = min(kTileBlocks, x.n_blk - tile * kTileBlocks);
       const bool first = tile == 0;
       if (!wait_bar(&c.pfull[g & 1], (g >> 1) & 1, c, p.hdr) ||
-          (first && !wait_bar(&c.ofree, (oi & 1) ^ 1, c, p.hdr)) ||
-          !wait_bar(&c.vfull, g & 1, c, p.hdr)) {
+          (first && !wait_bar(&c.ofree, (oi & 1) ^ 1, c, p.hdr))) {
         ok = false;
         break;
       }
-      tc_fence_after();
       const uint64_t dP = (g & 1) ? dP1 : dP0;
 #pragma unroll 1
-      for (int j = 0; j < nb; ++j) {
-        const uint64_t bd = dP + (uint64_t)(((j >> 2) * Gm::QCH + (j & 3) * 32) >> 4);
-        const uint64_t ad = dV + (uint64_t)((j * Gm::VSLOT) >> 4);
-        const uint32_t acc = (first && j == 0) ? 0u : 1u;
-        mma_ss(dO, ad, bd, IPV, acc);
+      for (int hh = 0; hh < 2; ++hh) {   // half tiles: blocks 4 hh .. 4 hh + 3
+        if (!wait_bar(&c.vfull[hh], g & 1, c, p.hdr)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int j = 4 * hh; j < min(nb, 4 * hh + 4); ++j) {
+          const uint64_t bd = dP + (uint64_t)(((j >> 2) * Gm::QCH + (j & 3) * 32) >> 4);
+          const uint64_t ad = dV + (uint64_t)((j * Gm::VSLOT) >> 4);
+          const uint32_t acc = (first && j == 0) ? 0u : 1u;
+          mma_ss(dO, ad, bd, IPV, acc);
+          mma_ss(dO + 64, ad + kHalf1, bd, IPV, acc);
+        }
+        tc_commit(&c.vfree[hh]);
       }
-      tc_commit(&c.vfree);
+      if (!ok) break;
       tc_commit(&c.pdone[g & 1]);
       if (tile == x.ntiles - 1) tc_commit(&c.odone);
     }
@@ -613,21 +629,22 @@ __device__ void role_pv(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t tme
 
 
 // Token row r of a raw stage dequantised to f16, 32 head-dim elements at a
-// time: sink(u, h) gets h[k] = (element 32u + 2k, element 32u + 2k + 1) as
-// f16x2 (low half first).  An invalid row yields zeros (codes and scales
+// time (the 64-element pieces u2b .. u2e - 1 of the row, all of it by
+// default): sink(u, h) gets h[k] = (element 32u + 2k, element 32u + 2k + 1)
+// as f16x2 (low half first).  An invalid row yields zeros (codes and scales
 // are not read: poisoned slots may hold NaN scales).  Every lane runs the
 // same instruction sequence whether its row is valid or not (zeros are
 // selected, not branched to): a K sink is a warp-wide tcgen05.st, which
 // all 32 lanes must execute together.
 template <int DT, int UU, typename Sink>
 __device__ __forceinline__ void deq_row(uint32_t st, int code_off, int scale_off, int r,
-                                        bool valid, Sink &&sink) {
+                                        bool valid, Sink &&sink, int u2b = 0, int u2e = 4) {
   static_assert(UU == 1 || UU == 2, "chunks in flight");
   const uint4 z = make_uint4(0, 0, 0, 0);
   if constexpr (DT == PA_KV_NVFP4) {
     // chunks 2 u2 and 2 u2 + 1 use the row's scale bytes 4 u2 .. 4 u2 + 3
 #pragma unroll 1
-    for (int u2 = 0; u2 < 4; ++u2) {
+    for (int u2 = u2b; u2 < u2e; ++u2) {
       const uint32_t sw = valid ? lds_u32(st + scale_off + r * 16 + 4 * u2) : 0u;
       uint32_t sd[4];
       tc::e4m3x2_dup(sw & 0xffffu, sd[0], sd[1]);
@@ -655,7 +672,7 @@ __device__ __forceinline__ void deq_row(uint32_t st, int code_off, int scale_off
     }
   } else {   // FP8-E4M3: one byte per element, exact in f16
 #pragma unroll 1
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 2 * u2b; u < 2 * u2e; ++u) {
       const uint4 w0 = valid ? lds_u4(st + code_off + tc::sw_off(r, 32 * u)) : z;
       const uint4 w1 = valid ? lds_u4(st + code_off + tc::sw_off(r, 32 * u + 16)) : z;
       const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -757,49 +774,60 @@ __device__ void role_kdeq(const AttnParams &p, uint8_t *smem, Ctl &c, uint32_t t
   }
 }
 
-// warps 16-19: token row r of each block -> the block's f16 V slot, laid out
-// [64-wide head-dim chunk][16 tokens][128 bytes, swizzled] (MN-major A of PV)
+// warps 16-19: the V tile in two half tiles of four blocks; in half hh warp
+// w takes block 4 hh + w, lane l row l % 16 and head-dim half l / 16 of it
+// -> the block's f16 V slot, laid out [64-wide head-dim chunk][16 tokens]
+// [128 bytes, swizzled] (MN-major A of PV)
 template <int DT, int N>
 __device__ void role_vdeq(const AttnParams &p, uint8_t *smem, Ctl &c, int num_items, int warp,
                           int lane) {
   using Gm = Geo<DT, N>;
-  const int t = (warp & 3) * 32 + lane, jb = t >> 4, r = t & 15;
-  uint32_t g = 0, ru[Gm::NRV] = {};   // uses of this row's raw stages
+  const int w = warp & 3, r = lane & 15, dh = lane >> 4;
+  uint32_t g = 0, ru[2][Gm::NRV] = {};   // uses of this thread's raw stages, per half
   bool ok = true;
   for (int ii = blockIdx.x; ii < num_items && ok; ii += gridDim.x) {
     const Item x = load_item(p, ii);
     if (x.n_blk == 0) continue;
     for (int tile = 0; tile < x.ntiles && ok; ++tile, ++g) {
       const int nb = min(kTileBlocks, x.n_blk - tile * kTileBlocks);
-      // the V tile buffer is free once PV of the previous tile completed
-      ok = wait_bar(&c.vfree, (g & 1) ^ 1, c, p.hdr);
-      if (!ok) break;
-      if (jb < nb) {
-        const uint32_t tp = g % Gm::NRV;
-        const int s = (int)tp * kTileBlocks + jb, vs = jb;
-        uint32_t use = 0;
-#pragma unroll
-        for (int i = 0; i < Gm::NRV; ++i)
-          if (i == (int)tp) use = ru[i];
-        ok = wait_bar(&c.rvfull[s], use & 1, c, p.hdr);
+      const uint32_t tp = g % Gm::NRV;
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        const int jb = 4 * hh + w;
+        // the half's buffer is free once its MMAs of the previous tile completed
+        ok = wait_bar(&c.vfree[hh], (g & 1) ^ 1, c, p.hdr);
         if (!ok) break;
+        if (jb < nb) {
+          const int s = (int)tp * kTileBlocks + jb;
+          uint32_t use = 0;
 #pragma unroll
-        for (int i = 0; i < Gm::NRV; ++i)
-          if (i == (int)tp) ++ru[i];
-        const int tok = x.t_begin + (tile * kTileBlocks + jb) * kBlock + r;
-        const bool valid = c.rvvalid[s] != 0 && tok < x.t_end;
-        const uint32_t vsl = smem_u32(smem) + Gm::OFF_V + vs * Gm::VSLOT + r * 128;
-        deq_row<DT, 2>(smem_u32(smem) + Gm::OFF_RV + tp * Gm::RSIDE, jb * Gm::CODE, Gm::R_SC + jb * Gm::SC,
-                    r, valid, [&](int u, const uint32_t(&h)[16]) {
+          for (int i = 0; i < Gm::NRV; ++i)
+            if (i == (int)tp) use = hh ? ru[1][i] : ru[0][i];
+          ok = wait_bar(&c.rvfull[s], use & 1, c, p.hdr);
+          if (!ok) break;
 #pragma unroll
-                      for (int w = 0; w < 4; ++w)
-                        sts_u4(vsl + (u >> 1) * 2048 + (((((u & 1) << 2) + w) ^ (r & 7)) << 4),
-                               h[4 * w], h[4 * w + 1], h[4 * w + 2], h[4 * w + 3]);
-                    });
-        fence_async_smem();
-        mbar_arrive(&c.rvfree[s]);
+          for (int i = 0; i < Gm::NRV; ++i)
+            if (i == (int)tp) {
+              if (hh) ++ru[1][i];
+              else ++ru[0][i];
+            }
+          const int tok = x.t_begin + (tile * kTileBlocks + jb) * kBlock + r;
+          const bool valid = c.rvvalid[s] != 0 && tok < x.t_end;
+          const uint32_t vsl = smem_u32(smem) + Gm::OFF_V + jb * Gm::VSLOT + r * 128;
+          deq_row<DT, 2>(smem_u32(smem) + Gm::OFF_RV + tp * Gm::RSIDE, jb * Gm::CODE,
+                         Gm::R_SC + jb * Gm::SC, r, valid,
+                         [&](int u, const uint32_t(&h)[16]) {
+#pragma unroll
+                           for (int q = 0; q < 4; ++q)
+                             sts_u4(vsl + (u >> 1) * 2048 + (((((u & 1) << 2) + q) ^ (r & 7)) << 4),
+                                    h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+                         },
+                         2 * dh, 2 * dh + 2);
+          fence_async_smem();
+          mbar_arrive(&c.rvfree[s]);
+        }
+        mbar_arrive(&c.vfull[hh]);   // every V thread, every half tile
       }
-      mbar_arrive(&c.vfull);   // every V thread, every tile
     }
   }
 }
@@ -1129,22 +1157,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int s = 0; s < Gm::NRV * kTileBlocks; ++s) {
       mbar_init(&c.rvfull[s], 1);
-      mbar_init(&c.rvfree[s], kBlock);   // the block's 16 V rows
+      mbar_init(&c.rvfree[s], 2 * kBlock);   // the block's 16 V rows, two threads each
     }
-    mbar_init(&c.vfull, 128);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&c.vfull[h], 128);   // every V thread
+      mbar_init(&c.vfree[h], 1);     // the PV thread's commit
+    }
     mbar_init(&c.ofree, 256);   // both softmax groups
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c.sfull[i], 1);
       mbar_init(&c.sfree[i], 256);
       mbar_init(&c.pfull[i], 256);
-      mbar_init(&c.pdone[i], 2);   // both PV threads
+      mbar_init(&c.pdone[i], 1);
       mbar_init(&c.kfull[i], 128);
       mbar_init(&c.kfree[i], 1);
     }
-    mbar_init(&c.done, 3);   // one commit from each MMA-issuing thread
-    mbar_init(&c.vfree, 2);  // one commit from each PV thread
-    mbar_init(&c.odone, 2);
+    mbar_init(&c.done, 2);   // one commit from each MMA-issuing thread
+    mbar_init(&c.odone, 1);
     c.abort = 0;
     fence_mbar_init();
   }
@@ -1160,16 +1191,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int wg = warp >> 2;   // warpgroup
   if (wg == 0) {
     setmaxnreg_to<kLaunchRegs, kRegCtl>();
-    if (warp == 0) {
-      if (lane < 2 * kTileBlocks)
-        role_producer<DT, N>(p, &tmK, &tmV, smem, c, num_items, lane & (kTileBlocks - 1),
-                             lane / kTileBlocks);
+    if (warp == 0 || warp == 3) {
+      if (lane < kTileBlocks)
+        role_producer<DT, N>(p, &tmK, &tmV, smem, c, num_items, lane, warp == 3 ? 1 : 0);
       __syncwarp();
     } else if (warp == 1) {
       if (lane == 0) role_qk<DT, N>(p, smem, c, tmem, num_items);
       __syncwarp();
     } else {
-      if (lane == 0) role_pv<DT, N>(p, smem, c, tmem, num_items, warp - 2);
+      if (lane == 0) role_pv<DT, N>(p, smem, c, tmem, num_items);
       __syncwarp();
     }
   } else if (wg == 1) {

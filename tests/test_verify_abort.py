@@ -8,8 +8,8 @@ as it sees the flag, each role leaves its loops, and before the CTA exits
   * each producer lane waits for the last fill it issued into each of its
     stages (a TMA copy still in flight would write into memory the CTA no
     longer owns);
-  * the three MMA-issuing threads commit to a common barrier and wait for
-    it, so that no tensor-core operation still reads or writes tensor memory.
+  * the two MMA-issuing threads commit to a common barrier and wait for it,
+    so that no tensor-core operation still reads or writes tensor memory.
 Copies and MMA completions are asynchronous here: a DMA agent lands issued
 copies in random order and one agent per issuing thread retires its MMAs in
 order (commit arrivals with them).  A role's n-th wait on a pending barrier
@@ -39,17 +39,17 @@ class AbortKernel:
         self.rkfull = [Bar(1) for _ in range(TB * nrk)]
         self.rkfree = [Bar(16) for _ in range(TB * nrk)]
         self.rvfull = [Bar(1) for _ in range(TB * nrv)]
-        self.rvfree = [Bar(16) for _ in range(TB * nrv)]
-        self.vfull, self.vfree = Bar(TB * 16), Bar(2)
+        self.rvfree = [Bar(32) for _ in range(TB * nrv)]
+        self.vfull, self.vfree = [Bar(128), Bar(128)], [Bar(1), Bar(1)]
         self.kfull, self.kfree = [Bar(128), Bar(128)], [Bar(1), Bar(1)]
         self.sfull, self.sfree = [Bar(1), Bar(1)], [Bar(256), Bar(256)]
-        self.pfull, self.pdone = [Bar(256), Bar(256)], [Bar(2), Bar(2)]
-        self.odone, self.ofree, self.done = Bar(2), Bar(256), Bar(3)
+        self.pfull, self.pdone = [Bar(256), Bar(256)], [Bar(1), Bar(1)]
+        self.odone, self.ofree, self.done = Bar(1), Bar(256), Bar(2)
         self.abort = False
         self.err = False
         self.pending_waits = {}
         self.inflight = []                        # (lane, barrier) of issued copies
-        self.mma = {"qk": [], "pv0": [], "pv1": []}   # per issuing thread: commits in order
+        self.mma = {"qk": [], "pv": []}   # per issuing thread: commits in order
 
     # -- waits
     def wait_bar(self, bar, parity, who):
@@ -126,18 +126,22 @@ class AbortKernel:
         self.mma["qk"].append(self.done)
         yield from self.drain_wait(self.done, 0)
 
-    def pv(self, h):
-        who, ok, oi = f"pv{h}", True, 0
+    def pv(self):
+        who, ok, oi = "pv", True, 0
         for tl in self.items_tiles():
             for g, ti, nt, _ in tl:
                 ok = (yield from self.wait_bar(self.pfull[g & 1], (g >> 1) & 1, who))
                 if ok and ti == 0:
                     ok = yield from self.wait_bar(self.ofree, (oi & 1) ^ 1, who)
-                if ok:
-                    ok = yield from self.wait_bar(self.vfull, g & 1, who)
+                for hh in range(2):
+                    if not ok:
+                        break
+                    ok = yield from self.wait_bar(self.vfull[hh], g & 1, who)
+                    if ok:
+                        self.mma[who].append(self.vfree[hh])
                 if not ok:
                     break
-                self.mma[who] += [self.vfree, self.pdone[g & 1]]
+                self.mma[who].append(self.pdone[g & 1])
                 if ti == nt - 1:
                     self.mma[who].append(self.odone)
             if not ok:
@@ -166,21 +170,24 @@ class AbortKernel:
                     self.rkfree[s].arrive(16)
                     use[s] += 1
 
-    def vdeq(self, jb):
-        who, use = f"vdeq{jb}", [0] * self.nrv
+    def vdeq(self, w):
+        who, use = f"vdeq{w}", [[0] * self.nrv, [0] * self.nrv]
         for tl in self.items_tiles():
             for g, _, _, nb in tl:
-                ok = yield from self.wait_bar(self.vfree, (g & 1) ^ 1, who)
-                if not ok:
-                    return
-                if jb < nb:
-                    st = g % self.nrv
-                    ok = yield from self.wait_bar(self.rvfull[st * TB + jb], use[st] & 1, who)
+                for hh in range(2):
+                    jb = 4 * hh + w
+                    ok = yield from self.wait_bar(self.vfree[hh], (g & 1) ^ 1, who)
                     if not ok:
                         return
-                    use[st] += 1
-                    self.rvfree[st * TB + jb].arrive(16)
-                self.vfull.arrive(16)
+                    if jb < nb:
+                        st = g % self.nrv
+                        ok = yield from self.wait_bar(self.rvfull[st * TB + jb], use[hh][st] & 1,
+                                                      who)
+                        if not ok:
+                            return
+                        use[hh][st] += 1
+                        self.rvfree[st * TB + jb].arrive(32)
+                    self.vfull[hh].arrive(32)
 
     def softmax(self, half):
         who, oi = f"soft{half}", 0
@@ -218,9 +225,9 @@ class AbortKernel:
         rng = random.Random(seed)
         roles = {f"prodK{j}": self.producer("K", j) for j in range(TB)}
         roles.update({f"prodV{j}": self.producer("V", j) for j in range(TB)})
-        roles.update({"qk": self.qk(), "pv0": self.pv(0), "pv1": self.pv(1), "kdeq": self.kdeq(),
+        roles.update({"qk": self.qk(), "pv": self.pv(), "kdeq": self.kdeq(),
                       "soft0": self.softmax(0), "soft1": self.softmax(1)})
-        roles.update({f"vdeq{j}": self.vdeq(j) for j in range(TB)})
+        roles.update({f"vdeq{w}": self.vdeq(w) for w in range(4)})
         engines = {"dma": self.dma(rng)}
         engines.update({f"mma_{w}": self.mma_engine(w) for w in self.mma})
         blocked = {a: None for a in roles}
@@ -256,7 +263,7 @@ class AbortKernel:
 
 
 ITEMS = [[20, 3, 9, 1, 8, 64, 0, 5, 17], [40, 40, 40], [1, 1, 2, 3], [128, 7, 0, 64]]
-ROLES = ["prodK0", "prodK5", "prodV3", "qk", "pv0", "pv1", "kdeq", "vdeq2", "soft0", "soft1"]
+ROLES = ["prodK0", "prodK5", "prodV3", "qk", "pv", "kdeq", "vdeq1", "vdeq3", "soft0", "soft1"]
 
 
 @pytest.mark.parametrize("nrk,nrv", [(4, 2), (2, 1)])    # NVFP4 and FP8 ring sizes

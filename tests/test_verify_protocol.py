@@ -10,11 +10,13 @@ the data flow itself: no buffer is read before it is written or overwritten
 before its reader is done.  A wrong wait parity, a missing wait or a wrong
 arrival count therefore fails an assert or deadlocks (both reported).
 
-Roles (per CTA): producer lanes 0-7 (K side of block j) and 8-15 (V side),
-each with its own ring of raw stages (stage = (tile % rings) * 8 + j); the QK
-issuer; two PV issuers (one head-dim half each); the K dequant group; the V
-dequant rows of each block position; two softmax groups (half of the columns
-each).  Items are lists of 16-token block counts; a tile is 8 blocks.
+Roles (per CTA): K-side producer lanes 0-7 and V-side producer lanes 0-7
+(block j of a tile), each side with its own ring of raw stages (stage =
+(tile % rings) * 8 + j); the QK issuer; the PV issuer, which takes the V tile
+in two half tiles of four blocks; the K dequant group; the four V dequant
+warps (warp w dequantises block w of the first half tile, then block 4 + w of
+the second); two softmax groups (half of the columns each).  Items are lists
+of 16-token block counts; a tile is 8 blocks.
 """
 import random
 
@@ -48,15 +50,16 @@ class Kernel:
         self.rkfull = [Bar(1) for _ in range(TB * nrk)]
         self.rkfree = [Bar(16) for _ in range(TB * nrk)]      # the block's 16 K rows
         self.rvfull = [Bar(1) for _ in range(TB * nrv)]
-        self.rvfree = [Bar(16) for _ in range(TB * nrv)]      # the block's 16 V rows
-        self.vfull, self.vfree = Bar(TB * 16), Bar(2)         # all V rows; both PV issuers
+        self.rvfree = [Bar(32) for _ in range(TB * nrv)]      # 16 V rows, two threads each
+        self.vfull = [Bar(128), Bar(128)]                     # every V thread, per half tile
+        self.vfree = [Bar(1), Bar(1)]                         # the PV issuer, per half tile
         self.kfull = [Bar(128), Bar(128)]
         self.kfree = [Bar(1), Bar(1)]
         self.sfull = [Bar(1), Bar(1)]
         self.sfree = [Bar(256), Bar(256)]                     # both softmax groups
         self.pfull = [Bar(256), Bar(256)]
-        self.pdone = [Bar(2), Bar(2)]                         # both PV issuers
-        self.odone, self.ofree = Bar(2), Bar(256)
+        self.pdone = [Bar(1), Bar(1)]                         # the PV issuer
+        self.odone, self.ofree = Bar(1), Bar(256)
         self.log = set()
 
     @staticmethod
@@ -104,19 +107,20 @@ class Kernel:
             self.sfull[g & 1].arrive()
             self.kfree[g & 1].arrive()
 
-    def pv(self, h):
+    def pv(self):
         oi = 0
         for g, ti, nt, nb in self.tiles_of_items():
             yield from self.wait(self.pfull[g & 1], (g >> 1) & 1)
             if ti == 0:
                 yield from self.wait(self.ofree, (oi & 1) ^ 1)
-            yield from self.wait(self.vfull, g & 1)
             assert ("p", g, 0) in self.log and ("p", g, 1) in self.log, "PV before P"
-            for j in range(nb):
-                assert ("v", g, j) in self.log, "PV before V"
-                assert ("v", g + 1, j) not in self.log, "V overwritten before PV read it"
-            self.log.add(("pv", g, h))
-            self.vfree.arrive()
+            for hh in range(2):
+                yield from self.wait(self.vfull[hh], g & 1)
+                for j in range(4 * hh, min(nb, 4 * hh + 4)):
+                    assert ("v", g, j) in self.log, "PV before V"
+                    assert ("v", g + 1, j) not in self.log, "V overwritten before PV read it"
+                self.log.add(("pv", g, hh))
+                self.vfree[hh].arrive()
             self.pdone[g & 1].arrive()
             if ti == nt - 1:
                 self.odone.arrive()
@@ -143,21 +147,23 @@ class Kernel:
                 self.rkfree[s].arrive(16)
                 use[s] += 1
 
-    def vdeq(self, jb):
-        use = [0] * self.nrv
+    def vdeq(self, w):
+        use = [[0] * self.nrv, [0] * self.nrv]
         for g, _, _, nb in self.tiles_of_items():
-            yield from self.wait(self.vfree, (g & 1) ^ 1)
-            if g >= 1:
-                assert ("pv", g - 1, 0) in self.log and ("pv", g - 1, 1) in self.log
-            if jb < nb:
-                st = g % self.nrv
-                yield from self.wait(self.rvfull[st * TB + jb], use[st] & 1)
-                assert ("fillV", g, jb) in self.log, "V dequant before its copy"
-                self.log.add(("v", g, jb))
-                self.log.add(("readV", g, jb))
-                self.rvfree[st * TB + jb].arrive(16)
-                use[st] += 1
-            self.vfull.arrive(16)
+            for hh in range(2):
+                jb = 4 * hh + w
+                yield from self.wait(self.vfree[hh], (g & 1) ^ 1)
+                if g >= 1:
+                    assert ("pv", g - 1, hh) in self.log, "V half overwritten before PV read it"
+                if jb < nb:
+                    st = g % self.nrv
+                    yield from self.wait(self.rvfull[st * TB + jb], use[hh][st] & 1)
+                    assert ("fillV", g, jb) in self.log, "V dequant before its copy"
+                    self.log.add(("v", g, jb))
+                    self.log.add(("readV", g, jb))
+                    self.rvfree[st * TB + jb].arrive(32)
+                    use[hh][st] += 1
+                self.vfull[hh].arrive(32)
 
     def softmax(self, half):
         oi = 0
@@ -165,7 +171,7 @@ class Kernel:
             yield from self.wait(self.sfull[g & 1], (g >> 1) & 1)
             yield from self.wait(self.pdone[g & 1], ((g >> 1) & 1) ^ 1)
             assert ("qk", g) in self.log, "softmax before S"
-            if g >= 2:   # the P buffer of tile g - 2 was read by both PV issuers
+            if g >= 2:   # the P buffer of tile g - 2 was read by both halves of PV
                 assert ("pv", g - 2, 0) in self.log and ("pv", g - 2, 1) in self.log
             if ti > 0 and ti % 3 == 1:   # a redo: O^T is rescaled after PV(g - 1)
                 yield from self.wait(self.pdone[(g - 1) & 1], ((g - 1) >> 1) & 1)
@@ -182,9 +188,9 @@ class Kernel:
     def run(self, seed):
         agents = {f"prodK{j}": self.producer("K", j) for j in range(TB)}
         agents.update({f"prodV{j}": self.producer("V", j) for j in range(TB)})
-        agents.update({"qk": self.qk(), "pv0": self.pv(0), "pv1": self.pv(1), "kdeq": self.kdeq(),
+        agents.update({"qk": self.qk(), "pv": self.pv(), "kdeq": self.kdeq(),
                        "soft0": self.softmax(0), "soft1": self.softmax(1)})
-        agents.update({f"vdeq{j}": self.vdeq(j) for j in range(TB)})
+        agents.update({f"vdeq{w}": self.vdeq(w) for w in range(4)})
         blocked = {a: None for a in agents}
         alive = set(agents)
         rng = random.Random(seed)
@@ -226,17 +232,46 @@ def test_model_catches_a_missing_wait():
     """The model is not vacuous: a V dequant that skips its wait for the
     previous PV overwrites V before it is read."""
     class Broken(Kernel):
-        def vdeq(self, jb):
-            use = [0] * self.nrv
+        def vdeq(self, w):
+            use = [[0] * self.nrv, [0] * self.nrv]
             for g, _, _, nb in self.tiles_of_items():
-                if jb < nb:
-                    st = g % self.nrv
-                    yield from self.wait(self.rvfull[st * TB + jb], use[st] & 1)
-                    self.log.add(("v", g, jb))
-                    self.rvfree[st * TB + jb].arrive(16)
-                    use[st] += 1
-                self.vfull.arrive(16)
+                for hh in range(2):
+                    jb = 4 * hh + w
+                    if jb < nb:
+                        st = g % self.nrv
+                        yield from self.wait(self.rvfull[st * TB + jb], use[hh][st] & 1)
+                        self.log.add(("v", g, jb))
+                        self.rvfree[st * TB + jb].arrive(32)
+                        use[hh][st] += 1
+                    self.vfull[hh].arrive(32)
 
     with pytest.raises(AssertionError):
         for seed in range(40):
+            Broken([40, 40, 40], 4, 2).run(seed)
+
+
+def test_model_catches_a_missing_half_tile_wait():
+    """A PV issuer that waits for the first half tile of V only reads the
+    second half before its dequant wrote it (under some schedules)."""
+    class Broken(Kernel):
+        def pv(self):
+            oi = 0
+            for g, ti, nt, nb in self.tiles_of_items():
+                yield from self.wait(self.pfull[g & 1], (g >> 1) & 1)
+                if ti == 0:
+                    yield from self.wait(self.ofree, (oi & 1) ^ 1)
+                for hh in range(2):
+                    if hh == 0:
+                        yield from self.wait(self.vfull[hh], g & 1)
+                    for j in range(4 * hh, min(nb, 4 * hh + 4)):
+                        assert ("v", g, j) in self.log, "PV before V"
+                    self.log.add(("pv", g, hh))
+                    self.vfree[hh].arrive()
+                self.pdone[g & 1].arrive()
+                if ti == nt - 1:
+                    self.odone.arrive()
+                    oi += 1
+
+    with pytest.raises(AssertionError):
+        for seed in range(60):
             Broken([40, 40, 40], 4, 2).run(seed)
