@@ -223,20 +223,28 @@ __device__ __forceinline__ unsigned long long sel_key(float s, int j) {
 // The keys are unique, so the top n are exactly the keys >= the n-th
 // largest, which is found bit by bit from the top: keep a bit when at least
 // n keys are >= the prefix with it set (warp ballots, per-warp counts in
-// shared memory, one barrier per bit).  While the score word is searched
-// the prefix's index word is 0, so comparing score words alone gives the
-// same counts; when exactly n keys then reach the score prefix (no tie at
-// the boundary) it is the answer and the index word is not searched.
-// Index bits 31..12 are 1 in every key (index < 4096) and are not searched.
-// A bitmap of the winners gives each one its rank in ascending block order.
+// shared memory, one barrier per bit).  The bits above the highest one in
+// which the valid score words differ are common to all of them and are not
+// searched (one AND / OR reduction first), and the search stops as soon as
+// exactly n keys reach the prefix.  While the score word is searched the
+// prefix's index word is 0, so comparing score words alone gives the same
+// counts; when exactly n keys reach the score prefix (no tie at the
+// boundary) it is the answer and the index word is not searched.  Index
+// bits 31..12 are 1 in every key (index < 4096) and are not searched.
+// A bitmap of the winners gives each one its rank in ascending block order;
+// the winners' block-table entries are then gathered with all of a thread's
+// loads in flight before its stores.
 __global__ void __launch_bounds__(kSelThreads) select_kernel(
     const int *tables, int stride, const int *seq_lens, int B, int H, int sb, int max_nsb,
     int top_k, const float *scores, int *selected, int *vtables, int vstride, int *vlens,
     int num_blocks, uint32_t *err) {
   constexpr int kPer = 4096 / kSelThreads;   // keys per thread
   constexpr int kWarpsSel = kSelThreads / 32;
+  constexpr int kGather = 8;                 // table entries in flight per thread
   __shared__ uint32_t s_flag[4096 / 32], s_wpre[4096 / 32];
   __shared__ int s_cnt[2][kWarpsSel];
+  __shared__ uint32_t s_and[kWarpsSel], s_or[kWarpsSel];
+  __shared__ int s_rank[4096];               // rank -> sparse block index
   const int b = blockIdx.x / H, h = blockIdx.x % H;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int L = seq_len_of(seq_lens, b, stride * kBlock);
@@ -254,14 +262,31 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   const int n = min(top_k, nsb);
   const float *sc = scores + ((size_t)b * H + h) * max_nsb;
   uint32_t khi[kPer], klo[kPer];   // score word, index word; 0 / 0 is below every real key
+  uint32_t kand = 0xFFFFFFFFu, kor = 0u;   // over this thread's valid score words
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int j = tid + i * kSelThreads;
     const unsigned long long k = j < nsb ? sel_key(sc[j], j) : 0ull;
     khi[i] = (uint32_t)(k >> 32);
     klo[i] = (uint32_t)k;
+    if (j < nsb) {
+      kand &= khi[i];
+      kor |= khi[i];
+    }
   }
   for (int i = tid; i < 4096 / 32; i += kSelThreads) s_flag[i] = 0;
+  kand = __reduce_and_sync(0xffffffffu, kand);
+  kor = __reduce_or_sync(0xffffffffu, kor);
+  if (lane == 0) {
+    s_and[warp] = kand;
+    s_or[warp] = kor;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < kWarpsSel; ++w) {
+    kand &= s_and[w];
+    kor |= s_or[w];
+  }
   // the n-th largest key (n < nsb), else 0 / 0 = take all
   uint32_t thr_hi = 0, thr_lo = 0;
   int buf = 0;
@@ -280,11 +305,21 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     return tot;
   };
   if (n < nsb) {
-    for (int bit = 31; bit >= 0; --bit) {   // the score word
+    // every valid score word has the bits above `top` of kand; every key
+    // that is not valid is 0 and below them all
+    const uint32_t diff = kand ^ kor;
+    const int top = diff ? 31 - __clz(diff) : -1;
+    thr_hi = top < 0 ? kand : top < 31 ? (kand & ~((2u << top) - 1u)) : 0u;
+    bool exact = false;   // exactly n keys reach thr_hi
+    for (int bit = top; bit >= 0 && !exact; --bit) {   // the score word
       const uint32_t cand = thr_hi | (1u << bit);
-      if (count_ge([&](int i) { return khi[i] >= cand; }) >= n) thr_hi = cand;
+      const int c = count_ge([&](int i) { return khi[i] >= cand; });
+      if (c >= n) {
+        thr_hi = cand;
+        exact = c == n;
+      }
     }
-    if (count_ge([&](int i) { return khi[i] >= thr_hi; }) != n) {   // a tie at the boundary
+    if (!exact && count_ge([&](int i) { return khi[i] >= thr_hi; }) != n) {   // a tie at the boundary
       thr_lo = 0xFFFFF000u;
       for (int bit = 11; bit >= 0; --bit) {   // the index word
         const uint32_t cand = thr_lo | (1u << bit);
@@ -316,20 +351,36 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     }
   }
   __syncthreads();
-  const int bps = sb / kBlock;   // 16-token blocks per sparse block
-  const int nblk = (L + kBlock - 1) / kBlock;
   const size_t vrow = (size_t)b * H + h;
   for (int j = tid; j < nsb; j += kSelThreads) {
     const uint32_t w = s_flag[j >> 5];
     if (!((w >> (j & 31)) & 1u)) continue;
     const int r = (int)(s_wpre[j >> 5] + __popc(w & ((1u << (j & 31)) - 1u)));
+    s_rank[r] = j;
     if (selected) selected[vrow * top_k + r] = j;
-    for (int i = 0; i < bps; ++i) {
-      const int lb = j * bps + i;
-      if (lb >= nblk) break;
-      const int phys = tables[(size_t)b * stride + lb];
-      vtables[vrow * vstride + r * bps + i] =
-          (phys >= 0 && phys < num_blocks) ? phys * H + h : -1;
+  }
+  __syncthreads();
+  // block-table entries of the winners: entry (r, i) = 16-token block i of
+  // the rank-r winner; all of a thread's loads are issued before its stores
+  const int bps = sb / kBlock;   // 16-token blocks per sparse block
+  const int nblk = (L + kBlock - 1) / kBlock;
+  const int total = n * bps;
+  const int *trow = tables + (size_t)b * stride;
+  int *vrow_t = vtables + vrow * vstride;
+  for (int e0 = 0; e0 < total; e0 += kGather * kSelThreads) {
+    int phys[kGather];
+    bool have[kGather];   // an entry of a block inside the sequence
+#pragma unroll
+    for (int k = 0; k < kGather; ++k) {
+      const int e = e0 + k * kSelThreads + tid;
+      const int lb = e < total ? s_rank[e / bps] * bps + e % bps : nblk;
+      have[k] = lb < nblk;
+      phys[k] = have[k] ? trow[lb] : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < kGather; ++k) {
+      const int e = e0 + k * kSelThreads + tid;
+      if (have[k]) vrow_t[e] = (phys[k] >= 0 && phys[k] < num_blocks) ? phys[k] * H + h : -1;
     }
   }
   if (selected)

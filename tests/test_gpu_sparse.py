@@ -156,3 +156,55 @@ def test_selection_ties_go_to_the_lower_index():
     _, sel, _ = pa.decode_sparse(kv, wl.q, wl.block_tables, wl.seq_lens, wl.softmax_scale,
                                  means.contiguous(), SB, 3, return_selected=True)
     assert (sel.cpu() == torch.tensor([2, 5, 7], dtype=torch.int32)).all()
+
+
+def test_selection_when_every_score_is_equal():
+    """Every sparse block has the same mean key, so every score is the same
+    number: the top k are blocks 0 .. k - 1 (ties to the lower index), for a
+    k below, at and above the number of blocks."""
+    wl = W.make_workload(NAMES["int8"], device=DEV, seq_lens=[1280, 1000])
+    M = 20
+    g = torch.Generator(device="cpu").manual_seed(5)
+    row = torch.randn(wl.D, generator=g)
+    means = row.expand(wl.B, M, wl.Hkv, wl.D).contiguous().to(DEV)
+    kv = pa.KvCache.from_workload(wl)
+    nsb = _nsb([1280, 1000])
+    for k in (1, 7, 16, 20, 25):
+        _, sel, _ = pa.decode_sparse(kv, wl.q, wl.block_tables, wl.seq_lens, wl.softmax_scale,
+                                     means, SB, k, return_selected=True)
+        sel = sel.cpu().numpy()
+        for b in range(wl.B):
+            n = min(k, nsb[b])
+            for h in range(wl.Hkv):
+                assert np.array_equal(sel[b, h, :n], np.arange(n)), (k, b, h)
+                assert (sel[b, h, n:] == -1).all(), (k, b, h)
+
+
+def test_selection_with_negative_and_mixed_sign_scores():
+    """Scores of both signs and all negative: the order of the sign-folded
+    keys must be the order of the scores."""
+    wl = W.make_workload(NAMES["int8"], device=DEV, seq_lens=[1280, 1280])
+    M = 20
+    G = wl.Hq // wl.Hkv
+    g = torch.Generator(device="cpu").manual_seed(9)
+    coef = torch.randn(wl.B, M, wl.Hkv, generator=g)
+    coef[1] = -coef[1].abs() - 0.5                          # sequence 1: every score negative
+    kv = pa.KvCache.from_workload(wl)
+    means = torch.empty(wl.B, M, wl.Hkv, wl.D)
+    qf = wl.q[:, 0].float().cpu()                            # [B, Hq, D]
+    for b in range(wl.B):
+        for h in range(wl.Hkv):
+            # nearly along every head of the group, so each head's dot has
+            # the sign of coef and so has the score (their max)
+            direction = qf[b, h * G:(h + 1) * G].sum(0)
+            direction = direction / direction.norm()
+            means[b, :, h] = coef[b, :, h, None] * direction
+    means = means.to(DEV).contiguous()
+    k = 6
+    _, sel, _ = pa.decode_sparse(kv, wl.q, wl.block_tables, wl.seq_lens, wl.softmax_scale,
+                                 means, SB, k, return_selected=True)
+    _, _, _, qb = compact_host(wl, list(range(wl.B)))
+    scores, _ = oracle.sparse_select(qb, wl.Hkv, means.cpu().numpy().astype(np.float64),
+                                     np.array(_nsb([1280, 1280]), np.int32), k)
+    assert (scores[1, :, :20] < 0).all() and (scores[0, :, :20] > 0).any()
+    check_selection(sel.cpu().numpy(), scores, _nsb([1280, 1280]), k, "mixed signs")
