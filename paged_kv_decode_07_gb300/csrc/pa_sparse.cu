@@ -261,12 +261,20 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   }
   const int n = min(top_k, nsb);
   const float *sc = scores + ((size_t)b * H + h) * max_nsb;
+  // the score row is read up to max_nsb whatever the length (in flight
+  // together with the length)
+  float sv[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int j = tid + i * kSelThreads;
+    sv[i] = j < max_nsb ? sc[j] : 0.f;
+  }
   uint32_t khi[kPer], klo[kPer];   // score word, index word; 0 / 0 is below every real key
   uint32_t kand = 0xFFFFFFFFu, kor = 0u;   // over this thread's valid score words
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int j = tid + i * kSelThreads;
-    const unsigned long long k = j < nsb ? sel_key(sc[j], j) : 0ull;
+    const unsigned long long k = j < nsb ? sel_key(sv[i], j) : 0ull;
     khi[i] = (uint32_t)(k >> 32);
     klo[i] = (uint32_t)k;
     if (j < nsb) {
