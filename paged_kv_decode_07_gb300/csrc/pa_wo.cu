@@ -19,11 +19,15 @@
 // Grid: (N / 256 column tiles) x (k splits) x (64-row blocks of M), about
 // one CTA per SM.  A CTA streams its W[k range, 256 columns] (four
 // 64-column TMA boxes per 64-deep k chunk, 128-byte swizzle) and o[rows,
-// k range] through a 4-stage mbarrier ring.  Warp 0 lane 0 issues the copies
-// and, per chunk, 2 x 4 MMAs (two M = 128 tiles, four k16 steps) into two
-// tensor-memory accumulators; warps 1-3 convert each o chunk into the bf16
-// hi / lo tiles (double-buffered) meanwhile; all four warps read the
-// accumulators at the end.  Each o chunk is read once per 256 columns.
+// k range] through a 4-stage mbarrier ring.  Warp 4 lane 0 issues the
+// copies; warp 0 lane 0 issues, per chunk, 2 x 4 MMAs (two M = 128 tiles,
+// four k16 steps) into two tensor-memory accumulators; warps 1-3 convert
+// each o chunk into the bf16 hi / lo tiles (double-buffered) meanwhile;
+// warps 0-3 read the accumulators at the end.  Copies and MMAs are issued
+// by different threads because a chunk's six TMA instructions and its
+// eight MMAs, issued by one thread, took about 1.7 K cycles per 40 KB
+// chunk, which held the SM below a third of its share of DRAM bandwidth.
+// Each o chunk is read once per 256 columns.
 // Split partials go to the workspace and a second kernel adds them in fixed
 // order (deterministic).  With programmatic dependent launch the W tiles of
 // the first stages are requested before the attention's output is complete.
@@ -32,7 +36,8 @@
 namespace pa {
 namespace {
 
-constexpr int kWoThreads = 128;
+constexpr int kWoThreads = 160;   // warp 0 MMAs, warps 1-3 conversion, warp 4 copies
+constexpr int kWoConv = 96;       // converter threads (warps 1-3)
 constexpr int kWoBoxN = 64;    // columns per TMA box of W (128 bytes of bf16)
 constexpr int kWoBoxes = 4;    // boxes per chunk: 256 columns per CTA
 constexpr int kWoN = kWoBoxes * kWoBoxN;
@@ -94,14 +99,14 @@ __device__ __forceinline__ bool wo_wait(uint64_t *bar, uint32_t parity, volatile
   return false;
 }
 
-// Warp 0 lane 0 issues the copies and the MMAs; warps 1-3 turn each o chunk
-// into the bf16 hi / lo tiles of the B operand.  Per chunk c (stage c % 4,
-// X buffer c % 2):
+// Warp 4 lane 0 issues the copies, warp 0 lane 0 the MMAs; warps 1-3 turn
+// each o chunk into the bf16 hi / lo tiles of the B operand.  Per chunk c
+// (stage c % 4, X buffer c % 2):
 //   full[st]  TMA -> converters (o box) and MMA thread (W boxes)
 //   xfull[b]  converters -> MMA thread (96 arrivals)
 //   xfree[b]  MMA commit -> converters (X b may be rewritten)
-//   done[st]  MMA commit -> the refill of stage st
-// All 4 warps read the accumulators in the epilogue (warp w: lanes 32 w ..).
+//   done[st]  MMA commit -> the copy thread's refill of stage st
+// Warps 0-3 read the accumulators in the epilogue (warp w: lanes 32 w ..).
 template <int MT>
 __global__ void __launch_bounds__(kWoThreads, 1) wo_kernel(const WoParams p,
                                                            const __grid_constant__ CUtensorMap tmW,
@@ -111,7 +116,7 @@ __global__ void __launch_bounds__(kWoThreads, 1) wo_kernel(const WoParams p,
   constexpr int kRows = MT * 16;       // rows of o per CTA
   constexpr int kN = 2 * kRows;        // MMA N: hi rows, then lo rows
   constexpr int kTiles = kWoN / 128;   // M = 128 column tiles of W per CTA
-  constexpr int kConv = kWoThreads - 32;   // converter threads (warps 1-3)
+  constexpr int kConv = kWoConv;
   // instruction descriptor: D fp32, A and B bf16, A MN-major, B K-major
   constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) |
                               ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
@@ -134,7 +139,26 @@ __global__ void __launch_bounds__(kWoThreads, 1) wo_kernel(const WoParams p,
   // different chunk so that they do not all hit the same L2 lines at once
   const int rot = nch > 0 ? (nt * 5) % nch : 0;
 
-  if (tid == 0) {
+  const uint64_t pol = policy_evict_first();    // W: read once
+  const uint64_t pol_o = policy_evict_last();   // o: read by every column tile
+  auto chunk_k = [&](int c) { return (c0 + (c + rot) % nch) * kWoK; };
+  auto issue = [&](int c, bool w_part, bool o_part) {   // the copy thread only
+    uint8_t *st = smem + (c % kWoStages) * Gm::Stage;
+    if (w_part) {
+      mbar_arrive_expect_tx(&full[c % kWoStages], Gm::Stage);
+#pragma unroll
+      for (int w = 0; w < kWoBoxes; ++w)
+        tc::tma_rows(st + w * kWoBoxBytes, &tmW, n0 + w * kWoBoxN, chunk_k(c),
+                     &full[c % kWoStages], pol);
+    }
+    if (o_part) {   // o rows m0 .. m0 + 16 MT - 1, two 32-k boxes
+      const int k = chunk_k(c);
+      tc::tma_rows(st + kWoWBytes, &tmA, k, m0, &full[c % kWoStages], pol_o);
+      tc::tma_rows(st + kWoWBytes + Gm::ABox, &tmA, k + 32, m0, &full[c % kWoStages], pol_o);
+    }
+  };
+  const int pro = min(kWoStages, nch);
+  if (tid == 128) {   // the copy thread: barriers, then the first W tiles at once
     for (int i = 0; i < kWoStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&done[i], 1);
@@ -146,6 +170,7 @@ __global__ void __launch_bounds__(kWoThreads, 1) wo_kernel(const WoParams p,
     mbar_init(&fin, 1);
     fence_mbar_init();
     s_abort = 0;
+    for (int c = 0; c < pro; ++c) issue(c, true, false);   // W does not depend on the attention
   }
   if (warp == 0) {
     tmem_alloc(&s_tmem, kWoTmemCols);
@@ -157,68 +182,58 @@ __global__ void __launch_bounds__(kWoThreads, 1) wo_kernel(const WoParams p,
   const uint32_t tmem = s_tmem;
   uint8_t *const xbase = smem + kWoStages * Gm::Stage;   // X[b]: hi rows then lo rows
 
-  if (warp == 0) {
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();   // W: read once
-      const uint64_t pol_o = policy_evict_last();   // o: read by every column tile
-      auto chunk_k = [&](int c) { return (c0 + (c + rot) % nch) * kWoK; };
-      auto issue = [&](int c, bool w_part, bool o_part) {
-        uint8_t *st = smem + (c % kWoStages) * Gm::Stage;
-        if (w_part) {
-          mbar_arrive_expect_tx(&full[c % kWoStages], Gm::Stage);
-#pragma unroll
-          for (int w = 0; w < kWoBoxes; ++w)
-            tc::tma_rows(st + w * kWoBoxBytes, &tmW, n0 + w * kWoBoxN, chunk_k(c),
-                         &full[c % kWoStages], pol);
-        }
-        if (o_part) {   // o rows m0 .. m0 + 16 MT - 1, two 32-k boxes
-          const int k = chunk_k(c);
-          tc::tma_rows(st + kWoWBytes, &tmA, k, m0, &full[c % kWoStages], pol_o);
-          tc::tma_rows(st + kWoWBytes + Gm::ABox, &tmA, k + 32, m0, &full[c % kWoStages], pol_o);
-        }
-      };
-      const int pro = min(kWoStages, nch);
-      for (int c = 0; c < pro; ++c) issue(c, true, false);   // W does not depend on the attention
-      griddep_wait();                                         // o of this call is complete
+  if (warp == 4) {
+    if (lane == 0) {   // the copies (the first W tiles are in flight already)
+      griddep_wait();   // o of this call is complete
       for (int c = 0; c < pro; ++c) issue(c, false, true);
-      int issued = pro, mmas = 0;
+      int issued = pro;
+      // chunk c refills the stage of chunk c - 4 once its MMAs completed
+      for (; issued < nch; ++issued) {
+        const int pc = issued - kWoStages;
+        if (!wo_wait(&done[pc % kWoStages], (pc / kWoStages) & 1, abort)) break;
+        issue(issued, true, true);
+      }
+      // after a failure the copies still in flight (the last one of each
+      // stage at most) land before the CTA exits
+      if (*abort)
+        for (int c = max(issued - kWoStages, 0); c < issued; ++c)
+          (void)mbar_wait(&full[c % kWoStages], (c / kWoStages) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 0) {
+    if (lane == 0) {   // the MMAs
+      // descriptors are built once; an operand's start address (the low
+      // field, address >> 4) moves by a constant per stage, tile and k step
+      const uint64_t ad0 = sdesc(smem_u32(smem), kWoBoxBytes, 1024);
+      const uint64_t bd0 = sdesc(smem_u32(xbase), 16, 1024);
       for (int c = 0; c < nch; ++c) {
         const int st = c % kWoStages;
-        if (!wo_wait(&full[st], (c / kWoStages) & 1, abort) ||
-            !wo_wait(&xfull[c & 1], (c >> 1) & 1, abort))
+        // both completion checks issued before either result is used
+        const bool r1 = mbar_test(&full[st], (c / kWoStages) & 1);
+        const bool r2 = mbar_test(&xfull[c & 1], (c >> 1) & 1);
+        if (!(r1 || wo_wait(&full[st], (c / kWoStages) & 1, abort)) ||
+            !(r2 || wo_wait(&xfull[c & 1], (c >> 1) & 1, abort)))
           break;
         tc_fence_after();
-        const uint32_t wst = smem_u32(smem + st * Gm::Stage);
-        const uint32_t xb = smem_u32(xbase + (c & 1) * 2 * Gm::XTile);
+        const uint64_t wst = ad0 + (uint64_t)((st * Gm::Stage) >> 4);
+        const uint64_t xb = bd0 + (uint64_t)(((c & 1) * 2 * Gm::XTile) >> 4);
 #pragma unroll
         for (int mi = 0; mi < kTiles; ++mi)
 #pragma unroll
           for (int ks = 0; ks < kWoK / 16; ++ks) {
             // A = W^T of columns 128 mi .. + 127 (two 64-column boxes LBO
             // apart, 8-row k groups 1024 bytes apart), chunk rows 16 ks .. + 15
-            const uint64_t ad = sdesc(wst + 2 * mi * kWoBoxBytes + ks * 2048, kWoBoxBytes, 1024);
+            const uint64_t ad = wst + (uint64_t)((2 * mi * kWoBoxBytes + ks * 2048) >> 4);
             // B = [hi; lo] rows, k 16 ks .. + 15: 32 bytes into each 128-byte row
-            const uint64_t bd = sdesc(xb + ks * 32, 16, 1024);
+            const uint64_t bd = xb + (uint64_t)((ks * 32) >> 4);
             mma_ss(tmem + (uint32_t)(mi * kN), ad, bd, kIdesc, (c > 0 || ks > 0) ? 1u : 0u);
           }
         tc_commit(&done[st]);       // the stage may be refilled once these MMAs completed
         tc_commit(&xfree[c & 1]);   // and X[c % 2] rewritten
-        ++mmas;
-        // refill the previous chunk's stage: its o box was converted (its xfull
-        // was waited for) and its W is read once its MMAs are done
-        if (c >= 1 && issued < nch) {
-          const int pc = c - 1;
-          if (!wo_wait(&done[pc % kWoStages], (pc / kWoStages) & 1, abort)) break;
-          issue(issued, true, true);
-          ++issued;
-        }
       }
-      // every MMA complete before the accumulators are read (and released);
-      // the copies still in flight land before the CTA exits
+      // every MMA complete before the accumulators are read (and released)
       tc_commit(&fin);
       (void)mbar_wait(&fin, 0);
-      for (int c = max(issued - kWoStages, mmas); c < issued; ++c)
-        (void)mbar_wait(&full[c % kWoStages], (c / kWoStages) & 1);
       if (*abort) set_err(p.hdr, PA_ERRF_WAIT_TIMEOUT);
     }
     __syncwarp();
@@ -251,25 +266,26 @@ __global__ void __launch_bounds__(kWoThreads, 1) wo_kernel(const WoParams p,
   }
   __syncthreads();   // the MMA thread has seen `fin`
   tc_fence_after();
-  if (!*abort) {
+  if (!*abort && warp < 4) {
     // warp w reads tensor-memory lanes 32 w .. + 31: W columns n0 + 128 mi + 32 w + lane;
     // column r of the tile is token row r of hi, column kRows + r of lo
 #pragma unroll 1
     for (int mi = 0; mi < kTiles; ++mi) {
       const int n = n0 + 128 * mi + 32 * warp + lane;
       const uint32_t ta = tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(mi * kN);
+      constexpr int kStep = kRows % 32 == 0 ? 32 : 16;   // rows per tensor-memory load
 #pragma unroll 1
-      for (int r0 = 0; r0 < kRows; r0 += 16) {
-        float h[16], l[16];
+      for (int r0 = 0; r0 < kRows; r0 += kStep) {
+        float h[kStep], l[kStep];
         if (nch > 0) {   // warp-uniform
-          tmem_ld16(ta + r0, h);
-          tmem_ld16(ta + kRows + r0, l);
+          tmem_ldn<kStep>(ta + r0, h);
+          tmem_ldn<kStep>(ta + kRows + r0, l);
         } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) h[j] = l[j] = 0.f;
+          for (int j = 0; j < kStep; ++j) h[j] = l[j] = 0.f;
         }
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < kStep; ++j) {
           const int m = m0 + r0 + j;
           if (m >= p.M || n >= p.N) continue;
           const float v = h[j] + l[j];
