@@ -307,11 +307,37 @@ __global__ void __launch_bounds__(kWoThreads, 1) wo_kernel(const WoParams p,
   }
 }
 
-// y = sum over splits of the partials, in split order
+// y = sum over splits of the partials, in split order; four consecutive
+// elements per thread (all of a thread's loads in flight at once) where the
+// buffers allow it, the rest one element per thread
 __global__ void wo_reduce_kernel(const WoParams p) {
   griddep_wait();
   const size_t total = (size_t)p.M * p.N;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+  // vector accesses only where every split's block and y are aligned for them
+  const bool vec = total % 4 == 0 && reinterpret_cast<uintptr_t>(p.part) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(p.y) % (p.y_fp32 ? 16 : 8) == 0;
+  const size_t n4 = vec ? total / 4 : 0;
+  for (size_t i4 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i4 < n4;
+       i4 += (size_t)gridDim.x * blockDim.x) {
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < p.splits; ++s) {
+      const float4 x = reinterpret_cast<const float4 *>(p.part + (size_t)s * total)[i4];
+      v.x += x.x;
+      v.y += x.y;
+      v.z += x.z;
+      v.w += x.w;
+    }
+    if (p.y_fp32) {
+      reinterpret_cast<float4 *>(p.y)[i4] = v;
+    } else {
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+      uint2 w;
+      w.x = *reinterpret_cast<const uint32_t *>(&lo);
+      w.y = *reinterpret_cast<const uint32_t *>(&hi);
+      reinterpret_cast<uint2 *>(p.y)[i4] = w;
+    }
+  }
+  for (size_t i = 4 * n4 + (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (size_t)gridDim.x * blockDim.x) {
     float v = 0.f;
     for (int s = 0; s < p.splits; ++s) v += p.part[(size_t)s * total + i];
@@ -395,7 +421,7 @@ cudaError_t launch_wo(const float *o, int M, int K, const void *w, int N, int sp
                               : launch_mt<1>(p, grid, o, tw, s);
   if (e != cudaSuccess || splits == 1) return e;
   const size_t total = (size_t)M * N;
-  const unsigned rgrid = (unsigned)std::min<size_t>((total + 255) / 256, 2048);
+  const unsigned rgrid = (unsigned)std::min<size_t>((total / 4 + 255) / 256 + 1, 2048);
   return launch_pdl(wo_reduce_kernel, rgrid, 256, 0, s, p);
 }
 
