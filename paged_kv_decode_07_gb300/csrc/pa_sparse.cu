@@ -135,7 +135,10 @@ __global__ void __launch_bounds__(512) means_kernel(const KvView kv, const int *
 // mean rows, so the four groups of a load instruction read four whole
 // 128-byte lines (coalesced); every query float4 read from shared memory
 // serves both blocks, and the eight partial dots of each head are added by
-// three shuffles.
+// three shuffles.  The mean rows are read with the streaming (evict-first)
+// cache hint: they are read once per step and would otherwise push out of L2
+// what the kernels after them reuse (decode step 0.154 -> 0.142 ms at
+// 8 x 262K).
 constexpr int kScoreThreads = 128;
 constexpr int kScoreCta = kScoreThreads;   // blocks per CTA
 
@@ -177,7 +180,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(
       const float4 *m = reinterpret_cast<const float4 *>(means + (((size_t)b * max_nsb + j) * H + h) * D);
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        x[u][i] = (i < per && j < nsb) ? m[l8 + 8 * i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        x[u][i] = (i < per && j < nsb) ? __ldcs(&m[l8 + 8 * i]) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
