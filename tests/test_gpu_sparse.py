@@ -208,3 +208,30 @@ def test_selection_with_negative_and_mixed_sign_scores():
                                      np.array(_nsb([1280, 1280]), np.int32), k)
     assert (scores[1, :, :20] < 0).all() and (scores[0, :, :20] > 0).any()
     check_selection(sel.cpu().numpy(), scores, _nsb([1280, 1280]), k, "mixed signs")
+
+
+@pytest.mark.parametrize("dt,Hq,Hkv,D", [("int8", 8, 2, 128), ("nvfp4", 8, 4, 128),
+                                         ("bf16", 8, 8, 256)])
+def test_sparse_other_head_shapes(dt, Hq, Hkv, D):
+    """Head dim 128 (half the float4 per lane in the score kernel) and group
+    sizes 4, 2 and 1."""
+    lens = [2000, 65, 640, 1]
+    wl = W.make_workload(NAMES[dt], device=DEV, seq_lens=lens, Hq=Hq, Hkv=Hkv, D=D)
+    nsb = _nsb(lens)
+    M = max(nsb)
+    means = _means(wl, M)
+    kv = pa.KvCache.from_workload(wl)
+    top_k = 5
+    o, lse, sel, ws = pa.decode_sparse(kv, wl.q, wl.block_tables, wl.seq_lens, wl.softmax_scale,
+                                       means, SB, top_k, out_fp32=True, return_lse=True,
+                                       return_selected=True)
+    torch.cuda.synchronize()
+    assert pa.read_error(ws) == 0
+    sel = sel.cpu().numpy()
+    cache, tab, lens_h, qb = compact_host(wl, list(range(wl.B)))
+    ref_means = oracle.block_means(cache, tab, lens_h, SB, M)
+    scores, _ = oracle.sparse_select(qb, wl.Hkv, ref_means, np.array(nsb, np.int32), top_k)
+    check_selection(sel, scores, nsb, top_k, f"{dt} Hq={Hq} Hkv={Hkv} D={D}")
+    ref_o, ref_l = oracle.attend_sparse(cache, qb, tab, lens_h, sel, SB, wl.softmax_scale)
+    compare(o, ref_o, f"sparse {dt} D={D}")
+    compare_lse(lse, ref_l, f"sparse {dt} D={D}")
