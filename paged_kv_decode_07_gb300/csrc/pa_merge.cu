@@ -27,13 +27,14 @@ __device__ __forceinline__ void store4(void *out, int out_fp32, size_t off, floa
 
 // Merges `parts` partials of one row with one CTA of kThreads threads.
 // po points at partial 0 of the row, consecutive partials `pstride` floats
-// apart; pl likewise with lstride.  The weights exp(lse_p - M) are computed
-// once per partial into shared memory (chunks of kChunk).  The threads form
-// kThreads / (D / 4) groups, each thread owning one float4 column: group k
-// accumulates partials k, k + groups, ... (four loads in flight per step),
-// so a row with hundreds of partials (a 262K-key sequence split into
-// partitions) is read by the whole CTA at once; the groups' sums are then
-// added in fixed order.
+// apart; pl likewise with lstride.  The lse values are read once (kept in
+// shared memory for the first kChunk partials) and the weights
+// exp(lse_p - M) computed once per partial into shared memory (chunks of
+// kChunk).  The threads form kThreads / (D / 4) groups, each thread owning
+// one float4 column: group k accumulates partials k, k + groups, ... (eight
+// loads in flight per step), so a row with hundreds of partials (a 262K-key
+// sequence split into partitions) is read by the whole CTA at once; the
+// groups' sums are then added in fixed order.
 constexpr int kThreads = 256;
 constexpr int kChunk = 512;
 
@@ -41,12 +42,17 @@ __device__ void merge_row(const float *po, size_t pstride, const float *pl, size
                           int parts, int D, void *out, int out_fp32, size_t out_off,
                           float *lse_out, size_t lse_off) {
   __shared__ float s_w[kChunk];
+  __shared__ float s_l[kChunk];   // lse of the first kChunk partials
   __shared__ float s_red[kThreads / 32];
   __shared__ float s_M;
   __shared__ float4 s_acc[kThreads];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   float M = kNegInf;
-  for (int q = tid; q < parts; q += kThreads) M = fmaxf(M, pl[(size_t)q * lstride]);
+  for (int q = tid; q < parts; q += kThreads) {
+    const float l = pl[(size_t)q * lstride];
+    if (q < kChunk) s_l[q] = l;
+    M = fmaxf(M, l);
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   if (lane == 0) s_red[warp] = M;
@@ -74,21 +80,22 @@ __device__ void merge_row(const float *po, size_t pstride, const float *pl, size
     const int n = min(kChunk, parts - q0);
     __syncthreads();
     for (int q = tid; q < n; q += kThreads) {
-      const float l = pl[(size_t)(q0 + q) * lstride];
+      const float l = q0 == 0 ? s_l[q] : pl[(size_t)(q0 + q) * lstride];
       s_w[q] = (l == kNegInf) ? 0.f : __expf(l - M);
     }
     __syncthreads();
-    for (int q = 0; q < n; ++q) wsum += s_w[q];
+    if (grp == 0 || tid == 0)   // the threads that write the row or its lse
+      for (int q = 0; q < n; ++q) wsum += s_w[q];
     if (!active) continue;
     const float *base = po + (size_t)q0 * pstride + 4 * col;
     int q = grp;
-    for (; q + 3 * groups < n; q += 4 * groups) {
-      float4 v[4];
+    for (; q + 7 * groups < n; q += 8 * groups) {
+      float4 v[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < 8; ++u)
         v[u] = *reinterpret_cast<const float4 *>(base + (size_t)(q + u * groups) * pstride);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 8; ++u) {
         const float w = s_w[q + u * groups];
         if (w != 0.f) {   // an empty partial may hold anything
           acc.x += w * v[u].x;
