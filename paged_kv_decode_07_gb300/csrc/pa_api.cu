@@ -1,6 +1,7 @@
 // pa_api.cu -- host side of the C ABI declared in include/pa.h: argument
 // validation (errors return before anything is launched), workspace layout,
 // and the planner -> attention kernel -> merge launch sequence.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 
@@ -32,6 +33,36 @@ cudaError_t launch_decode_tc_cluster(const AttnParams &p, int P, cudaStream_t s)
     case PA_KV_FP8: return launch_decode_tc_cluster_fp8(p, P, s);
   }
   return cudaErrorInvalidValue;
+}
+
+int decode_tc_occupancy_bf16(int D, int R);
+int decode_tc_occupancy_int8(int D, int R);
+int decode_tc_occupancy_nvfp4(int D, int R);
+int decode_tc_occupancy_fp8(int D, int R);
+
+// CTAs of the tensor-core decode kernel one SM holds at once, 0 if unknown;
+// queried once per (device, format, head dim, rows) and kept
+int decode_tc_occupancy(int dtype, int D, int R) {
+  constexpr int kDevs = 16;
+  static std::atomic<int> known[kDevs][4][2][kMaxG + 1];   // occupancy + 1, 0 = not yet asked
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dtype < PA_KV_BF16 || dtype > PA_KV_FP8 || R < 1 || R > kMaxG || (D != 128 && D != 256))
+    return 0;
+  std::atomic<int> *slot = dev >= 0 && dev < kDevs ? &known[dev][dtype][D == 256][R] : nullptr;
+  if (slot) {
+    const int v = slot->load(std::memory_order_relaxed);
+    if (v > 0) return v - 1;
+  }
+  int n = 0;
+  switch (dtype) {
+    case PA_KV_BF16: n = decode_tc_occupancy_bf16(D, R); break;
+    case PA_KV_INT8: n = decode_tc_occupancy_int8(D, R); break;
+    case PA_KV_NVFP4: n = decode_tc_occupancy_nvfp4(D, R); break;
+    case PA_KV_FP8: n = decode_tc_occupancy_fp8(D, R); break;
+  }
+  if (slot && n > 0) slot->store(n + 1, std::memory_order_relaxed);
+  return n;
 }
 
 cudaError_t launch_decode_tc(const AttnParams &p, int grid, cudaStream_t s) {
@@ -108,6 +139,8 @@ namespace {
 
 constexpr int kVersion = 100;
 constexpr int kMinSplitBlocks = 8;       // partitions never shorter than 128 tokens (auto mode)
+constexpr int kItemCostDecode = 16;      // fixed cost of a work item in key blocks (planner)
+constexpr int kItemCostVerify = 32;
 // single-launch decode: at most 8 CTAs per cluster (the portable limit), a
 // CTA's 4 warps taking up to 2 blocks each in auto mode, and the whole grid
 // resident at once (one CTA per SM)
@@ -345,14 +378,27 @@ int run_attention(const pa_kv_cache *kv, const pa_problem *p, const pa_options *
   // persistent tcgen05 verify kernel pays a fixed cost per item (its q tile,
   // epilogue and first-tile rescale), so it gets about 2 per SM
   int auto_target = kDefaultTargetItems;
-  if (umma) {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
-      auto_target = std::min(2 * sms, kMaxTargetItems);
-  }
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 0;
+  if (umma && sms > 0) auto_target = std::min(2 * sms, kMaxTargetItems);
   pp.target_items = (o && o->target_items > 0) ? std::min(o->target_items, kMaxTargetItems)
                                                : auto_target;
+  // resident CTAs of the attention kernel (the planner rounds equal-length
+  // batches to whole rounds of them): one persistent CTA per SM for the
+  // tcgen05 verify, the occupancy of the one-CTA-per-item decode kernel.
+  // The fixed cost of an item, in key blocks streamed, from sweeps of the
+  // item count on equal-length batches: decode (q load, first copies,
+  // partial write, merge share) about 16, the tcgen05 verify (its q tile,
+  // epilogue and first-tile rescale between items) about 32.
+  if (sms > 0 && umma) {
+    pp.resident = sms;
+    pp.item_cost = kItemCostVerify;
+  } else if (sms > 0 && use_tc && !dense) {
+    pp.resident = sms * decode_tc_occupancy(kv->dtype, kv->head_dim, L.R);
+    pp.item_cost = kItemCostDecode;
+  }
   pp.split_blocks = o ? o->split_blocks : 0;
   pp.min_split_blocks = kMinSplitBlocks;
   pp.max_items = L.max_items;

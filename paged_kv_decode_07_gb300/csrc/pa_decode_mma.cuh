@@ -930,6 +930,29 @@ cudaError_t launch_cluster_dtype(const AttnParams &p, int P, cudaStream_t s) {
   return cudaErrorInvalidValue;
 }
 
+// CTAs of decode_kernel<DT, D, R> one SM holds at once (0 if unknown)
+template <int DT, int D, int R>
+int occupancy_one() {
+  using Gm = Geo<DT, D>;
+  auto kern = decode_kernel<DT, D, R>;
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, Gm::SMEM) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+template <int DT>
+int occupancy_dtype(int D, int R) {
+#define PA_TC_CASE(DD, RR) \
+  if (D == DD && R == RR) return occupancy_one<DT, DD, RR>();
+  PA_TC_CASE(128, 1) PA_TC_CASE(128, 2) PA_TC_CASE(128, 4) PA_TC_CASE(128, 6)
+  PA_TC_CASE(128, 8) PA_TC_CASE(256, 1) PA_TC_CASE(256, 2) PA_TC_CASE(256, 4)
+  PA_TC_CASE(256, 6) PA_TC_CASE(256, 8)
+#undef PA_TC_CASE
+  return 0;
+}
+
 template <int DT>
 cudaError_t launch_dtype(const AttnParams &p, int grid, cudaStream_t s) {
   const int D = p.kv.D, R = p.R;

@@ -31,6 +31,7 @@ enum : int {
   HDR_NUM_ITEMS = 1,   // work items planned
   HDR_SPLIT = 2,       // blocks per partition chosen by the planner
   HDR_NUM_SLOTS = 3,   // partial slots used
+  HDR_ROUND = 4,       // resident CTAs the item count was rounded to (0: not rounded)
 };
 
 // KV pool as the kernels see it
@@ -91,6 +92,11 @@ struct PlanParams {
   int capacity;             // 16 * stride
   int target_items, split_blocks, min_split_blocks;
   int max_items, max_slots;
+  // CTAs of the attention kernel resident at once on the whole GPU (SMs x
+  // CTAs per SM), or 0: with equal-length sequences the planner then makes
+  // the item count a whole number of such rounds; item_cost is the fixed
+  // cost of one item in key blocks streamed, which sets how many rounds
+  int resident, item_cost;
   uint32_t *hdr;
   WorkItem *items;
   UnitInfo *units;

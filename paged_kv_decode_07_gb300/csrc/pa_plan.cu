@@ -12,8 +12,12 @@
 //   units[u]  = {parts, slot_base, nblk, len}
 //   items[j]  = {unit, kvh, blk_begin, blk_end, part, parts, slot}
 // Partition size W (blocks) = max(min_split, ceil(total_blocks * Hkv /
-// target_items)) unless fixed by the caller; parts_u = ceil(nblk_u / W);
-// blocks are split evenly, ceil(nblk_u / parts_u) per part (never empty).
+// target_items)) unless fixed by the caller; when every sequence has the
+// same length, W then grows until the item count is a whole number of
+// rounds of the attention kernel's resident CTAs (the number of rounds from
+// a cost model: a round costs its items' blocks plus a fixed cost per item).  parts_u = ceil(nblk_u /
+// W); blocks are split evenly, ceil(nblk_u / parts_u) per part (never
+// empty).
 // Items of multi-part units come first (they are about W blocks each), then
 // the single-part ones (shorter), a longest-first order for the hardware's
 // in-order CTA dispatch.
@@ -110,7 +114,8 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
   __shared__ unsigned long long s_total;
   __shared__ uint32_t s_err;
   __shared__ int2 s_tot;
-  __shared__ int s_W;
+  __shared__ int s_W, s_round;
+  __shared__ int s_gmin, s_gmax;   // least / most blocks of a group's partition basis
   __shared__ int s_pa[kSmemGroups], s_pb[kSmemGroups];         // item prefix per group
   __shared__ int s_parts[kSmemGroups], s_nblk[kSmemGroups], s_slot[kSmemGroups];
   griddep_launch();   // the attention kernel may launch now; it waits for this grid to finish
@@ -119,6 +124,9 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
   if (tid == 0) {
     s_total = 0;
     s_err = 0;
+    s_round = 0;
+    s_gmin = 0x7fffffff;
+    s_gmax = 0;
   }
   __syncthreads();
 
@@ -134,8 +142,29 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
     int n = unit_len(p, u, err);
     tot += (unsigned long long)((n + kBlock - 1) / kBlock);
   }
-  for (int o = 16; o > 0; o >>= 1) tot += __shfl_down_sync(0xffffffffu, tot, o);
-  if ((tid & 31) == 0) atomicAdd(&s_total, tot);
+  // the blocks every group partitions (those of its longest unit): the same
+  // in every group when the sequences have equal lengths
+  int gmin = 0x7fffffff, gmax = 0;
+  if (p.resident > 0 && p.split_blocks <= 0) {
+    uint32_t e1 = 0;
+    for (int g = tid; g < NG; g += kThreads) {
+      int nmax = 0;
+      for (int i = 0; i < GS; ++i) nmax = max(nmax, unit_len(p, g * GS + i, e1));
+      const int nb = (nmax + kBlock - 1) / kBlock;
+      gmin = min(gmin, nb);
+      gmax = max(gmax, nb);
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    tot += __shfl_down_sync(0xffffffffu, tot, o);
+    gmin = min(gmin, __shfl_down_sync(0xffffffffu, gmin, o));
+    gmax = max(gmax, __shfl_down_sync(0xffffffffu, gmax, o));
+  }
+  if ((tid & 31) == 0) {
+    atomicAdd(&s_total, tot);
+    atomicMin(&s_gmin, gmin);
+    atomicMax(&s_gmax, gmax);
+  }
   if (err) atomicOr(&s_err, err);
   __syncthreads();
   if (tid == 0) {
@@ -146,6 +175,33 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
       long long work = (long long)s_total * p.hkv;
       W = (work + p.target_items - 1) / p.target_items;
       if (W < p.min_split_blocks) W = p.min_split_blocks;
+      // Equal-length groups give items of one size, and the kernel then takes
+      // as long as the rounds of resident CTAs its items fill: a last round
+      // that is only partly full costs a whole round, and every item adds a
+      // fixed cost.  Over k = 1 .. the rounds the target's item count fills
+      // completely, with parts_k = the most partitions per unit that fit k
+      // rounds, the partitions take the k of least k * (nb / parts_k + c).
+      const int nb = s_gmax;
+      if (p.resident > 0 && nb > 0 && s_gmin == nb) {
+        const long long per = (long long)NG * GS * p.hkv;   // items per partition index
+        const long long items0 = per * ((nb + W - 1) / W);
+        const long long kmax = items0 / p.resident;
+        long long best_w = 0, best_t = 0;
+        for (long long k = 1; k <= kmax; ++k) {
+          const long long parts = k * p.resident / per;
+          if (parts < 1) continue;
+          const long long wk = (nb + parts - 1) / parts;
+          const long long t = k * (wk + p.item_cost);
+          if (best_w == 0 || t < best_t) {
+            best_w = wk;
+            best_t = t;
+          }
+        }
+        if (best_w > 0) {
+          W = max(W, best_w);
+          s_round = p.resident;
+        }
+      }
     }
     if (W < 1) W = 1;
     if (W > (1 << 30)) W = 1 << 30;
@@ -253,6 +309,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
     p.hdr[HDR_NUM_ITEMS] = (uint32_t)num_items;
     p.hdr[HDR_SPLIT] = (uint32_t)W;
     p.hdr[HDR_NUM_SLOTS] = (uint32_t)slots;
+    p.hdr[HDR_ROUND] = (uint32_t)s_round;
   }
 }
 

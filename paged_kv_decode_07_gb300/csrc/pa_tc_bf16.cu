@@ -9,4 +9,5 @@ cudaError_t launch_decode_tc_bf16(const AttnParams &p, int grid, cudaStream_t s)
 cudaError_t launch_decode_tc_cluster_bf16(const AttnParams &p, int P, cudaStream_t s) {
   return tc::launch_cluster_dtype<PA_KV_BF16>(p, P, s);
 }
+int decode_tc_occupancy_bf16(int D, int R) { return tc::occupancy_dtype<PA_KV_BF16>(D, R); }
 }  // namespace pa

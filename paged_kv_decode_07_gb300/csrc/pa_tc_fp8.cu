@@ -10,4 +10,5 @@ cudaError_t launch_decode_tc_fp8(const AttnParams &p, int grid, cudaStream_t s) 
 cudaError_t launch_decode_tc_cluster_fp8(const AttnParams &p, int P, cudaStream_t s) {
   return tc::launch_cluster_dtype<PA_KV_FP8>(p, P, s);
 }
+int decode_tc_occupancy_fp8(int D, int R) { return tc::occupancy_dtype<PA_KV_FP8>(D, R); }
 }  // namespace pa

@@ -10,4 +10,5 @@ cudaError_t launch_decode_tc_int8(const AttnParams &p, int grid, cudaStream_t s)
 cudaError_t launch_decode_tc_cluster_int8(const AttnParams &p, int P, cudaStream_t s) {
   return tc::launch_cluster_dtype<PA_KV_INT8>(p, P, s);
 }
+int decode_tc_occupancy_int8(int D, int R) { return tc::occupancy_dtype<PA_KV_INT8>(D, R); }
 }  // namespace pa

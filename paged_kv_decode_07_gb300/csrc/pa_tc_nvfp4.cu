@@ -10,4 +10,5 @@ cudaError_t launch_decode_tc_nvfp4(const AttnParams &p, int grid, cudaStream_t s
 cudaError_t launch_decode_tc_cluster_nvfp4(const AttnParams &p, int P, cudaStream_t s) {
   return tc::launch_cluster_dtype<PA_KV_NVFP4>(p, P, s);
 }
+int decode_tc_occupancy_nvfp4(int D, int R) { return tc::occupancy_dtype<PA_KV_NVFP4>(D, R); }
 }  // namespace pa

@@ -392,6 +392,8 @@ def read_error(workspace: torch.Tensor, stream=None) -> int:
 
 
 def header(workspace: torch.Tensor):
-    """(err, num_items, split_blocks, slots) from the workspace header."""
-    h = workspace[:16].view(torch.int32).cpu().tolist()
-    return tuple(h[:4])
+    """(err, num_items, split_blocks, slots, resident) from the workspace
+    header; resident is the count of CTAs the planner rounded the items to
+    (0 when it did not round)."""
+    h = workspace[:32].view(torch.int32).cpu().tolist()
+    return tuple(h[:5])

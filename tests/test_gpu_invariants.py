@@ -5,6 +5,7 @@ flag in the workspace header).
 * physical-block permutation gives bitwise-identical output;
 * run-to-run bitwise determinism (no float atomics);
 * forced single partition, forced tiny partitions and auto agree;
+* equal-length batches are planned in whole rounds of resident CTAs;
 * padded rows (seq_len 0) give 0 and lse -inf;
 * an out-of-range block id is skipped and flagged; a length beyond the
   table's capacity is clamped and flagged; verify rows shorter than q_len
@@ -61,6 +62,41 @@ def test_split_settings_agree(dt, kernel):
         compare(o, ref, f"{dt} {tag}")
     assert pa.header(ws1)[3] == 0            # no partial slots when nothing splits
     assert pa.header(ws2)[3] > 0
+
+
+# the library's item target and shortest partition in auto mode: the plan
+# before any rounding
+DEFAULT_TARGET, MIN_SPLIT = 1184, 8
+
+
+@pytest.mark.parametrize("dt", ["int8", "nvfp4"])
+def test_equal_lengths_fill_whole_rounds(dt):
+    """Equal-length sequences: the planner grows the partitions until the
+    items fill whole rounds of the decode kernel's resident CTAs (no more
+    rounds than the unrounded plan fills completely, each as full as the
+    partition granularity allows); one sequence a block shorter keeps the
+    unrounded plan.  Results stay those of the oracle."""
+    L = 32768
+    wl = W.make_workload(NAMES[dt], device=DEV, seq_lens=[L] * 4)
+    o, ws = run(wl, out_fp32=True)
+    _, n_items, split, _, res = pa.header(ws)
+    per = wl.B * wl.Hkv                        # items per partition index
+    nb = L // 16
+    w0 = max(MIN_SPLIT, -(-nb * per // DEFAULT_TARGET))
+    items0 = per * -(-nb // w0)
+    assert res > 0 and items0 > res, (res, items0)
+    assert n_items == per * -(-nb // split)
+    assert n_items <= items0 // res * res, (n_items, items0, res)
+    rounds = -(-n_items // res)
+    assert rounds * res - per < n_items, (n_items, rounds, res, per)
+    ref, _ = oracle_rows(wl, bs=[0, 3])
+    compare(o[[0, 3]], ref, f"{dt} rounded plan")
+
+    wl2 = W.make_workload(NAMES[dt], device=DEV, seq_lens=[L] * 3 + [L - 16])
+    _, ws2 = run(wl2, out_fp32=True)
+    h2 = pa.header(ws2)
+    assert h2[4] == 0
+    assert h2[2] == max(MIN_SPLIT, -(-(4 * nb - 1) * wl.Hkv // DEFAULT_TARGET))
 
 
 def test_padded_rows_zero_and_neg_inf():
