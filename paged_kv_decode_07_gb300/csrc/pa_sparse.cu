@@ -19,6 +19,9 @@
 // changes.  Only the sequence's last sparse block can be partial, and it
 // sorts last, so every virtual sequence is whole 16-token blocks but its
 // last.
+#include <algorithm>
+#include <atomic>
+
 #include "pa_internal.cuh"
 
 namespace pa {
@@ -130,8 +133,9 @@ __global__ void __launch_bounds__(512) means_kernel(const KvView kv, const int *
 }
 
 // Eight lanes per sparse block, two blocks per lane group: a CTA of 128
-// threads scores 128 consecutive blocks of one (b, h), eight blocks per warp
-// step.  Lane l8 of a group reads float4 l8, l8 + 8, ... of its two blocks'
+// threads scores a run of consecutive blocks of one (b, h), 32 per step of
+// its four warps; the runs are as long as makes the grid one round of the
+// GPU's resident CTAs.  Lane l8 of a group reads float4 l8, l8 + 8, ... of its two blocks'
 // mean rows, so the four groups of a load instruction read four whole
 // 128-byte lines (coalesced); every query float4 read from shared memory
 // serves both blocks, and the eight partial dots of each head are added by
@@ -140,14 +144,14 @@ __global__ void __launch_bounds__(512) means_kernel(const KvView kv, const int *
 // what the kernels after them reuse (decode step 0.154 -> 0.142 ms at
 // 8 x 262K).
 constexpr int kScoreThreads = 128;
-constexpr int kScoreCta = kScoreThreads;   // blocks per CTA
 
+// per_cta: blocks per CTA, a multiple of 8 (a warp step's blocks)
 template <int G>
 __global__ void __launch_bounds__(kScoreThreads) score_kernel(
     const __nv_bfloat16 *q, int Hq, const int *seq_lens, int capacity, int B, int H, int D,
-    int sb, int max_nsb, const float *means, float *scores) {
+    int sb, int max_nsb, int per_cta, const float *means, float *scores) {
   __shared__ float4 sq[G][256 / 4];
-  const int chunks = (max_nsb + kScoreCta - 1) / kScoreCta;
+  const int chunks = (max_nsb + per_cta - 1) / per_cta;
   const int c = blockIdx.x % chunks;
   const int h = (blockIdx.x / chunks) % H;
   const int b = blockIdx.x / (chunks * H);
@@ -164,9 +168,10 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sub = lane >> 3, l8 = lane & 7;
   const int per = D / 32;   // float4 of a row per lane
-  for (int step = 0; step < kScoreCta / 32; ++step) {
-    const int j0 = c * kScoreCta + step * 32 + warp * 8;   // the warp's first block
-    if (j0 >= max_nsb) break;                               // the whole warp
+  const int j_end = min(max_nsb, (c + 1) * per_cta);
+  for (int step = 0; step * 32 < per_cta; ++step) {
+    const int j0 = c * per_cta + step * 32 + warp * 8;   // the warp's first block
+    if (j0 >= j_end) break;                              // the whole warp
     const int ja = j0 + sub, jb = ja + 4;                   // this group's two blocks
     float acc[2][G];
 #pragma unroll
@@ -418,20 +423,67 @@ cudaError_t launch_means(const KvView &kv, const int *tables, int stride, const 
   return cudaGetLastError();
 }
 
+// CTAs of score_kernel<G> resident on the whole GPU (SMs x CTAs per SM), 0
+// if unknown; asked once per (device, G)
+template <int G>
+static int score_occupancy() {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, score_kernel<G>, kScoreThreads, 0) !=
+      cudaSuccess)
+    return 0;
+  return n;
+}
+
+static int score_slots(int G) {
+  constexpr int kDevs = 16;
+  static std::atomic<int> known[kDevs][9];   // slots + 1, 0 = not yet asked
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || G < 1 || G > 8) return 0;
+  std::atomic<int> *slot = dev >= 0 && dev < kDevs ? &known[dev][G] : nullptr;
+  if (slot) {
+    const int v = slot->load(std::memory_order_relaxed);
+    if (v > 0) return v - 1;
+  }
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  int occ = 0;
+  switch (G) {
+    case 1: occ = score_occupancy<1>(); break;
+    case 2: occ = score_occupancy<2>(); break;
+    case 3: occ = score_occupancy<3>(); break;
+    case 4: occ = score_occupancy<4>(); break;
+    case 5: occ = score_occupancy<5>(); break;
+    case 6: occ = score_occupancy<6>(); break;
+    case 7: occ = score_occupancy<7>(); break;
+    case 8: occ = score_occupancy<8>(); break;
+  }
+  const int n = occ * sms;
+  if (slot && n > 0) slot->store(n + 1, std::memory_order_relaxed);
+  return n;
+}
+
 cudaError_t launch_sparse_select(const KvView &kv, const __nv_bfloat16 *q, int Hq,
                                  const int *tables, int stride, const int *seq_lens, int B, int sb,
                                  int max_nsb, int top_k, const float *means, float *scores,
                                  int *selected, int *vtables, int vstride, int *vlens,
                                  uint32_t *err, cudaStream_t s) {
   const int H = kv.hkv, G = Hq / H;
-  const long long grid = (long long)B * H * ((max_nsb + kScoreCta - 1) / kScoreCta);
+  if (G < 1 || G > 8) return cudaErrorInvalidValue;
+  // one round of resident CTAs: the (b, h) rows' blocks are cut into as many
+  // chunks as fill the GPU's resident CTAs once (the last of two rounds was
+  // a third full with 128 blocks per CTA: 30.7 us for 8 x 4 x 4096 blocks)
+  const long long rows = (long long)B * H;
+  const int slots = score_slots(G);
+  const long long cpr = slots > 0 ? std::max(1LL, slots / rows) : 1LL;
+  int per_cta = (int)((max_nsb + cpr - 1) / cpr);
+  per_cta = std::max(8, (per_cta + 7) / 8 * 8);
+  const long long grid = rows * ((max_nsb + per_cta - 1) / per_cta);
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int cap = stride * kBlock;
 #define PA_SCORE_CASE(GG)                                                                    \
   case GG:                                                                                   \
     score_kernel<GG><<<(unsigned)grid, kScoreThreads, 0, s>>>(q, Hq, seq_lens, cap, B, H,    \
-                                                              kv.D, sb, max_nsb, means,      \
-                                                              scores);                       \
+                                                              kv.D, sb, max_nsb, per_cta,    \
+                                                              means, scores);                \
     break;
   switch (G) {
     PA_SCORE_CASE(1) PA_SCORE_CASE(2) PA_SCORE_CASE(3) PA_SCORE_CASE(4)
