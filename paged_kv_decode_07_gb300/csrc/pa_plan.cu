@@ -185,7 +185,9 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(PlanParams p) {
       if (p.resident > 0 && nb > 0 && s_gmin == nb) {
         const long long per = (long long)NG * GS * p.hkv;   // items per partition index
         const long long items0 = per * ((nb + W - 1) / W);
-        const long long kmax = items0 / p.resident;
+        // at most 64 rounds are weighed: past that a partial round costs
+        // under 2 % (and thread 0 stays quick for very large batches)
+        const long long kmax = min(items0 / p.resident, 64LL);
         long long best_w = 0, best_t = 0;
         for (long long k = 1; k <= kmax; ++k) {
           const long long parts = k * p.resident / per;
